@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark: paged FP8 decode attention on the Llama-3.1-8B-shaped layer.
+
+One step = one decode step of one attention layer through the C ABI:
+kv_append of the new token (B=32 x Hkv=8 rows quantised into e4m3 page slots)
+then paged_decode_attn (tag validation, split-KV attention, combine) over
+lengths ~ U[512, 8192] + 1, Hq=32, Hkv=8, head_dim 128, 16-token pages
+scattered over a 65,536-page pool.  Steps rotate over R independent layer
+replicas (each its own pool, tables and query) so that the live KV read by a
+step (~286 MB; R x that in total) is never resident in the 129 MB L2.
+
+Reported (one JSON line on rank 0):
+  value        KV GB/s of the whole job: algorithmic bytes of the step (KV +
+               tables + scales + tags + q + out + flags + appended rows) per
+               second, summed over ranks
+  tokens_per_s decode tokens/s of a 32-layer model whose every layer is this
+               layer: ranks x B / (32 x step time)
+  roofline     decode_split (the dominant kernel) timed live with CUDA events
+               around its stage launch, against MEASURED_PEAKS.json hbm_gbs
+  e2e          the same metric with the step's inputs copied from pinned host
+               memory and its result read back inside the timed region
+  cpu_baseline the oracle (test infrastructure) on a bounded sample, host cores
+
+--impl reference times the oracle alone (CPU), as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV GB/s (Llama-3.1-8B-shaped FP8 layer, append + attend)"
+UNIT = "GB/s"
+WORKLOAD = "llama8b-fp8-decode-layer"
+N_LAYERS = 32  # Llama-3.1-8B layer count, for tokens/s
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="pfkv", choices=["pfkv", "reference"])
+    ap.add_argument("--replicas", type=int, default=8)
+    ap.add_argument("--split", type=int, default=0, help="split-KV tokens (0 = library choice)")
+    ap.add_argument("--no-tags", action="store_true", help="no-op tracker (no tag validation)")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# multi-rank helpers (pure host logic; covered by a gloo test)
+# --------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base: int, rank: int, replica: int) -> int:
+    """Every (rank, replica) draws its own batch: same shapes, own data."""
+    return base + 1000 * rank + replica
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(bytes_per_step_per_rank: float, steps: int, seconds_max: float, world: int) -> float:
+    """Whole-job GB/s: every rank moved bytes_per_step per step; the job took
+    the slowest rank's time."""
+    return bytes_per_step_per_rank * steps * world / seconds_max / 1e9
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path, self.proc = path, None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        return self.summary()
+
+    def summary(self):
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        load = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in load),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(load), "power_w_max": max(r[2] for r in rows)}
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+class PreparedStep:
+    """The C-ABI calls of one step with their argument structs built once."""
+
+    def __init__(self, db, B, stream_handle):
+        self.db, self.B, self.s = db, B, stream_handle
+        L = B.lib()
+        self.L = L
+        self.c = db.cache.c_struct()
+        self.p = db.pages.c_struct()
+        ws = db.workspace
+        self.args = (ctypes.byref(self.c), ctypes.byref(self.p), db.q.data_ptr(), db.spec.Hq,
+                     ctypes.c_float(db.spec.sm_scale), db.split_tokens, db.max_seq_len,
+                     ws.data_ptr(), ws.numel(), db.out.data_ptr(), db.flags.data_ptr())
+        self.append_args = None
+        if db.spec.append:
+            self.append_args = (ctypes.byref(self.c), ctypes.byref(self.p), db.positions.data_ptr(),
+                                None, 1, db.k_new.data_ptr(), db.v_new.data_ptr(),
+                                db.append_flags.data_ptr(), stream_handle)
+
+    def append(self):
+        if self.append_args is not None:
+            st = self.L.pfkv_kv_append(*self.append_args)
+            if st:
+                raise RuntimeError(f"pfkv_kv_append: status {st}")
+
+    def stage(self, mask):
+        st = self.L.pfkv_paged_decode_attn_stages(*self.args, mask, self.s)
+        if st:
+            raise RuntimeError(f"pfkv_paged_decode_attn_stages: status {st}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_fp8_kv_decode_gb300 import binding as B
+    from paged_fp8_kv_decode_gb300 import workloads as W
+    from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
+
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    reps = []
+    for r in range(args.replicas):
+        spec = W.spec_llama8b("full", seed=rank_seed(W.BASE_SEED + 2, rank, r))
+        spec.split_tokens = args.split
+        if args.no_tags:
+            spec.tags = False
+        db = DeviceBatch(W.make_batch(spec), device=dev)
+        reps.append(PreparedStep(db, B, sh))
+    torch.cuda.synchronize()
+    spec0 = reps[0].db.spec
+    # bytes per step (same shapes in every replica; lengths differ): mean over replicas
+    attn_bytes = statistics.mean(p.db.algorithmic_bytes() for p in reps)
+    kv_bytes = statistics.mean(p.db.kv_bytes() for p in reps)
+    append_bytes = spec0.B * spec0.Hkv * spec0.D * (2 * 2 + 2 * 1) + spec0.B * spec0.Hkv * 8
+    step_bytes = attn_bytes + append_bytes
+
+    S_ALL = B.PFKV_STAGE_ALL
+    S_V, S_S, S_C = B.PFKV_STAGE_VALIDATE, B.PFKV_STAGE_SPLIT, B.PFKV_STAGE_COMBINE
+
+    def one_step(p, ev=None):
+        p.append()
+        if ev is None:
+            p.stage(S_ALL)
+        else:
+            p.stage(S_V)
+            ev[0].record(stream)
+            p.stage(S_S)
+            ev[1].record(stream)
+            p.stage(S_C)
+
+    for i in range(args.warmup):
+        one_step(reps[i % len(reps)])
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler = None
+    if rank == 0 and not args.no_clocks:
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        one_step(reps[i % len(reps)], ev_split[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed = t0.elapsed_time(t1) / 1e3
+    elapsed_max = reduce_max(elapsed, world, dev)
+    split_ms = [a.elapsed_time(b) for a, b in ev_split]
+    split_avg = sum(split_ms) / len(split_ms) / 1e3
+    # the split kernel's algorithmic bytes: KV + table entries + scales of the
+    # live pages (tags are read by the validation kernel)
+    lens = [p.db.batch.lens_bh("seq").astype(np.int64) for p in reps]
+    pages_live = statistics.mean(int(((l + 15) // 16).sum()) for l in lens)
+    split_bytes = kv_bytes + pages_live * (4 + 8) + 2 * spec0.B * spec0.Hq * spec0.D
+    split_gbs = split_bytes / split_avg / 1e9
+    peak, peak_kind = peaks()
+
+    # check the last step's flags (no request should be flagged in this workload)
+    for p in reps:
+        if int(p.db.flags[:spec0.B].sum()) or int(p.db.append_flags[:spec0.B].sum()):
+            raise RuntimeError("benchmark workload flagged a request")
+
+    value = aggregate(step_bytes, K, elapsed_max, world)
+    ms_per_step = elapsed_max / K * 1e3
+    tokens_per_s = world * spec0.B / (N_LAYERS * elapsed_max / K)
+
+    e2e = run_e2e(args, reps, B, stream, step_bytes, world, dev)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(reps[0].db)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 KV, fp32 accumulate, bf16 q/out", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": spec0.B, "num_q_heads": spec0.Hq,
+                       "num_kv_heads": spec0.Hkv, "head_dim": spec0.D, "page_size": 16,
+                       "seq_lens": "U[512,8192]+1 appended", "num_pages": spec0.num_pages,
+                       "kv_dtype": spec0.kv_dtype, "tags": not args.no_tags,
+                       "split_tokens": args.split, "replicas": args.replicas,
+                       "l2": "inputs larger than L2: %d rotating replicas, %.0f MB live KV each"
+                             % (args.replicas, kv_bytes / 1e6),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tokens_per_s": round(tokens_per_s, 1),
+            "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+            "roofline": {"kernel": "decode_split", "bound": "hbm",
+                         "achieved": round(split_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(split_gbs / peak, 4), "traffic": None,
+                         "peak_kind": peak_kind, "avg_launch_us": round(split_avg * 1e6, 3),
+                         "bytes_per_launch": int(split_bytes)},
+            "e2e": e2e, "gpu_launches": K * (3 if args.no_tags else 4),
+            "clocks": clocks, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, reps, B, stream, step_bytes, world, dev):
+    """Same metric through the public API with host buffers: each step copies
+    its inputs (q, new K/V rows, positions, lengths, block table, expected
+    tags) from pinned host memory, runs append + attention, and reads the
+    output and flags back."""
+    import torch
+    K = max(1, min(args.e2e_steps, args.steps))
+    host = []
+    for p in reps:
+        db = p.db
+        tensors_in = [db.q, db.positions, db.seq_lens, db.block_tables]
+        if db.spec.append:
+            tensors_in += [db.k_new, db.v_new]
+        if db.cache.page_tags is not None:
+            tensors_in.append(db.expected_tags)
+        h_in = [t.detach().cpu().pin_memory() for t in tensors_in]
+        h_out = [torch.empty_like(db.out, device="cpu").pin_memory(),
+                 torch.empty_like(db.flags, device="cpu").pin_memory()]
+        host.append((tensors_in, h_in, h_out))
+    h2d = sum(t.numel() * t.element_size() for t in host[0][1])
+    d2h = sum(t.numel() * t.element_size() for t in host[0][2])
+    for i in range(5):
+        p = reps[i % len(reps)]
+        p.append()
+        p.stage(B.PFKV_STAGE_ALL)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(K):
+        r = i % len(reps)
+        p = reps[r]
+        d_in, h_in, h_out = host[r]
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        p.append()
+        p.stage(B.PFKV_STAGE_ALL)
+        h_out[0].copy_(p.db.out, non_blocking=True)
+        h_out[1].copy_(p.db.flags, non_blocking=True)
+        stream.synchronize()
+    el = time.perf_counter() - t0
+    el = reduce_max(el, world, dev)
+    return {"value": round(aggregate(step_bytes, K, el, world), 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K,
+            "ms_per_step": round(el / K * 1e3, 4)}
+
+
+# --------------------------------------------------------------------------
+# the oracle (test infrastructure) as CPU baseline / reference arm
+# --------------------------------------------------------------------------
+def _oracle_sample(spec, n_requests: int, n_kv_heads: int, seed: int):
+    """A bounded sample of the workload for the oracle: n requests with the
+    workload's lengths, group size and head_dim but only n_kv_heads kv heads
+    (and their G query heads each), quantised by the oracle itself."""
+    import dataclasses
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from oracle_cases import cache_dict, fill_pool, pages_dict
+    from paged_fp8_kv_decode_gb300 import workloads as W
+    sub = dataclasses.replace(spec, B=n_requests, lens=np.asarray(spec.lens[:n_requests]),
+                              Hkv=n_kv_heads, Hq=spec.G * n_kv_heads, seed=seed,
+                              num_pages=4096)
+    batch = W.make_batch(sub)
+    T = int(batch.fill_lens.max())
+    k_rows = W.draw_kv_rows(sub, T, "k")
+    v_rows = W.draw_kv_rows(sub, T, "v")
+    k, v, ks, vs = fill_pool(sub, batch, W.bf16_bits(k_rows), W.bf16_bits(v_rows))
+    cache = cache_dict(sub, batch, k, v, ks, vs)
+    pages = pages_dict(sub, batch, batch.seq_lens)
+    if sub.append:
+        oracle.kv_append(cache, pages, batch.positions,
+                         W.bf16_bits(W.draw_new_token(sub, "k")),
+                         W.bf16_bits(W.draw_new_token(sub, "v")))
+    q = W.bf16_bits(W.draw_q(sub))
+    kv = int(batch.lens_bh("seq").astype(np.int64).sum()) * sub.D * 2
+    return oracle, cache, pages, q, sub, batch, kv
+
+
+def _time_oracle(oracle, cache, pages, q, sub, batch):
+    t0 = time.perf_counter()
+    oracle.paged_decode(cache, pages, q, sub.Hq, sub.sm_scale, int(batch.seq_lens.max()))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(db, target_s: float = 15.0):
+    """Oracle KV GB/s on host cores over a bounded sample of the workload."""
+    spec = db.spec
+    oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, 2, spec.Hkv, spec.seed + 555)
+    t = _time_oracle(oracle, cache, pages, q, sub, batch)
+    reps = max(1, min(50, int(target_s / max(t, 1e-3))))
+    total = t
+    for _ in range(reps - 1):
+        total += _time_oracle(oracle, cache, pages, q, sub, batch)
+    return {"value": round(kv * reps / total / 1e9, 4), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{sub.B} of {spec.B} requests ({int(batch.seq_lens.sum())} tokens, all "
+                      f"{sub.Hq} q heads), attention only, {reps} repetitions in {total:.1f} s; "
+                      f"KV bytes read / oracle time"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_fp8_kv_decode_gb300 import workloads as W
+    spec = W.spec_llama8b("full")
+    # per step: one request of the workload, restricted to enough kv heads that
+    # warmup + steps fit in about two minutes of oracle time
+    oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, 1, 1, spec.seed + 777)
+    t1 = min(_time_oracle(oracle, cache, pages, q, sub, batch) for _ in range(2))
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nh = max(1, min(spec.Hkv, int(budget / max(t1, 1e-6))))
+    if nh > 1:
+        oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, 1, nh, spec.seed + 777)
+    for _ in range(args.warmup):
+        _time_oracle(oracle, cache, pages, q, sub, batch)
+    ts = [_time_oracle(oracle, cache, pages, q, sub, batch) for _ in range(args.steps)]
+    total = sum(ts)
+    value = kv * len(ts) / total / 1e9
+    sample = (f"1 request ({int(batch.seq_lens[0])} tokens), {sub.Hkv} of {spec.Hkv} kv heads "
+              f"({sub.Hq} q heads) per step, attention only; KV bytes read / oracle time")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / len(ts) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 quantiser",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": spec.B, "num_q_heads": spec.Hq,
+                       "num_kv_heads": spec.Hkv, "head_dim": spec.D, "page_size": 16,
+                       "kv_dtype": "fp8"},
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

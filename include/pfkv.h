@@ -1,0 +1,248 @@
+/*
+ * pfkv.h -- C ABI of libpfkv.so: decode attention over a paged FP8 (e4m3) or
+ * BF16 KV cache with per-page integrity tags, for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed comes from these web pages (cited by title and section):
+ *  - "How we built the most efficient inference engine for Cloudflare's
+ *    network", section "Batching to feed the Tensor Cores": the KV cache is
+ *    split into small pages that are handed out only as a sequence grows.
+ *  - "Workers AI targets the inference bottleneck", section "KV cache
+ *    compression goes open source": a block table of integer page indices maps
+ *    each sequence's logical pages onto physical pages, which lets every
+ *    attention head keep a different number of tokens (per-head eviction).
+ *  - "Cloudflare quantizes Kimi and GLM caches for 41% faster inference",
+ *    2nd paragraph: the cache is stored as FP8 e4m3 instead of BF16, halving
+ *    it, and decode (memory-bound) reads the FP8 cache; 4th paragraph: every
+ *    physical page carries a tag that changes when the page is reallocated,
+ *    each request's expected (page, tag) pairs are checked by a separate batch
+ *    validation before decode reads the cache, a request with any mismatch is
+ *    aborted, and with checking disabled a no-op tracker costs nothing.
+ *
+ * Conventions for every call:
+ *  - Memory: every pointer argument not marked "host" is DEVICE memory owned
+ *    by the caller.  The library never allocates or frees memory and keeps no
+ *    state between calls; calls on different streams are independent.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
+ *    work is enqueued asynchronously on it; no call synchronises the host.
+ *  - Alignment: k_pages, v_pages, q, out, k_new and v_new 16-byte aligned;
+ *    workspace 256-byte aligned; index, length, tag, scale and e4m3-utility
+ *    arrays 4-byte aligned; flags 4-byte aligned and backed by at least
+ *    round_up(batch, 4) bytes (bits are OR-ed through 32-bit words).
+ *    Misalignment returns PFKV_ERR_ALIGNMENT.
+ *  - Errors: argument errors the host can see are returned before anything is
+ *    enqueued.  PFKV_ERR_CUDA means a launch failed (cudaGetLastError).  Errors
+ *    in device-resident data (page ids, lengths, tags) never fault: they are
+ *    reported per request in `flags` and that request's output is zero, which
+ *    callers treat as "aborted".
+ *  - Hardware: compiled for sm_103a only.  Calls return PFKV_ERR_UNSUPPORTED on
+ *    other devices.
+ */
+#ifndef PFKV_H
+#define PFKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PFKV_OK = 0,
+    PFKV_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, stride or count      */
+    PFKV_ERR_UNSUPPORTED = 2,  /* head_dim, group size, page size or device    */
+    PFKV_ERR_ALIGNMENT = 3,    /* a pointer is not suitably aligned            */
+    PFKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required   */
+    PFKV_ERR_CUDA = 5          /* a CUDA runtime call or launch failed         */
+} pfkv_status;
+
+typedef enum {
+    PFKV_KV_BF16 = 0,          /* pages hold bf16 values                       */
+    PFKV_KV_FP8_E4M3 = 1       /* pages hold OCP e4m3 bytes + fp32 unit scales */
+} pfkv_kv_dtype;
+
+/* Tokens per page. */
+#define PFKV_PAGE_SIZE 16
+
+/* Per-request flag bits (uint8 per request). */
+#define PFKV_FLAG_TAG_MISMATCH 0x01u  /* a live page's tag != the expected tag  */
+#define PFKV_FLAG_BAD_PAGE 0x02u      /* a live table entry is outside the pool  */
+#define PFKV_FLAG_BAD_LENGTH 0x04u    /* length/position outside the table or
+                                         above max_seq_len                       */
+#define PFKV_FLAG_DEVICE_TIMEOUT 0x08u /* a bounded device-side wait gave up;
+                                          the output of the request is invalid   */
+
+/*
+ * The page pool.  A "unit" is one (physical page, kv head) slab of
+ * PFKV_PAGE_SIZE tokens x head_dim elements; a block-table entry `phys` read
+ * for kv head h always names unit (phys, h).
+ *   k_pages, v_pages : [num_pages][num_kv_heads][PFKV_PAGE_SIZE][head_dim],
+ *                      bf16 (dtype BF16) or e4m3 bytes (dtype FP8_E4M3)
+ *   k_scale, v_scale : fp32 [num_pages][num_kv_heads] for FP8 (value of an
+ *                      element = e4m3 value x unit scale); ignored for BF16
+ *   page_tags        : uint32 [num_pages][num_kv_heads], or NULL when tags are
+ *                      not tracked (the no-op tracker: no check is run)
+ */
+typedef struct pfkv_cache {
+    int32_t num_pages;
+    int32_t num_kv_heads;
+    int32_t page_size;     /* must be PFKV_PAGE_SIZE */
+    int32_t head_dim;      /* 64 or 128 */
+    int32_t dtype;         /* pfkv_kv_dtype */
+    void *k_pages;
+    void *v_pages;
+    float *k_scale;
+    float *v_scale;
+    const uint32_t *page_tags;
+} pfkv_cache;
+
+/*
+ * The batch's view of the pool.
+ *   block_tables  : int32, entry (b, h, p) at
+ *                   block_tables[b*bt_stride_b + h*bt_stride_h + p],
+ *                   p < max_pages.  bt_stride_h = 0 shares one table across
+ *                   kv heads; > 0 gives every kv head its own table.
+ *   seq_lens      : int32 tokens of (b, h) at
+ *                   seq_lens[b*len_stride_b + h*len_stride_h] (len_stride_h = 0:
+ *                   one length per request).  Only entries p < ceil(len/16) are
+ *                   live; the rest of a row is never read.
+ *   expected_tags : uint32, indexed like block_tables: the tag the request
+ *                   expects on each live page.  NULL iff page_tags is NULL.
+ */
+typedef struct pfkv_pages {
+    int32_t batch;
+    int32_t max_pages;
+    const int32_t *block_tables;
+    int64_t bt_stride_b;
+    int64_t bt_stride_h;
+    const int32_t *seq_lens;
+    int64_t len_stride_b;
+    int64_t len_stride_h;
+    const uint32_t *expected_tags;
+} pfkv_pages;
+
+/*
+ * pfkv_kv_append -- write new tokens' K and V into their page slots,
+ * quantising to e4m3 for an FP8 pool ("Cloudflare quantizes Kimi and GLM
+ * caches for 41% faster inference", 2nd paragraph).
+ *
+ *   positions    : int32, indexed with the length strides of `pages`: position
+ *                  of the first new token of (b, h)
+ *   new_lens     : int32 (same indexing) number of new tokens of (b, h), each
+ *                  <= num_new_tokens; NULL means num_new_tokens for all
+ *   num_new_tokens: T >= 1
+ *   k_new, v_new : bf16 [batch][num_kv_heads][T][head_dim]
+ *   flags        : uint8 [batch] or NULL; bits are OR-ed in, never cleared
+ *
+ * Token t of (b, h) goes to position pos = positions + t: unit
+ * (block_tables[b,h,pos/16], h), slot pos % 16.  FP8: the call that writes
+ * slot 0 of a unit sets that unit's K and V scales to absmax/448 (fp32 IEEE
+ * division; 1 if absmax is 0) over the tokens it writes into the unit; other
+ * calls keep the stored scales.  Each byte is the e4m3 encoding, round to
+ * nearest even and saturating to +-448, of the fp32 quotient x / scale.  BF16:
+ * values are copied.  seq_lens is not read or updated.
+ * A destination whose logical page is >= max_pages (PFKV_FLAG_BAD_LENGTH),
+ * whose page id is outside the pool (PFKV_FLAG_BAD_PAGE) or, when tags are
+ * tracked, whose pool tag differs from the expected tag
+ * (PFKV_FLAG_TAG_MISMATCH) is not written.  Two calls, or two (b, h), that
+ * write the same unit concurrently race.
+ */
+pfkv_status pfkv_kv_append(const pfkv_cache *cache, const pfkv_pages *pages,
+                           const int32_t *positions, const int32_t *new_lens,
+                           int32_t num_new_tokens, const void *k_new,
+                           const void *v_new, uint8_t *flags, void *stream);
+
+/*
+ * pfkv_decode_workspace_size -- bytes of device workspace that
+ * pfkv_paged_decode_attn needs for these arguments (host call; reads no
+ * device memory).  *bytes (host) receives the size.
+ */
+pfkv_status pfkv_decode_workspace_size(const pfkv_cache *cache, const pfkv_pages *pages,
+                                       int32_t num_q_heads, int32_t split_tokens,
+                                       int32_t max_seq_len, size_t *bytes);
+
+/*
+ * pfkv_paged_decode_attn -- one decode step of attention for every request
+ * and query head, reading K/V through the block tables ("Workers AI targets
+ * the inference bottleneck", KV cache compression section) from an FP8 or
+ * BF16 pool ("Cloudflare quantizes Kimi and GLM caches ...", 2nd paragraph),
+ * after the integrity check of the 4th paragraph of the same page.
+ *
+ *   q            : bf16 [batch][num_q_heads][head_dim]
+ *   num_q_heads  : a multiple G of num_kv_heads with G in {1, 2, 4, 8}; query
+ *                  head hq reads kv head hq / G
+ *   sm_scale     : softmax scale (usually 1/sqrt(head_dim))
+ *   split_tokens : tokens per split-KV chunk (a multiple of 16), or 0 to let
+ *                  the library choose
+ *   max_seq_len  : host-known upper bound of every seq_lens entry (sizes the
+ *                  launch); a longer length is flagged PFKV_FLAG_BAD_LENGTH
+ *   workspace    : >= pfkv_decode_workspace_size(...) bytes; contents on entry
+ *                  are ignored; must not be used concurrently by another call
+ *   out          : bf16 [batch][num_q_heads][head_dim]
+ *   flags        : uint8 [batch], written (not OR-ed); may be NULL
+ *
+ * For each (b, hq) with h = hq / G and n = seq_lens(b, h):
+ *   out = sum_j softmax_j(sm_scale * q . k_j) v_j over tokens j < n, where
+ *   token j is slot j % 16 of unit (block_tables[b,h,j/16], h) and FP8 values
+ *   are e4m3 value x unit scale.  Computed in fp32, rounded to bf16.
+ * out is zero for a zero-length head and for every head of a flagged request.
+ * When page_tags is non-NULL every live entry's pool tag is compared with the
+ * expected tag before any page of the batch is read (a separate validation
+ * kernel, stream-ordered before attention); page ids and lengths are always
+ * bounds-checked.
+ */
+pfkv_status pfkv_paged_decode_attn(const pfkv_cache *cache, const pfkv_pages *pages,
+                                   const void *q, int32_t num_q_heads, float sm_scale,
+                                   int32_t split_tokens, int32_t max_seq_len,
+                                   void *workspace, size_t workspace_bytes, void *out,
+                                   uint8_t *flags, void *stream);
+
+/* Stages of one attention call, in stream order. */
+#define PFKV_STAGE_VALIDATE 0x1u  /* tag/bounds check (runs only if tags tracked) */
+#define PFKV_STAGE_SPLIT 0x2u     /* per-chunk attention into the workspace       */
+#define PFKV_STAGE_COMBINE 0x4u   /* merge chunks, write out and flags            */
+#define PFKV_STAGE_ALL 0x7u
+
+/*
+ * pfkv_paged_decode_attn_stages -- the same computation as
+ * pfkv_paged_decode_attn, launching only the stages named in `stages` (a
+ * PFKV_STAGE_* mask).  Calling VALIDATE, then SPLIT, then COMBINE with the
+ * same arguments and workspace, in stream order, gives exactly the result of
+ * one pfkv_paged_decode_attn call (which is this call with PFKV_STAGE_ALL).
+ * The workspace carries the state between stages; calling a later stage
+ * without the earlier ones of the same arguments gives unspecified (but
+ * in-bounds) output.  Lets a caller time or interleave the kernels.
+ * stages == 0 or containing unknown bits: PFKV_ERR_INVALID_ARG.
+ */
+pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pages *pages,
+                                          const void *q, int32_t num_q_heads, float sm_scale,
+                                          int32_t split_tokens, int32_t max_seq_len,
+                                          void *workspace, size_t workspace_bytes, void *out,
+                                          uint8_t *flags, uint32_t stages, void *stream);
+
+/*
+ * pfkv_e4m3_encode -- out[i] = e4m3 code of x[i] (fp32), round to nearest
+ * even, saturating to +-448, NaN -> 0x7F: the conversion kv_append uses.
+ * x: fp32 [n], out: uint8 [n] (device).  n >= 0.
+ */
+pfkv_status pfkv_e4m3_encode(const float *x, int64_t n, uint8_t *out, void *stream);
+
+/*
+ * pfkv_e4m3_decode -- out[i] = value of e4m3 code codes[i] (fp32, exact; NaN
+ * for 0x7F/0xFF): the conversion the attention kernel uses.
+ * codes: uint8 [n], out: fp32 [n] (device).  n >= 0.
+ */
+pfkv_status pfkv_e4m3_decode(const uint8_t *codes, int64_t n, float *out, void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *pfkv_status_string(pfkv_status status);
+
+/* ABI version of this header (incremented on incompatible changes). */
+#define PFKV_ABI_VERSION 1
+int32_t pfkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PFKV_H */

@@ -1,0 +1,250 @@
+"""ctypes binding of libpfkv.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (see
+``include/pfkv.h`` for the full contract) and forwards torch CUDA tensors as
+raw device pointers plus the caller's CUDA stream.  All computation runs in the
+library's kernels; there is no fallback.  If the library has not been built,
+the first call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpfkv.so")
+
+PFKV_OK = 0
+PFKV_ERR_INVALID_ARG = 1
+PFKV_ERR_UNSUPPORTED = 2
+PFKV_ERR_ALIGNMENT = 3
+PFKV_ERR_WORKSPACE = 4
+PFKV_ERR_CUDA = 5
+
+PFKV_KV_BF16 = 0
+PFKV_KV_FP8_E4M3 = 1
+PFKV_PAGE_SIZE = 16
+
+PFKV_FLAG_TAG_MISMATCH = 0x01
+PFKV_FLAG_BAD_PAGE = 0x02
+PFKV_FLAG_BAD_LENGTH = 0x04
+PFKV_FLAG_DEVICE_TIMEOUT = 0x08
+
+PFKV_STAGE_VALIDATE = 0x1
+PFKV_STAGE_SPLIT = 0x2
+PFKV_STAGE_COMBINE = 0x4
+PFKV_STAGE_ALL = 0x7
+
+# every symbol include/pfkv.h declares
+EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",
+            "pfkv_paged_decode_attn_stages", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string", "pfkv_abi_version")
+
+
+class PfkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {pfkv_status_string(status)} (status {status})")
+
+
+class _CCache(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("k_pages", ctypes.c_void_p),
+                ("v_pages", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("page_tags", ctypes.c_void_p)]
+
+
+class _CPages(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("block_tables", ctypes.c_void_p), ("bt_stride_b", ctypes.c_int64),
+                ("bt_stride_h", ctypes.c_int64), ("seq_lens", ctypes.c_void_p),
+                ("len_stride_b", ctypes.c_int64), ("len_stride_h", ctypes.c_int64),
+                ("expected_tags", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpfkv.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.pfkv_kv_append.argtypes = [ctypes.POINTER(_CCache), ctypes.POINTER(_CPages), P, P, I32,
+                                     P, P, P, P]
+        L.pfkv_kv_append.restype = ctypes.c_int
+        L.pfkv_decode_workspace_size.argtypes = [ctypes.POINTER(_CCache),
+                                                 ctypes.POINTER(_CPages), I32, I32, I32,
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+        L.pfkv_decode_workspace_size.restype = ctypes.c_int
+        L.pfkv_paged_decode_attn.argtypes = [ctypes.POINTER(_CCache), ctypes.POINTER(_CPages), P,
+                                             I32, ctypes.c_float, I32, I32, P, ctypes.c_size_t,
+                                             P, P, P]
+        L.pfkv_paged_decode_attn.restype = ctypes.c_int
+        L.pfkv_paged_decode_attn_stages.argtypes = [ctypes.POINTER(_CCache),
+                                                    ctypes.POINTER(_CPages), P, I32,
+                                                    ctypes.c_float, I32, I32, P, ctypes.c_size_t,
+                                                    P, P, ctypes.c_uint32, P]
+        L.pfkv_paged_decode_attn_stages.restype = ctypes.c_int
+        L.pfkv_e4m3_encode.argtypes = [P, I64, P, P]
+        L.pfkv_e4m3_encode.restype = ctypes.c_int
+        L.pfkv_e4m3_decode.argtypes = [P, I64, P, P]
+        L.pfkv_e4m3_decode.restype = ctypes.c_int
+        L.pfkv_status_string.argtypes = [ctypes.c_int]
+        L.pfkv_status_string.restype = ctypes.c_char_p
+        L.pfkv_abi_version.argtypes = []
+        L.pfkv_abi_version.restype = ctypes.c_int32
+        _lib = L
+    return _lib
+
+
+def pfkv_status_string(status: int) -> str:
+    return lib().pfkv_status_string(int(status)).decode()
+
+
+def pfkv_abi_version() -> int:
+    return int(lib().pfkv_abi_version())
+
+
+# --------------------------------------------------------------------------
+# argument containers
+# --------------------------------------------------------------------------
+@dataclasses.dataclass
+class Cache:
+    """The page pool (caller-owned CUDA tensors).
+
+    k_pages, v_pages: [num_pages][Hkv][16][head_dim], torch.bfloat16 or
+    torch.uint8 (e4m3 codes); k_scale, v_scale: float32 [num_pages][Hkv] (FP8);
+    page_tags: int32 (uint32 bit patterns) [num_pages][Hkv] or None."""
+    k_pages: torch.Tensor
+    v_pages: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+    page_tags: Optional[torch.Tensor] = None
+
+    @property
+    def dtype(self) -> int:
+        return PFKV_KV_BF16 if self.k_pages.dtype == torch.bfloat16 else PFKV_KV_FP8_E4M3
+
+    def c_struct(self) -> _CCache:
+        NP, H, PS, D = self.k_pages.shape
+        return _CCache(NP, H, PS, D, self.dtype, _ptr(self.k_pages), _ptr(self.v_pages),
+                       _ptr(self.k_scale), _ptr(self.v_scale), _ptr(self.page_tags))
+
+
+@dataclasses.dataclass
+class Pages:
+    """The batch's block tables (int32), lengths (int32) and expected tags,
+    with element strides (stride_h = 0: shared by every kv head)."""
+    batch: int
+    max_pages: int
+    block_tables: torch.Tensor
+    bt_stride_b: int
+    bt_stride_h: int
+    seq_lens: torch.Tensor
+    len_stride_b: int
+    len_stride_h: int
+    expected_tags: Optional[torch.Tensor] = None
+
+    def c_struct(self) -> _CPages:
+        return _CPages(self.batch, self.max_pages, _ptr(self.block_tables), self.bt_stride_b,
+                       self.bt_stride_h, _ptr(self.seq_lens), self.len_stride_b,
+                       self.len_stride_h, _ptr(self.expected_tags))
+
+    def with_lens(self, seq_lens: torch.Tensor) -> "Pages":
+        return dataclasses.replace(self, seq_lens=seq_lens)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != PFKV_OK:
+        raise PfkvError(status, where)
+
+
+# --------------------------------------------------------------------------
+# entry points
+# --------------------------------------------------------------------------
+def pfkv_kv_append(cache: Cache, pages: Pages, positions: torch.Tensor, k_new: torch.Tensor,
+                   v_new: torch.Tensor, new_lens: Optional[torch.Tensor] = None,
+                   flags: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k_new, v_new: bf16 [B][Hkv][T][D]; positions/new_lens int32 with the
+    length strides of ``pages``; flags uint8 [>= round_up(B, 4)] (OR-ed)."""
+    c, p = cache.c_struct(), pages.c_struct()
+    T = int(k_new.shape[2])
+    _check(lib().pfkv_kv_append(ctypes.byref(c), ctypes.byref(p), _ptr(positions),
+                                _ptr(new_lens), T, _ptr(k_new), _ptr(v_new), _ptr(flags),
+                                _stream(stream)), "pfkv_kv_append")
+
+
+def pfkv_decode_workspace_size(cache: Cache, pages: Pages, num_q_heads: int, split_tokens: int,
+                               max_seq_len: int) -> int:
+    c, p = cache.c_struct(), pages.c_struct()
+    out = ctypes.c_size_t(0)
+    _check(lib().pfkv_decode_workspace_size(ctypes.byref(c), ctypes.byref(p), int(num_q_heads),
+                                            int(split_tokens), int(max_seq_len),
+                                            ctypes.byref(out)), "pfkv_decode_workspace_size")
+    return int(out.value)
+
+
+def pfkv_paged_decode_attn(cache: Cache, pages: Pages, q: torch.Tensor, sm_scale: float,
+                           split_tokens: int, max_seq_len: int, workspace: torch.Tensor,
+                           out: torch.Tensor, flags: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """q, out: bf16 [B][Hq][D]; workspace: uint8 CUDA tensor of at least
+    pfkv_decode_workspace_size(...) bytes; flags uint8 [>= round_up(B, 4)]."""
+    c, p = cache.c_struct(), pages.c_struct()
+    Hq = int(q.shape[1])
+    _check(lib().pfkv_paged_decode_attn(ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq,
+                                        float(sm_scale), int(split_tokens), int(max_seq_len),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _ptr(out), _ptr(flags), _stream(stream)),
+           "pfkv_paged_decode_attn")
+
+
+def pfkv_paged_decode_attn_stages(cache: Cache, pages: Pages, q: torch.Tensor, sm_scale: float,
+                                  split_tokens: int, max_seq_len: int, workspace: torch.Tensor,
+                                  out: torch.Tensor, flags: Optional[torch.Tensor], stages: int,
+                                  stream=None) -> None:
+    """pfkv_paged_decode_attn restricted to the PFKV_STAGE_* kernels in ``stages``."""
+    c, p = cache.c_struct(), pages.c_struct()
+    Hq = int(q.shape[1])
+    _check(lib().pfkv_paged_decode_attn_stages(
+        ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
+        int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(flags), int(stages), _stream(stream)), "pfkv_paged_decode_attn_stages")
+
+
+def pfkv_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _check(lib().pfkv_e4m3_encode(_ptr(x), x.numel(), _ptr(out), _stream(stream)),
+           "pfkv_e4m3_encode")
+
+
+def pfkv_e4m3_decode(codes: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _check(lib().pfkv_e4m3_decode(_ptr(codes), codes.numel(), _ptr(out), _stream(stream)),
+           "pfkv_e4m3_decode")

@@ -1,0 +1,319 @@
+// api.cu -- the C ABI of libpfkv.so (declared in include/pfkv.h): argument
+// validation, launch planning and dispatch.  No allocation, no host
+// synchronisation; every launch goes to the caller's stream.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "pfkv_internal.cuh"
+
+namespace pfkv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+// per-device: 0 = unknown, 1 = supported (sm_103), 2 = unsupported; SM count
+std::atomic<int> g_dev_state[kMaxDevices];
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Checks that the current device is an sm_103 GPU; returns its SM count.
+pfkv_status device_check(int *num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PFKV_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return PFKV_ERR_UNSUPPORTED;
+    int st = g_dev_state[dev].load(std::memory_order_acquire);
+    if (st == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return PFKV_ERR_CUDA;
+        }
+        g_dev_sms[dev].store(sms, std::memory_order_relaxed);
+        st = (major == 10 && minor == 3) ? 1 : 2;
+        g_dev_state[dev].store(st, std::memory_order_release);
+    }
+    if (st != 1) return PFKV_ERR_UNSUPPORTED;
+    if (num_sms) *num_sms = g_dev_sms[dev].load(std::memory_order_relaxed);
+    return PFKV_OK;
+}
+
+pfkv_status check_cache(const pfkv_cache *c) {
+    if (!c) return PFKV_ERR_INVALID_ARG;
+    if (c->page_size != kPage) return PFKV_ERR_UNSUPPORTED;
+    if (c->head_dim != 64 && c->head_dim != 128) return PFKV_ERR_UNSUPPORTED;
+    if (c->dtype != PFKV_KV_BF16 && c->dtype != PFKV_KV_FP8_E4M3) return PFKV_ERR_INVALID_ARG;
+    if (c->num_pages <= 0 || c->num_kv_heads <= 0) return PFKV_ERR_INVALID_ARG;
+    if (!c->k_pages || !c->v_pages) return PFKV_ERR_INVALID_ARG;
+    if (c->dtype == PFKV_KV_FP8_E4M3 && (!c->k_scale || !c->v_scale)) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(c->k_pages, 16) || !aligned(c->v_pages, 16)) return PFKV_ERR_ALIGNMENT;
+    if (c->dtype == PFKV_KV_FP8_E4M3 && (!aligned(c->k_scale, 4) || !aligned(c->v_scale, 4)))
+        return PFKV_ERR_ALIGNMENT;
+    if (c->page_tags && !aligned(c->page_tags, 4)) return PFKV_ERR_ALIGNMENT;
+    return PFKV_OK;
+}
+
+pfkv_status check_pages(const pfkv_cache *c, const pfkv_pages *p) {
+    if (!p) return PFKV_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->max_pages <= 0) return PFKV_ERR_INVALID_ARG;
+    if (p->batch == 0) return PFKV_OK;
+    if (!p->block_tables || !p->seq_lens) return PFKV_ERR_INVALID_ARG;
+    if (p->bt_stride_b < 0 || p->bt_stride_h < 0 || p->len_stride_b < 0 || p->len_stride_h < 0)
+        return PFKV_ERR_INVALID_ARG;
+    // a table row must hold max_pages entries without running into the next
+    if (p->bt_stride_h == 0 && p->batch > 1 && p->bt_stride_b < p->max_pages)
+        return PFKV_ERR_INVALID_ARG;
+    if ((c->page_tags == nullptr) != (p->expected_tags == nullptr)) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(p->block_tables, 4) || !aligned(p->seq_lens, 4)) return PFKV_ERR_ALIGNMENT;
+    if (p->expected_tags && !aligned(p->expected_tags, 4)) return PFKV_ERR_ALIGNMENT;
+    return PFKV_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int auto_chunk_tokens(int B, int Hkv, int max_seq_len, int num_sms) {
+    // aim for about eight chunks per SM if every head had max_seq_len tokens
+    const long long work = (long long)B * Hkv * (max_seq_len > 0 ? max_seq_len : 1);
+    long long per = (work + 8LL * num_sms - 1) / (8LL * num_sms);
+    per = (per + 255) / 256 * 256;
+    if (per < 256) per = 256;
+    if (per > 4096) per = 4096;
+    return (int)per;
+}
+
+// Host-visible checks of the attention arguments (no CUDA call).
+pfkv_status check_decode_args(const pfkv_cache *c, int32_t num_q_heads, int32_t split_tokens,
+                              int32_t max_seq_len) {
+    if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PFKV_ERR_INVALID_ARG;
+    const int G = num_q_heads / c->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PFKV_ERR_UNSUPPORTED;
+    if (max_seq_len < 0) return PFKV_ERR_INVALID_ARG;
+    if (split_tokens < 0 || split_tokens % kPage != 0) return PFKV_ERR_INVALID_ARG;
+    if (split_tokens > 8192) return PFKV_ERR_UNSUPPORTED;
+    return PFKV_OK;
+}
+
+pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_heads,
+                      int32_t split_tokens, int32_t max_seq_len, int num_sms, DecodePlan *plan) {
+    const pfkv_status st = check_decode_args(c, num_q_heads, split_tokens, max_seq_len);
+    if (st != PFKV_OK) return st;
+    const int G = num_q_heads / c->num_kv_heads;
+    DecodePlan q{};
+    q.B = p->batch;
+    q.Hkv = c->num_kv_heads;
+    q.Hq = num_q_heads;
+    q.G = G;
+    q.D = c->head_dim;
+    q.dtype = c->dtype;
+    q.tags = c->page_tags != nullptr;
+    q.chunk_tokens = split_tokens > 0 ? split_tokens
+                                      : auto_chunk_tokens(q.B, q.Hkv, max_seq_len, num_sms);
+    q.nchunks = max_seq_len > 0 ? (max_seq_len + q.chunk_tokens - 1) / q.chunk_tokens : 1;
+    const long long items = (long long)q.B * q.Hkv * q.nchunks;
+    if (items > 0x7fffffffLL || (long long)q.B * q.Hq > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
+    size_t off = 0;
+    q.off_hflags = off;
+    off = align256(off + (q.tags ? sizeof(uint32_t) * q.B * q.Hkv : 0));
+    q.off_status = off;
+    off = align256(off + sizeof(uint32_t) * (size_t)items);
+    q.off_lse = off;
+    off = align256(off + sizeof(float) * (size_t)q.B * q.Hq * q.nchunks);
+    q.off_o = off;
+    off = align256(off + sizeof(float) * (size_t)q.B * q.Hq * q.nchunks * q.D);
+    q.total = off;
+    *plan = q;
+    return PFKV_OK;
+}
+
+}  // namespace
+}  // namespace pfkv
+
+using namespace pfkv;
+
+extern "C" {
+
+const char *pfkv_status_string(pfkv_status s) {
+    switch (s) {
+        case PFKV_OK: return "ok";
+        case PFKV_ERR_INVALID_ARG: return "invalid argument";
+        case PFKV_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case PFKV_ERR_ALIGNMENT: return "misaligned pointer";
+        case PFKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PFKV_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int32_t pfkv_abi_version(void) { return PFKV_ABI_VERSION; }
+
+pfkv_status pfkv_kv_append(const pfkv_cache *cache, const pfkv_pages *pages,
+                           const int32_t *positions, const int32_t *new_lens,
+                           int32_t num_new_tokens, const void *k_new, const void *v_new,
+                           uint8_t *flags, void *stream) {
+    pfkv_status st = check_cache(cache);
+    if (st != PFKV_OK) return st;
+    st = check_pages(cache, pages);
+    if (st != PFKV_OK) return st;
+    if (num_new_tokens <= 0) return PFKV_ERR_INVALID_ARG;
+    if (pages->batch == 0) return PFKV_OK;
+    if (!positions || !k_new || !v_new) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(positions, 4) || (new_lens && !aligned(new_lens, 4))) return PFKV_ERR_ALIGNMENT;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PFKV_ERR_ALIGNMENT;
+    if (flags && !aligned(flags, 4)) return PFKV_ERR_ALIGNMENT;
+    const long long units = ((long long)num_new_tokens + 30) / kPage;
+    if ((units + 3) / 4 > 65535) return PFKV_ERR_UNSUPPORTED;
+    if ((long long)pages->batch * cache->num_kv_heads > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
+    st = device_check(nullptr);
+    if (st != PFKV_OK) return st;
+
+    AppendArgs a{};
+    a.k_pages = cache->k_pages;
+    a.v_pages = cache->v_pages;
+    a.k_scale = cache->k_scale;
+    a.v_scale = cache->v_scale;
+    a.page_tags = cache->page_tags;
+    a.num_pages = cache->num_pages;
+    a.Hkv = cache->num_kv_heads;
+    a.D = cache->head_dim;
+    a.dtype = cache->dtype;
+    a.block_tables = pages->block_tables;
+    a.bt_sb = pages->bt_stride_b;
+    a.bt_sh = pages->bt_stride_h;
+    a.expected_tags = pages->expected_tags;
+    a.max_pages = pages->max_pages;
+    a.positions = positions;
+    a.new_lens = new_lens;
+    a.len_sb = pages->len_stride_b;
+    a.len_sh = pages->len_stride_h;
+    a.T = num_new_tokens;
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.flags = flags;
+    if (launch_kv_append(a, pages->batch, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PFKV_ERR_CUDA;
+    return PFKV_OK;
+}
+
+pfkv_status pfkv_decode_workspace_size(const pfkv_cache *cache, const pfkv_pages *pages,
+                                       int32_t num_q_heads, int32_t split_tokens,
+                                       int32_t max_seq_len, size_t *bytes) {
+    if (!bytes) return PFKV_ERR_INVALID_ARG;
+    pfkv_status st = check_cache(cache);
+    if (st != PFKV_OK) return st;
+    st = check_pages(cache, pages);
+    if (st != PFKV_OK) return st;
+    st = check_decode_args(cache, num_q_heads, split_tokens, max_seq_len);
+    if (st != PFKV_OK) return st;
+    int sms = 0;
+    st = device_check(&sms);
+    if (st != PFKV_OK) return st;
+    DecodePlan plan;
+    st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan);
+    if (st != PFKV_OK) return st;
+    *bytes = plan.total;
+    return PFKV_OK;
+}
+
+pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pages *pages,
+                                          const void *q, int32_t num_q_heads, float sm_scale,
+                                          int32_t split_tokens, int32_t max_seq_len,
+                                          void *workspace, size_t workspace_bytes, void *out,
+                                          uint8_t *flags, uint32_t stages, void *stream) {
+    if (stages == 0 || (stages & ~PFKV_STAGE_ALL)) return PFKV_ERR_INVALID_ARG;
+    pfkv_status st = check_cache(cache);
+    if (st != PFKV_OK) return st;
+    st = check_pages(cache, pages);
+    if (st != PFKV_OK) return st;
+    if (!(sm_scale == sm_scale) || std::isinf(sm_scale)) return PFKV_ERR_INVALID_ARG;
+    if (pages->batch == 0) return PFKV_OK;
+    if (!q || !out) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16)) return PFKV_ERR_ALIGNMENT;
+    if (flags && !aligned(flags, 4)) return PFKV_ERR_ALIGNMENT;
+    st = check_decode_args(cache, num_q_heads, split_tokens, max_seq_len);
+    if (st != PFKV_OK) return st;
+    if (!workspace) return PFKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PFKV_ERR_ALIGNMENT;
+    int sms = 0;
+    st = device_check(&sms);
+    if (st != PFKV_OK) return st;
+    DecodePlan plan;
+    st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan);
+    if (st != PFKV_OK) return st;
+    if (workspace_bytes < plan.total) return PFKV_ERR_WORKSPACE;
+
+    DecodeArgs a{};
+    a.k_pages = cache->k_pages;
+    a.v_pages = cache->v_pages;
+    a.k_scale = cache->k_scale;
+    a.v_scale = cache->v_scale;
+    a.page_tags = cache->page_tags;
+    a.num_pages = cache->num_pages;
+    a.block_tables = pages->block_tables;
+    a.bt_sb = pages->bt_stride_b;
+    a.bt_sh = pages->bt_stride_h;
+    a.seq_lens = pages->seq_lens;
+    a.len_sb = pages->len_stride_b;
+    a.len_sh = pages->len_stride_h;
+    a.expected_tags = pages->expected_tags;
+    a.max_pages = pages->max_pages;
+    a.max_seq_len = max_seq_len;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.flags = flags;
+    a.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): scores in log2 units
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.hflags = plan.tags ? reinterpret_cast<uint32_t *>(ws + plan.off_hflags) : nullptr;
+    a.status = reinterpret_cast<uint32_t *>(ws + plan.off_status);
+    a.lse = reinterpret_cast<float *>(ws + plan.off_lse);
+    a.o = reinterpret_cast<float *>(ws + plan.off_o);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((stages & PFKV_STAGE_VALIDATE) && plan.tags && launch_validate(a, plan, s) != cudaSuccess)
+        return PFKV_ERR_CUDA;
+    if ((stages & PFKV_STAGE_SPLIT) && launch_split(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
+    if ((stages & PFKV_STAGE_COMBINE) && launch_combine(a, plan, s) != cudaSuccess)
+        return PFKV_ERR_CUDA;
+    return PFKV_OK;
+}
+
+pfkv_status pfkv_paged_decode_attn(const pfkv_cache *cache, const pfkv_pages *pages,
+                                   const void *q, int32_t num_q_heads, float sm_scale,
+                                   int32_t split_tokens, int32_t max_seq_len, void *workspace,
+                                   size_t workspace_bytes, void *out, uint8_t *flags,
+                                   void *stream) {
+    return pfkv_paged_decode_attn_stages(cache, pages, q, num_q_heads, sm_scale, split_tokens,
+                                         max_seq_len, workspace, workspace_bytes, out, flags,
+                                         PFKV_STAGE_ALL, stream);
+}
+
+pfkv_status pfkv_e4m3_encode(const float *x, int64_t n, uint8_t *out, void *stream) {
+    if (n < 0) return PFKV_ERR_INVALID_ARG;
+    if (n == 0) return PFKV_OK;
+    if (!x || !out) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(x, 4)) return PFKV_ERR_ALIGNMENT;
+    pfkv_status st = device_check(nullptr);
+    if (st != PFKV_OK) return st;
+    return launch_e4m3_encode(x, n, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PFKV_OK
+               : PFKV_ERR_CUDA;
+}
+
+pfkv_status pfkv_e4m3_decode(const uint8_t *codes, int64_t n, float *out, void *stream) {
+    if (n < 0) return PFKV_ERR_INVALID_ARG;
+    if (n == 0) return PFKV_OK;
+    if (!codes || !out) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(out, 4)) return PFKV_ERR_ALIGNMENT;
+    pfkv_status st = device_check(nullptr);
+    if (st != PFKV_OK) return st;
+    return launch_e4m3_decode(codes, n, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PFKV_OK
+               : PFKV_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,207 @@
+// append.cu -- kv_append (write/quantise new tokens into page slots), the
+// separate integrity/bounds validation that runs before attention, and the
+// e4m3 conversion utilities.
+//
+// FP8 e4m3 cache instead of BF16: "Cloudflare quantizes Kimi and GLM caches
+// for 41% faster inference", 2nd paragraph.  Tag check as a separate batch
+// validation before decode reads: same page, 4th paragraph.
+#include "pfkv_internal.cuh"
+
+namespace pfkv {
+
+// --------------------------------------------------------------------------
+// kv_append: one warp per (request, kv head, k-th unit touched by the call).
+// A warp owns every token of the call that falls into its unit, so the unit
+// scale (absmax over those tokens / 448) is a warp reduction, and the rows it
+// writes are whole 16-token page slabs or their parts.
+// --------------------------------------------------------------------------
+constexpr int kAppendWarps = 4;
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(AppendArgs a) {
+    constexpr int EPL = D / 32;  // elements per lane per row (4 or 2)
+    const int bh = blockIdx.x;
+    const int b = bh / a.Hkv, h = bh - b * a.Hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = blockIdx.y * kAppendWarps + warp;
+
+    const long long li = (long long)b * a.len_sb + (long long)h * a.len_sh;
+    const int p0 = a.positions[li];
+    int n = a.new_lens ? a.new_lens[li] : a.T;
+    n = min(n, a.T);
+    if (n <= 0) return;
+    if (p0 < 0) {
+        if (k == 0 && lane == 0 && a.flags) atomic_or_byte(a.flags, b, PFKV_FLAG_BAD_LENGTH);
+        return;
+    }
+    const long long lp = (long long)(p0 / kPage) + k;  // logical page of this unit
+    const long long tb = max((long long)p0, lp * kPage) - p0;
+    const long long te = min((long long)p0 + n, (lp + 1) * kPage) - p0;
+    if (tb >= te) return;  // the call writes nothing into this unit
+    if (lp >= a.max_pages) {
+        if (lane == 0 && a.flags) atomic_or_byte(a.flags, b, PFKV_FLAG_BAD_LENGTH);
+        return;
+    }
+    const long long bi = (long long)b * a.bt_sb + (long long)h * a.bt_sh + lp;
+    const int phys = a.block_tables[bi];
+    if (phys < 0 || phys >= a.num_pages) {
+        if (lane == 0 && a.flags) atomic_or_byte(a.flags, b, PFKV_FLAG_BAD_PAGE);
+        return;
+    }
+    const long long u = (long long)phys * a.Hkv + h;
+    if (a.page_tags && a.expected_tags && a.page_tags[u] != a.expected_tags[bi]) {
+        if (lane == 0 && a.flags) atomic_or_byte(a.flags, b, PFKV_FLAG_TAG_MISMATCH);
+        return;
+    }
+    const int slot0 = (int)((p0 + tb) % kPage);
+    const int cnt = (int)(te - tb);
+    const long long src_row0 = ((long long)(b * a.Hkv + h) * a.T + tb);
+    const __nv_bfloat16 *ksrc = a.k_new + src_row0 * D + lane * EPL;
+    const __nv_bfloat16 *vsrc = a.v_new + src_row0 * D + lane * EPL;
+    const long long dst_row0 = u * kPage + slot0;
+
+    if constexpr (!FP8) {
+        using Vec = typename std::conditional<EPL == 4, uint2, uint32_t>::type;
+        Vec *kd = reinterpret_cast<Vec *>(static_cast<__nv_bfloat16 *>(a.k_pages) + dst_row0 * D) + lane;
+        Vec *vd = reinterpret_cast<Vec *>(static_cast<__nv_bfloat16 *>(a.v_pages) + dst_row0 * D) + lane;
+        for (int j = 0; j < cnt; ++j) {
+            kd[j * (D / EPL)] = *reinterpret_cast<const Vec *>(ksrc + (long long)j * D);
+            vd[j * (D / EPL)] = *reinterpret_cast<const Vec *>(vsrc + (long long)j * D);
+        }
+    } else {
+        float kscale, vscale;
+        if (slot0 == 0) {
+            // this call opens the unit: scale from its own tokens in the unit
+            float ka = 0.f, va = 0.f;
+            for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    ka = fmaxf(ka, fabsf(__bfloat162float(ksrc[(long long)j * D + e])));
+                    va = fmaxf(va, fabsf(__bfloat162float(vsrc[(long long)j * D + e])));
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, off));
+                va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, off));
+            }
+            kscale = ka == 0.f ? 1.f : __fdiv_rn(ka, 448.f);
+            vscale = va == 0.f ? 1.f : __fdiv_rn(va, 448.f);
+            if (lane == 0) {
+                a.k_scale[u] = kscale;
+                a.v_scale[u] = vscale;
+            }
+        } else {
+            kscale = a.k_scale[u];
+            vscale = a.v_scale[u];
+        }
+        uint8_t *kd = static_cast<uint8_t *>(a.k_pages) + dst_row0 * D + lane * EPL;
+        uint8_t *vd = static_cast<uint8_t *>(a.v_pages) + dst_row0 * D + lane * EPL;
+        for (int j = 0; j < cnt; ++j) {
+            uint32_t kw = 0, vw = 0;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const float kx = __bfloat162float(ksrc[(long long)j * D + e]);
+                const float vx = __bfloat162float(vsrc[(long long)j * D + e]);
+                kw |= (uint32_t)float_to_e4m3(__fdiv_rn(kx, kscale)) << (8 * e);
+                vw |= (uint32_t)float_to_e4m3(__fdiv_rn(vx, vscale)) << (8 * e);
+            }
+            if constexpr (EPL == 4) {
+                *reinterpret_cast<uint32_t *>(kd + (long long)j * D) = kw;
+                *reinterpret_cast<uint32_t *>(vd + (long long)j * D) = vw;
+            } else {
+                *reinterpret_cast<uint16_t *>(kd + (long long)j * D) = (uint16_t)kw;
+                *reinterpret_cast<uint16_t *>(vd + (long long)j * D) = (uint16_t)vw;
+            }
+        }
+    }
+}
+
+cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
+    const long long units = ((long long)a.T + 30) / kPage;  // ceil((T + 15) / 16)
+    dim3 grid((unsigned)(B * a.Hkv), (unsigned)((units + kAppendWarps - 1) / kAppendWarps));
+    dim3 block(kAppendWarps * 32);
+    if (a.dtype == PFKV_KV_FP8_E4M3) {
+        if (a.D == 128) kv_append_kernel<128, true><<<grid, block, 0, s>>>(a);
+        else kv_append_kernel<64, true><<<grid, block, 0, s>>>(a);
+    } else {
+        if (a.D == 128) kv_append_kernel<128, false><<<grid, block, 0, s>>>(a);
+        else kv_append_kernel<64, false><<<grid, block, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------------------
+// validate: one CTA per (request, kv head).  Bits for the live entries of the
+// row: LEN for a bad length, PAGE for an id outside the pool, TAG when the
+// pool's tag differs from the expected one.  Written (not OR-ed) to
+// hflags[b][h]; the attention kernels read them after this kernel completes.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) validate_kernel(DecodeArgs a, int Hkv) {
+    const int bh = blockIdx.x;
+    const int b = bh / Hkv, h = bh - b * Hkv;
+    const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+    uint32_t bits = 0;
+    if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) {
+        bits = PFKV_FLAG_BAD_LENGTH;
+    } else {
+        const int np = (n + kPage - 1) / kPage;
+        const long long row = (long long)b * a.bt_sb + (long long)h * a.bt_sh;
+        for (int p = threadIdx.x; p < np; p += blockDim.x) {
+            const int phys = a.block_tables[row + p];
+            if (phys < 0 || phys >= a.num_pages) {
+                bits |= PFKV_FLAG_BAD_PAGE;
+            } else if (a.page_tags[(long long)phys * Hkv + h] != a.expected_tags[row + p]) {
+                bits |= PFKV_FLAG_TAG_MISMATCH;
+            }
+        }
+    }
+    const int any_page = __syncthreads_or(bits & PFKV_FLAG_BAD_PAGE);
+    const int any_tag = __syncthreads_or(bits & PFKV_FLAG_TAG_MISMATCH);
+    if (threadIdx.x == 0) {
+        uint32_t f = bits & PFKV_FLAG_BAD_LENGTH;
+        if (any_page) f |= PFKV_FLAG_BAD_PAGE;
+        if (any_tag) f |= PFKV_FLAG_TAG_MISMATCH;
+        a.hflags[bh] = f;
+    }
+}
+
+cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    validate_kernel<<<p.B * p.Hkv, 256, 0, s>>>(a, p.Hkv);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------------------
+// e4m3 conversion utilities (the same device conversions the kernels use)
+// --------------------------------------------------------------------------
+__global__ void e4m3_encode_kernel(const float *x, int64_t n, uint8_t *out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = float_to_e4m3(x[i]);
+}
+
+__global__ void e4m3_decode_kernel(const uint8_t *c, int64_t n, float *out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = e4m3x2_to_float2((uint16_t)c[i]).x;
+}
+
+static unsigned grid_for(int64_t n) {
+    int64_t g = (n + 255) / 256;
+    if (g > 152LL * 32) g = 152LL * 32;
+    return (unsigned)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *out, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    e4m3_encode_kernel<<<grid_for(n), 256, 0, s>>>(x, n, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    e4m3_decode_kernel<<<grid_for(n), 256, 0, s>>>(c, n, out);
+    return cudaGetLastError();
+}
+
+}  // namespace pfkv

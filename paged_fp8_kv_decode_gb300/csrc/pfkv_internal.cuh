@@ -1,0 +1,185 @@
+// pfkv_internal.cuh -- device primitives and launch plans shared by the
+// kernels of libpfkv.so (sm_103a).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pfkv.h"
+
+namespace pfkv {
+
+constexpr int kPage = PFKV_PAGE_SIZE;
+
+// per-(request, kv head, chunk) status bits written by the split kernel
+constexpr uint32_t kStatusBadPage = PFKV_FLAG_BAD_PAGE;
+constexpr uint32_t kStatusTimeout = PFKV_FLAG_DEVICE_TIMEOUT;
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 100ull * 1000ull * 1000ull;
+
+// --------------------------------------------------------------------------
+// Launch plan of one paged_decode_attn call (computed on the host; the same
+// numbers size the workspace).
+// --------------------------------------------------------------------------
+struct DecodePlan {
+    int B, Hkv, Hq, G, D, dtype;
+    int chunk_tokens;   // tokens per split-KV chunk (multiple of 16)
+    int nchunks;        // ceil(max_seq_len / chunk_tokens), >= 1
+    bool tags;
+    // workspace layout (byte offsets, 256-aligned)
+    size_t off_hflags, off_status, off_lse, off_o, total;
+};
+
+struct DecodeArgs {
+    // pool
+    const void *k_pages, *v_pages;
+    const float *k_scale, *v_scale;
+    const uint32_t *page_tags;
+    int num_pages;
+    // batch
+    const int32_t *block_tables;
+    long long bt_sb, bt_sh;
+    const int32_t *seq_lens;
+    long long len_sb, len_sh;
+    const uint32_t *expected_tags;
+    int max_pages, max_seq_len;
+    // query / output
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    uint8_t *flags;
+    float q_scale;      // sm_scale * log2(e): scores are kept in log2 units
+    // workspace
+    uint32_t *hflags;   // [B][Hkv] tag/bounds bits from the validation kernel
+    uint32_t *status;   // [B][Hkv][nchunks]
+    float *lse;         // [B][Hq][nchunks]  log2-sum-exp of the chunk
+    float *o;           // [B][Hq][nchunks][D] chunk output (normalised)
+};
+
+struct AppendArgs {
+    void *k_pages, *v_pages;
+    float *k_scale, *v_scale;
+    const uint32_t *page_tags;
+    int num_pages, Hkv, D, dtype;
+    const int32_t *block_tables;
+    long long bt_sb, bt_sh;
+    const uint32_t *expected_tags;
+    int max_pages;
+    const int32_t *positions, *new_lens;
+    long long len_sb, len_sh;
+    int T;
+    const __nv_bfloat16 *k_new, *v_new;
+    uint8_t *flags;
+};
+
+// launchers (defined in the .cu files)
+cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s);
+cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_combine(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *out, cudaStream_t s);
+cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStream_t s);
+
+// --------------------------------------------------------------------------
+// device helpers
+// --------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; false if the bounded wait
+// gave up (the caller records a timeout and stops issuing work).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared (this CTA), completing `bytes` of tx on bar.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Two e4m3 codes (low byte first) -> two exact fp32 values, via the hardware
+// e4m3x2 -> f16x2 conversion (every e4m3 value is exact in f16).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<__half2 *>(&h));
+}
+
+// bf16 pair packed in a 32-bit word (low half first) -> two exact fp32 values.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// fp32 -> e4m3, round to nearest even, saturating to +-448 (NaN -> 0x7F).
+__device__ __forceinline__ uint8_t float_to_e4m3(float x) {
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+
+// OR `bits` into byte `idx` of a byte array through its aligned 32-bit word.
+__device__ __forceinline__ void atomic_or_byte(uint8_t *base, int idx, uint32_t bits) {
+    uintptr_t addr = reinterpret_cast<uintptr_t>(base + idx);
+    unsigned int *word = reinterpret_cast<unsigned int *>(addr & ~uintptr_t(3));
+    atomicOr(word, bits << (8 * (addr & 3)));
+}
+
+#endif  // __CUDACC__
+
+}  // namespace pfkv

@@ -48,3 +48,50 @@ def fill_pool(spec, batch, k_rows_bits, v_rows_bits, tags_during_fill=False):
     zeros = np.zeros_like(batch.fill_lens)
     oracle.kv_append(cache, pages, zeros, k_rows_bits, v_rows_bits, new_lens=batch.fill_lens)
     return k, v, ks, vs
+
+
+# --------------------------------------------------------------------------
+# GPU-vs-oracle comparison helpers (used by the -m gpu tests)
+# --------------------------------------------------------------------------
+ATOL = 1e-2   # the contract: |gpu - ref| <= 1e-2 + 1e-2 * |ref| per element
+RTOL = 1e-2
+
+
+def host_pool(t):
+    """Host numpy view of a device pool tensor (uint16 bits for bf16)."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def assert_outputs_close(gpu_out, ref, label=""):
+    """Element-wise |gpu - ref| <= ATOL + RTOL*|ref|; returns (max_abs, max_rel)."""
+    g = gpu_out.float().cpu().numpy().astype(np.float64)
+    err = np.abs(g - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, (label, [(tuple(i), g[tuple(i)], ref[tuple(i)]) for i in bad[:8]])
+    max_abs = float(err.max()) if err.size else 0.0
+    max_rel = float((err / np.maximum(np.abs(ref), 1e-30)).max()) if err.size else 0.0
+    return max_abs, max_rel
+
+
+def oracle_reference(spec, batch, k_rows, v_rows, q, k_new=None, v_new=None,
+                     split_check=None, tags=True):
+    """Run the whole step on the oracle: fill, append (if the workload appends),
+    attention.  Returns dict(k, v, ks, vs, append_flags, out, flags)."""
+    k, v, ks, vs = fill_pool(spec, batch, W.bf16_bits(k_rows), W.bf16_bits(v_rows))
+    res = dict(fill_k=k.copy(), fill_v=v.copy(),
+               fill_ks=None if ks is None else ks.copy(),
+               fill_vs=None if vs is None else vs.copy())
+    cache = cache_dict(spec, batch, k, v, ks, vs, tags=tags)
+    pages = pages_dict(spec, batch, batch.seq_lens, tags=tags)
+    aflags = np.zeros(spec.B, dtype=np.uint8)
+    if spec.append:
+        oracle.kv_append(cache, pages, batch.positions, W.bf16_bits(k_new), W.bf16_bits(v_new),
+                         flags=aflags)
+    out, flags = oracle.paged_decode(cache, pages, W.bf16_bits(q), spec.Hq, spec.sm_scale,
+                                     int(batch.seq_lens.max()))
+    res.update(k=k, v=v, ks=ks, vs=vs, append_flags=aflags, out=out, flags=flags)
+    return res

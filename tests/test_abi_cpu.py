@@ -1,0 +1,142 @@
+"""The C ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before touching CUDA.
+No call here launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pfkv.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from paged_fp8_kv_decode_gb300 import build as pbuild
+    pbuild.build()
+    from paged_fp8_kv_decode_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pfkv_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    assert names == sorted(["pfkv_abi_version", "pfkv_decode_workspace_size", "pfkv_e4m3_decode",
+                            "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_paged_decode_attn",
+                            "pfkv_paged_decode_attn_stages", "pfkv_status_string"])
+
+
+def test_library_exports_every_declared_symbol(B):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in _declared_functions():
+        assert name in exported, name
+        assert hasattr(B.lib(), name)
+    # nothing but the C entry points is exported
+    assert {n for n in exported if not n.startswith("pfkv_")} <= set()
+    assert set(B.EXPORTED) == set(_declared_functions())
+
+
+def test_status_strings_and_version(B):
+    assert B.pfkv_abi_version() == 1
+    for code in range(6):
+        assert isinstance(B.pfkv_status_string(code), str)
+    assert B.pfkv_status_string(0) == "ok"
+    assert B.pfkv_status_string(99) == "unknown status"
+
+
+def _structs(B, **over):
+    c = dict(num_pages=8, num_kv_heads=2, page_size=16, head_dim=128, dtype=1,
+             k_pages=0x10000, v_pages=0x20000, k_scale=0x30000, v_scale=0x40000, page_tags=None)
+    p = dict(batch=2, max_pages=4, block_tables=0x50000, bt_stride_b=4, bt_stride_h=0,
+             seq_lens=0x60000, len_stride_b=1, len_stride_h=0, expected_tags=None)
+    for k, v in over.items():
+        (c if k in c else p)[k] = v
+    return B._CCache(**c), B._CPages(**p)
+
+
+def _append(B, c, p, positions=0x70000, T=1, k=0x80000, v=0x90000, flags=None):
+    return B.lib().pfkv_kv_append(ctypes.byref(c), ctypes.byref(p), positions, None, T, k, v,
+                                  flags, None)
+
+
+def _attn(B, c, p, Hq=4, q=0xA0000, ws=0xB0000, ws_bytes=1 << 30, out=0xC0000, split=0,
+          max_len=64):
+    return B.lib().pfkv_paged_decode_attn(ctypes.byref(c), ctypes.byref(p), q, Hq, 0.125, split,
+                                          max_len, ws, ws_bytes, out, None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(page_size=32), 2), (dict(head_dim=96), 2), (dict(dtype=7), 1), (dict(num_pages=0), 1),
+    (dict(k_pages=None), 1), (dict(k_scale=None), 1), (dict(k_pages=0x10008), 3),
+    (dict(max_pages=0), 1), (dict(block_tables=None), 1), (dict(bt_stride_b=-1), 1),
+    (dict(bt_stride_b=2), 1), (dict(page_tags=0x11000), 1), (dict(expected_tags=0x12000), 1),
+    (dict(block_tables=0x50002), 3),
+])
+def test_host_rejects_bad_cache_or_pages(B, over, code):
+    c, p = _structs(B, **over)
+    assert _append(B, c, p) == code
+    assert _attn(B, c, p) == code
+
+
+def test_host_rejects_bad_call_arguments(B):
+    c, p = _structs(B)
+    assert _append(B, c, p, T=0) == 1
+    assert _append(B, c, p, k=None) == 1
+    assert _append(B, c, p, k=0x80008) == 3
+    assert _append(B, c, p, positions=0x70002) == 3
+    assert _append(B, c, p, flags=0xD0001) == 3
+    assert _attn(B, c, p, Hq=3) == 1           # not a multiple of the kv heads
+    assert _attn(B, c, p, Hq=6) == 2           # group size 3
+    assert _attn(B, c, p, Hq=32) == 2          # group size 16
+    assert _attn(B, c, p, split=24) == 1       # not a multiple of 16
+    assert _attn(B, c, p, split=8192 + 16) == 2
+    assert _attn(B, c, p, max_len=-1) == 1
+    assert _attn(B, c, p, q=None) == 1
+    assert _attn(B, c, p, out=0xC0004) == 3
+    assert _attn(B, c, p, ws=None) == 4
+    assert _attn(B, c, p, ws=0xB0010) == 3
+    bad = ctypes.c_size_t(0)
+    assert B.lib().pfkv_decode_workspace_size(ctypes.byref(c), ctypes.byref(p), 4, 0, 64,
+                                              None) == 1
+
+
+def test_stage_mask_is_checked(B):
+    c, p = _structs(B)
+    L = B.lib()
+    for mask in (0, 8, 0x17):
+        assert L.pfkv_paged_decode_attn_stages(ctypes.byref(c), ctypes.byref(p), 0xA0000, 4, 0.125,
+                                               0, 64, 0xB0000, 1 << 30, 0xC0000, None, mask,
+                                               None) == 1
+
+
+def test_empty_batch_is_a_no_op(B):
+    c, p = _structs(B, batch=0, block_tables=None, seq_lens=None)
+    assert _append(B, c, p) == 0
+    assert _attn(B, c, p) == 0
+
+
+def test_e4m3_utilities_reject_bad_sizes(B):
+    L = B.lib()
+    assert L.pfkv_e4m3_encode(None, -1, None, None) == 1
+    assert L.pfkv_e4m3_encode(None, 0, None, None) == 0
+    assert L.pfkv_e4m3_encode(None, 5, None, None) == 1
+    assert L.pfkv_e4m3_encode(0x1002, 5, 0x2000, None) == 3
+    assert L.pfkv_e4m3_decode(0x1000, 5, 0x2002, None) == 3
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from paged_fp8_kv_decode_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "libpfkv.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib()

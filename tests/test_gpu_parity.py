@@ -1,0 +1,220 @@
+"""GPU path vs the oracle on the same seeded inputs (small sizes that still
+span several units, chunks and a ragged tail).
+
+Bit-exact: e4m3 bytes and fp32 scales written by kv_append (fill and the
+decode-step append), append flags and attention flags.  Within the contract
+tolerance |gpu - ref| <= 1e-2 + 1e-2 |ref|: bf16 attention outputs (both sides
+read the same e4m3 bytes, each produced by its own quantiser).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle_cases import (assert_outputs_close, cache_dict, host_pool, oracle_reference,
+                          pages_dict)
+from paged_fp8_kv_decode_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from paged_fp8_kv_decode_gb300 import build as pbuild
+    pbuild.build()
+    from paged_fp8_kv_decode_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _db(batch, **kw):
+    from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
+    return DeviceBatch(batch, keep_rows=True, **kw)
+
+
+def run_and_compare(spec, tags=None, rows=None, q=None, label=""):
+    """Fill, append, attend on the GPU and on the oracle; compare everything."""
+    batch = W.make_batch(spec)
+    use_tags = spec.tags if tags is None else tags
+    db = _db(batch, tags=use_tags, rows=rows, q=q)
+    ref = oracle_reference(spec, batch, db.k_rows.cpu(), db.v_rows.cpu(), db.q.cpu(),
+                           None if db.k_new is None else db.k_new.cpu(),
+                           None if db.v_new is None else db.v_new.cpu(), tags=use_tags)
+    # the fill: bytes and scales bit for bit
+    assert np.array_equal(host_pool(db.cache.k_pages), ref["fill_k"]), label
+    assert np.array_equal(host_pool(db.cache.v_pages), ref["fill_v"]), label
+    if spec.kv_dtype == "fp8":
+        assert np.array_equal(db.cache.k_scale.cpu().numpy(), ref["fill_ks"]), label
+        assert np.array_equal(db.cache.v_scale.cpu().numpy(), ref["fill_vs"]), label
+    # the decode step
+    db.append_step()
+    db.attend()
+    torch.cuda.synchronize()
+    assert np.array_equal(host_pool(db.cache.k_pages), ref["k"]), label
+    assert np.array_equal(host_pool(db.cache.v_pages), ref["v"]), label
+    if spec.kv_dtype == "fp8":
+        assert np.array_equal(db.cache.k_scale.cpu().numpy(), ref["ks"]), label
+        assert np.array_equal(db.cache.v_scale.cpu().numpy(), ref["vs"]), label
+    assert np.array_equal(db.append_flags.cpu().numpy()[:spec.B], ref["append_flags"]), label
+    flags = db.flags.cpu().numpy()[:spec.B]
+    assert np.array_equal(flags, ref["flags"]), (label, flags, ref["flags"])
+    errs = assert_outputs_close(db.out, ref["out"], label)
+    # flagged requests are all zero
+    for b in np.nonzero(flags)[0]:
+        assert not db.out[b].float().abs().sum().item()
+    return db, ref, errs
+
+
+# --------------------------------------------------------------------------
+# the workloads at reduced size
+# --------------------------------------------------------------------------
+def test_tiny_bf16(B):
+    run_and_compare(W.spec_tiny(), label="tiny")
+
+
+@pytest.mark.parametrize("split", [0, 16, 48, 256, 1024, 8192])
+def test_llama8b_small_fp8_append(B, split):
+    spec = dataclasses.replace(W.spec_llama8b("small"), split_tokens=split)
+    run_and_compare(spec, label=f"llama8b-small split={split}")
+
+
+def test_long_small_split(B):
+    run_and_compare(W.spec_long("small"), label="long-small")
+
+
+def test_evict_small_per_head_tables_and_stale_tags(B):
+    spec = W.spec_evict("small")
+    db, ref, _ = run_and_compare(spec, label="evict-small")
+    assert ref["flags"].any() and not ref["flags"].all()
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_sweep_small(B, kv_dtype):
+    run_and_compare(W.spec_sweep(3, kv_dtype, scale="small"), label=f"sweep-{kv_dtype}")
+
+
+def test_evict_small_without_tags(B):
+    spec = W.spec_evict("small")
+    _, ref, _ = run_and_compare(spec, tags=False, label="evict-small-untracked")
+    assert not ref["flags"].any()
+
+
+# --------------------------------------------------------------------------
+# shapes: group sizes, head dims, dtypes, lengths at page and chunk edges
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_group_sizes_and_head_dims(B, kv_dtype, D, G):
+    Hkv = 2
+    lens = np.array([1, 15, 16, 17, 33, 255, 256, 257], dtype=np.int32)
+    spec = W.Spec(f"g{G}d{D}", B=len(lens), Hq=Hkv * G, Hkv=Hkv, D=D, kv_dtype=kv_dtype,
+                  num_pages=256, lens=lens, append=True, tags=True, split_tokens=64,
+                  seed=100 + G * 7 + D)
+    run_and_compare(spec, label=spec.name)
+
+
+@pytest.mark.parametrize("split", [16, 32, 0])
+def test_per_head_lengths_with_zero_length_heads(B, split):
+    lens = np.array([[0, 5, 16, 31], [64, 0, 0, 1], [200, 17, 33, 0]], dtype=np.int32)
+    spec = W.Spec("ph", B=3, Hq=8, Hkv=4, D=128, kv_dtype="fp8", num_pages=128, lens=lens,
+                  per_head=True, tags=True, split_tokens=split, seed=77)
+    run_and_compare(spec, label=f"per-head split={split}")
+
+
+def test_all_lengths_zero(B):
+    lens = np.zeros(3, dtype=np.int32)
+    spec = W.Spec("zero", B=3, Hq=8, Hkv=2, D=128, kv_dtype="fp8", num_pages=16, lens=lens,
+                  tags=False, seed=5)
+    batch = W.make_batch(spec)
+    db = _db(batch, tags=False)
+    db.out.fill_(1.0)
+    db.attend()
+    torch.cuda.synchronize()
+    assert not db.out.float().abs().sum().item()
+    assert not db.flags.cpu().numpy()[:3].any()
+
+
+# --------------------------------------------------------------------------
+# needles: one dominant key, so a dropped or misplaced token shows up as a
+# wholly different output
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_dominant_key_at_page_and_chunk_edges(B, kv_dtype):
+    split = 64
+    lens = np.array([1, 16, 17, 64, 65, 130, 191, 300], dtype=np.int32)
+    spec = W.Spec("needle", B=len(lens), Hq=8, Hkv=2, D=128, kv_dtype=kv_dtype, num_pages=256,
+                  lens=lens, tags=True, split_tokens=split, seed=31, outlier_prob=0.0)
+    T = int(lens.max())
+    q = W.draw_q(spec)
+    k_rows = (W.draw_kv_rows(spec, T, "k").float() * 0.05).to(torch.bfloat16)
+    v_rows = W.draw_kv_rows(spec, T, "v")
+    rng = np.random.Generator(np.random.PCG64(3))
+    for b, n in enumerate(lens):
+        cands = sorted({0, n - 1, min(15, n - 1), min(16, n - 1), min(split - 1, n - 1),
+                        min(split, n - 1), n // 2})
+        for h in range(spec.Hkv):
+            j = int(cands[(b + h) % len(cands)])
+            k_rows[b, h, j] = (q[b, h * spec.G].float() * 3.0).to(torch.bfloat16)
+    db, ref, _ = run_and_compare(spec, rows=(k_rows, v_rows), q=q, label=f"needle-{kv_dtype}")
+    # the first q head of each group is dominated by its needle token
+    for b in range(spec.B):
+        for h in range(spec.Hkv):
+            o = ref["out"][b, h * spec.G]
+            assert np.abs(o).max() > 0.3
+
+
+# --------------------------------------------------------------------------
+# data errors: bad page ids and lengths are flagged, never read
+# --------------------------------------------------------------------------
+def test_bad_page_ids_and_lengths_are_flagged(B):
+    spec = W.Spec("bad", B=5, Hq=8, Hkv=2, D=128, kv_dtype="fp8", num_pages=64,
+                  lens=np.array([40, 40, 40, 40, 40], dtype=np.int32), tags=False, seed=8)
+    batch = W.make_batch(spec)
+    db = _db(batch, tags=False)
+    bt = batch.block_tables.copy()
+    bt[1, 2] = 64            # == pool size
+    bt[2, 0] = -3            # negative
+    bt[3, 3] = 10 ** 9       # padding entry past the live pages: never read
+    lens = batch.seq_lens.copy()
+    lens[4] = 40000          # longer than the table
+    db.block_tables.copy_(torch.from_numpy(bt).cuda())
+    db.seq_lens.copy_(torch.from_numpy(lens).cuda())
+    db.attend()
+    torch.cuda.synchronize()
+    flags = db.flags.cpu().numpy()[:5]
+    cache = dict(num_pages=64, num_kv_heads=2, head_dim=128, dtype=1,
+                 k_pages=np.zeros(1, np.uint8), v_pages=np.zeros(1, np.uint8),
+                 k_scale=np.zeros(1, np.float32), v_scale=np.zeros(1, np.float32),
+                 page_tags=None)
+    pages = pages_dict(spec, batch, lens, tags=False)
+    pages["block_tables"] = bt
+    want = oracle.validate(cache, pages, db.max_seq_len)
+    assert list(flags) == list(want) == [0, 2, 2, 0, 4]
+    out = db.out.float().cpu()
+    assert not out[1].abs().sum() and not out[2].abs().sum() and not out[4].abs().sum()
+    assert out[0].abs().sum() > 0 and out[3].abs().sum() > 0
+
+
+def test_workspace_too_small_is_rejected(B):
+    spec = W.spec_tiny()
+    db = _db(W.make_batch(spec))
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.PfkvError) as e:
+        B.pfkv_paged_decode_attn(db.cache, db.pages, db.q, spec.sm_scale, 0, db.max_seq_len,
+                                 small, db.out, db.flags)
+    assert e.value.status == B.PFKV_ERR_WORKSPACE
+
+
+def test_repeat_calls_are_deterministic(B):
+    spec = W.spec_llama8b("small")
+    db = _db(W.make_batch(spec))
+    db.attend()
+    first = db.out.clone()
+    for _ in range(3):
+        db.attend()
+    torch.cuda.synchronize()
+    assert torch.equal(first, db.out)
