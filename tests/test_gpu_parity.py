@@ -178,8 +178,9 @@ def test_bad_page_ids_and_lengths_are_flagged(B):
     bt = batch.block_tables.copy()
     bt[1, 2] = 64            # == pool size
     bt[2, 0] = -3            # negative
-    bt[3, 3] = 10 ** 9       # padding entry past the live pages: never read
     lens = batch.seq_lens.copy()
+    lens[3] = 20             # 2 live pages ...
+    bt[3, 2] = 10 ** 9       # ... so this entry is padding: never read
     lens[4] = 40000          # longer than the table
     db.block_tables.copy_(torch.from_numpy(bt).cuda())
     db.seq_lens.copy_(torch.from_numpy(lens).cuda())
