@@ -112,20 +112,37 @@ pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_he
     q.D = c->head_dim;
     q.dtype = c->dtype;
     q.tags = c->page_tags != nullptr;
+    // persistent balanced path: one segment per (request, kv head) unless the
+    // caller fixes the split size
+    q.kind = 1;
     q.chunk_tokens = split_tokens > 0 ? split_tokens
-                                      : auto_chunk_tokens(q.B, q.Hkv, max_seq_len, num_sms);
+                                      : (max_seq_len > 0 ? (max_seq_len + kPage - 1) / kPage * kPage
+                                                         : kPage);
     q.nchunks = max_seq_len > 0 ? (max_seq_len + q.chunk_tokens - 1) / q.chunk_tokens : 1;
+    q.pers_ctas = num_sms;
+    q.workers = num_sms * pers_workers_per_cta();
+    if (!pers_supported(q, c->num_pages)) {
+        q.kind = 0;
+        q.chunk_tokens = split_tokens > 0 ? split_tokens
+                                          : auto_chunk_tokens(q.B, q.Hkv, max_seq_len, num_sms);
+        q.nchunks = max_seq_len > 0 ? (max_seq_len + q.chunk_tokens - 1) / q.chunk_tokens : 1;
+        q.pers_ctas = q.workers = 0;
+    }
     const long long items = (long long)q.B * q.Hkv * q.nchunks;
     if (items > 0x7fffffffLL || (long long)q.B * q.Hq > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
+    // rows of partial results: one per (b, hq, chunk), or segment + worker
+    const size_t rows_kv = q.kind == 1 ? (size_t)items + q.workers : (size_t)items;
     size_t off = 0;
     q.off_hflags = off;
     off = align256(off + (q.tags ? sizeof(uint32_t) * q.B * q.Hkv : 0));
+    q.off_prefix = off;
+    off = align256(off + (q.kind == 1 ? sizeof(int) * ((size_t)items + 1) : 0));
     q.off_status = off;
-    off = align256(off + sizeof(uint32_t) * (size_t)items);
+    off = align256(off + sizeof(uint32_t) * rows_kv);
     q.off_lse = off;
-    off = align256(off + sizeof(float) * (size_t)q.B * q.Hq * q.nchunks);
+    off = align256(off + sizeof(float) * rows_kv * q.G);
     q.off_o = off;
-    off = align256(off + sizeof(float) * (size_t)q.B * q.Hq * q.nchunks * q.D);
+    off = align256(off + sizeof(float) * rows_kv * q.G * q.D);
     q.total = off;
     *plan = q;
     return PFKV_OK;
@@ -272,6 +289,7 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
     a.status = reinterpret_cast<uint32_t *>(ws + plan.off_status);
     a.lse = reinterpret_cast<float *>(ws + plan.off_lse);
     a.o = reinterpret_cast<float *>(ws + plan.off_o);
+    a.ws_prefix = reinterpret_cast<int *>(ws + plan.off_prefix);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((stages & PFKV_STAGE_VALIDATE) && plan.tags && launch_validate(a, plan, s) != cudaSuccess)

@@ -1,0 +1,895 @@
+// decode_pers.cu -- persistent, load-balanced split-KV decode attention for
+// e4m3 pools with head_dim 128 and query groups of up to 4 heads, plus the
+// combine kernel that merges its partial rows.
+//
+// What is computed is the attention of decode.cu (single query per head over
+// the tokens its kv head holds, read through the block table from the FP8
+// pool); this file changes how the work is cut and fed:
+//
+// Segments and balanced ranges.  A segment is one (request b, kv head h,
+// chunk c) — c is always 0 unless the caller fixes a split size.  Every CTA
+// computes the same exclusive prefix sum of the segments' 16-token units
+// (units of a request the validation kernel rejected count as zero).  With U
+// units in all and W workers, worker w takes the units
+// [ceil(wU/W), ceil((w+1)U/W)): equal shares, crossing segment boundaries, so
+// no worker idles while another finishes a long sequence.  A worker writes one
+// partial row (normalised output and log2-sum-exp per query head) for every
+// segment it touches, at row index segment + worker, which is unique.
+//
+// Workers.  A worker is a pair of warps sharing a 3-stage shared-memory ring
+// (8 KB per stage: K and V slabs of a 2-unit granule, TMA tile loads with the
+// 128-byte swizzle):
+//  * the score warp holds a 16-dim slice of the G query heads in registers
+//    (lane (t, c): slice c, token 4r + t in pass r), converts K bytes to fp32
+//    pairs, takes packed fp32x2 dot products, finishes each score with a
+//    reduce-scatter over the 8 lanes of a token group (so lane (t, c) ends with
+//    the G scores of token 4c + t), runs the online softmax per granule and
+//    hands the value warp the probabilities times the unit's V scale, as
+//    ready-made pairs, plus rescale factors and segment totals;
+//  * the value warp accumulates its 16-dim slice of the output in registers,
+//    writes the partial row at the end of each segment, and refills the stage
+//    it has just finished with the TMA loads of the granule ST ahead, whose
+//    page ids the score warp wrote next to the probabilities.
+// Splitting scores and values over two warps halves the registers each needs,
+// so 12 warps fit an SM, and the two phases of neighbouring granules overlap.
+#include <atomic>
+#include <cuda.h>
+
+#include "pfkv_internal.cuh"
+
+namespace pfkv {
+
+namespace {
+
+__device__ __forceinline__ float pexp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float plog2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float pwarp_max(float x) {
+    float m;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(x));
+    return m;
+}
+
+__device__ __forceinline__ void ptma_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                        uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void pdequant4(uint32_t w, float2 &lo, float2 &hi) {
+    asm("{\n\t.reg .b16 l, h, a0, a1, b0, b1;\n\t.reg .b32 x, y;\n\t"
+        "mov.b32 {l, h}, %4;\n\t"
+        "cvt.rn.f16x2.e4m3x2 x, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 y, h;\n\t"
+        "mov.b32 {a0, a1}, x;\n\t"
+        "mov.b32 {b0, b1}, y;\n\t"
+        "cvt.f32.f16 %0, a0;\n\t"
+        "cvt.f32.f16 %1, a1;\n\t"
+        "cvt.f32.f16 %2, b0;\n\t"
+        "cvt.f32.f16 %3, b1;\n\t}"
+        : "=f"(lo.x), "=f"(lo.y), "=f"(hi.x), "=f"(hi.y)
+        : "r"(w));
+}
+
+__device__ __forceinline__ void pdequant16(const uint4 w, float2 (&f)[8]) {
+    pdequant4(w.x, f[0], f[1]);
+    pdequant4(w.y, f[2], f[3]);
+    pdequant4(w.z, f[4], f[5]);
+    pdequant4(w.w, f[6], f[7]);
+}
+
+constexpr float kLazy = 8.0f;  // rescale only when the max grows by > 2^8
+
+// worker of global unit x when U units are shared by W workers (see header)
+__device__ __forceinline__ int worker_of(long long x, long long U, int W) {
+    return (int)((x * W) / U);
+}
+
+}  // namespace
+
+template <int G>
+struct PersCfg {
+    static constexpr int D = 128;
+    static constexpr int ROWB = 128;
+    static constexpr int UNITB = kPage * ROWB;   // 2 KB
+    static constexpr int GT = 32;                // tokens per granule (2 units)
+    static constexpr int STAGEB = 4 * UNITB;     // K u0 | K u1 | V u0 | V u1
+    static constexpr int PAIRS = 6;
+    static constexpr int STAGES = 3;
+    static constexpr int NT = PAIRS * 64;
+    static constexpr int MAXK = 4096;            // segments (prefix array in smem)
+    static constexpr int MAXB = 4096;            // requests
+    enum : int { F_RESCALE = 1, F_SEGEND = 2 };
+    struct alignas(16) PBuf {
+        float p[GT][2 * G];   // [token row][g pairs]: probability x V scale, twice
+        float alpha[G];
+        float m[G], l[G];
+        int flags, nv0, nv1, row;
+        int tma_row0, tma_row1;  // K/V tile rows of the granule ST ahead (-1: none)
+        uint32_t status;
+        int pad[1];
+    };
+    struct Pair {
+        alignas(1024) uint8_t ring[STAGES][STAGEB];
+        alignas(16) PBuf pb[STAGES];
+        alignas(16) __nv_bfloat16 q[2][G][D];
+        alignas(8) uint64_t full[STAGES];
+        alignas(8) uint64_t pready[STAGES];
+        alignas(8) uint64_t qbar[2];
+        int ngran;
+    };
+    static_assert(sizeof(PBuf) % 16 == 0, "vector stores into every stage buffer");
+    struct Smem {
+        Pair pair[PAIRS];
+        int prefix[MAXK + 1];
+        int part[NT];
+        uint8_t rflag[MAXB];
+        uint8_t last_nv[MAXK];   // tokens in the last unit of each segment
+    };
+};
+
+// The segment containing global unit x (prefix: exclusive sums, K segments;
+// segments with no units never contain a unit).
+__device__ __forceinline__ int seg_of(const int *prefix, int K, long long x) {
+    int lo = 0, hi = K;  // prefix[lo] <= x < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= x) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+template <int G>
+__global__ void __launch_bounds__(PersCfg<G>::NT, 1)
+    decode_split_pers_kernel(const __grid_constant__ CUtensorMap tmk,
+                             const __grid_constant__ CUtensorMap tmv, DecodeArgs a, int Hkv,
+                             int B, int nchunks, int chunk_tokens, int *ws_prefix) {
+    using C = PersCfg<G>;
+    constexpr int ST = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    typename C::Smem &sm = *reinterpret_cast<typename C::Smem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int K = B * Hkv * nchunks;
+
+    // ---------------- prologue: request flags, unit prefix sums ----------------
+    for (int b = tid; b < B; b += C::NT) {
+        uint32_t f = 0;
+        if (a.hflags)
+            for (int i = 0; i < Hkv; ++i) f |= a.hflags[b * Hkv + i];
+        sm.rflag[b] = f ? 1 : 0;
+    }
+    __syncthreads();
+    const int per = (K + C::NT - 1) / C::NT;
+    const int k0 = min(K, tid * per), k1 = min(K, k0 + per);
+    int local = 0;
+    for (int k = k0; k < k1; ++k) {
+        const int bh = k / nchunks, c = k - bh * nchunks;
+        const int b = bh / Hkv, h = bh - b * Hkv;
+        const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+        int units = 0, lastnv = 0;
+        if (!sm.rflag[b] && n >= 0 && (long long)n <= (long long)a.max_pages * kPage &&
+            n <= a.max_seq_len) {
+            const int pages = (n + kPage - 1) / kPage;
+            const int cp = chunk_tokens / kPage;
+            units = max(0, min(pages, (c + 1) * cp) - c * cp);
+            const int tok_end = min(n, (c + 1) * chunk_tokens);
+            lastnv = tok_end - (tok_end - 1) / kPage * kPage;
+        }
+        sm.prefix[k] = units;  // the count, turned into the prefix below
+        sm.last_nv[k] = (uint8_t)lastnv;
+        local += units;
+    }
+    sm.part[tid] = local;
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan of the per-thread partials by one warp
+        int carry = 0;
+        for (int base = 0; base < C::NT; base += 32) {
+            const int v = sm.part[base + tid];
+            int x = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (tid >= off) x += y;
+            }
+            sm.part[base + tid] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (tid == 0) sm.prefix[K] = carry;
+    }
+    __syncthreads();
+    {
+        int run = sm.part[tid];
+        for (int k = k0; k < k1; ++k) {  // each thread converts its own range
+            const int units = sm.prefix[k];
+            sm.prefix[k] = run;
+            run += units;
+        }
+    }
+    __syncthreads();
+    const long long U = sm.prefix[K];
+    // never more workers than units: every worker then owns at least one unit,
+    // so all workers between a segment's first and last unit write its rows
+    const int W = (int)min((long long)gridDim.x * C::PAIRS, U);
+    if (blockIdx.x == 0) {
+        for (int k = tid; k <= K; k += C::NT) ws_prefix[k] = sm.prefix[k];
+    }
+    if (U == 0) return;
+
+    // ---------------- the worker ----------------
+    const int warp = tid >> 5, lane = tid & 31;
+    const int pi = warp >> 1;           // pair index in the CTA
+    const bool is_score = (warp & 1) == 0;
+    typename C::Pair &P = sm.pair[pi];
+    const int w = blockIdx.x * C::PAIRS + pi;
+    const long long x0 = w < W ? ((long long)w * U + W - 1) / W : U;
+    const long long x1 = w < W ? ((long long)(w + 1) * U + W - 1) / W : U;
+    const int vt = lane >> 3, vc = lane & 7;
+    const uint64_t policy = l2_policy_evict_first();
+
+    if (is_score) {
+        // count this worker's granules (2 units each, never across a segment)
+        int ngran = 0;
+        if (x0 < x1) {
+            long long x = x0;
+            int k = seg_of(sm.prefix, K, x);
+            while (x < x1) {
+                const long long e = min((long long)sm.prefix[k + 1], x1);
+                ngran += (int)((e - x + 1) / 2);
+                x = e;
+                ++k;
+                while (k < K && sm.prefix[k + 1] == sm.prefix[k]) ++k;
+            }
+        }
+        if (lane == 0) {
+            P.ngran = ngran;
+            for (int s = 0; s < ST; ++s) {
+                mbar_init(&P.full[s], 1);
+                mbar_init(&P.pready[s], 1);
+            }
+            mbar_init(&P.qbar[0], 1);
+            mbar_init(&P.qbar[1], 1);
+            fence_mbar_init();
+        }
+    }
+    named_sync(1 + pi, 64);
+    const int ngran = P.ngran;
+    if (ngran == 0) return;
+
+    if (is_score) {
+        // ===================== score warp =====================
+        // unit metadata window: lane l holds unit base + l (cur) and
+        // base + 32 + l (nxt): page id (-1 bad, -2 absent) and the two scales
+        long long base = x0;
+        int cphys, nphys;
+        float cks, cvs, nks, nvs;
+        uint32_t cbad, nbad;  // bad-page bit of the lane's unit
+        auto load_ids = [&](long long bx, int &phys, uint32_t &bad) {
+            const long long x = bx + lane;
+            phys = -2;
+            bad = 0;
+            if (x < x1) {
+                const int k = seg_of(sm.prefix, K, x);
+                const int bh = k / nchunks, c = k - bh * nchunks;
+                const int b = bh / Hkv, h = bh - b * Hkv;
+                const int page = c * (chunk_tokens / kPage) + (int)(x - sm.prefix[k]);
+                const int id = a.block_tables[(long long)b * a.bt_sb + (long long)h * a.bt_sh + page];
+                if (id < 0 || id >= a.num_pages) {
+                    phys = -1;
+                    bad = kStatusBadPage;
+                } else {
+                    phys = id * Hkv + h;  // unit index = tile row / 16
+                }
+            }
+        };
+        auto load_scales = [&](int phys, float &ks, float &vs) {
+            const long long u = phys >= 0 ? phys : 0;
+            ks = a.k_scale[u];
+            vs = a.v_scale[u];
+        };
+        load_ids(base, cphys, cbad);
+        load_ids(base + 32, nphys, nbad);
+        load_scales(cphys, cks, cvs);
+        load_scales(nphys, nks, nvs);
+        // metadata of unit x (must lie in [base, base + 64))
+        // (uniform branches, not selects: a select would wait for the next
+        // window's loads even when only the current one is read)
+        auto unit_phys = [&](long long x) {
+            const int d = (int)(x - base);
+            if (d < 32) return __shfl_sync(0xffffffffu, cphys, d);
+            return __shfl_sync(0xffffffffu, nphys, d - 32);
+        };
+        auto unit_ks = [&](long long x) {
+            const int d = (int)(x - base);
+            if (d < 32) return __shfl_sync(0xffffffffu, cks, d);
+            return __shfl_sync(0xffffffffu, nks, d - 32);
+        };
+        auto unit_vs = [&](long long x) {
+            const int d = (int)(x - base);
+            if (d < 32) return __shfl_sync(0xffffffffu, cvs, d);
+            return __shfl_sync(0xffffffffu, nvs, d - 32);
+        };
+        auto unit_bad = [&](long long x) {
+            const int d = (int)(x - base);
+            if (d < 32) return __shfl_sync(0xffffffffu, cbad, d);
+            return __shfl_sync(0xffffffffu, nbad, d - 32);
+        };
+
+        // cursors over the granule sequence
+        struct Cursor {
+            long long x, seg_end;
+            int k;
+        };
+        auto cursor_init = [&](Cursor &c) {
+            c.x = x0;
+            c.k = seg_of(sm.prefix, K, x0);
+            c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
+        };
+        auto cursor_next = [&](Cursor &c, int n) {
+            c.x += n;
+            if (c.x >= c.seg_end && c.x < x1) {
+                c.k = seg_of(sm.prefix, K, c.x);
+                c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
+            }
+        };
+        Cursor iss, con;
+        cursor_init(iss);
+        cursor_init(con);
+        // tile rows (unit index * 16) of the granule at cursor c, -1 if absent/bad
+        auto granule_rows = [&](const Cursor &c, int &r0, int &r1) {
+            const int n = (int)min((long long)2, c.seg_end - c.x);
+            const int p0 = unit_phys(c.x);
+            const int p1 = n == 2 ? unit_phys(c.x + 1) : -2;
+            r0 = p0 >= 0 ? p0 * kPage : -1;
+            r1 = p1 >= 0 ? p1 * kPage : -1;
+            return n;
+        };
+        auto issue = [&](int s, int r0, int r1) {  // lane 0: load or mark empty
+            if (r0 < 0 && r1 < 0) {
+                mbar_arrive(&P.full[s]);
+                return;
+            }
+            uint8_t *dst = P.ring[s];
+            mbar_arrive_expect_tx(&P.full[s], (r0 >= 0 ? 2 * C::UNITB : 0) + (r1 >= 0 ? 2 * C::UNITB : 0));
+            if (r0 >= 0) {
+                ptma_2d(dst, &tmk, 0, r0, &P.full[s], policy);
+                ptma_2d(dst + 2 * C::UNITB, &tmv, 0, r0, &P.full[s], policy);
+            }
+            if (r1 >= 0) {
+                ptma_2d(dst + C::UNITB, &tmk, 0, r1, &P.full[s], policy);
+                ptma_2d(dst + 3 * C::UNITB, &tmv, 0, r1, &P.full[s], policy);
+            }
+        };
+        // prime the ring
+        for (int j = 0; j < ST && j < ngran; ++j) {
+            int r0, r1;
+            const int n = granule_rows(iss, r0, r1);
+            if (lane == 0) issue(j, r0, r1);
+            cursor_next(iss, n);
+        }
+        // query of the first segment (and the next) into the two q slots
+        auto q_copy = [&](int slot, int k) {  // lane 0
+            const int bh = k / nchunks;
+            const __nv_bfloat16 *src = a.q + (long long)bh * G * C::D;  // (b*Hkv + h)*G rows
+            mbar_arrive_expect_tx(&P.qbar[slot], G * C::D * 2);
+            bulk_g2s(&P.q[slot][0][0], src, G * C::D * 2, &P.qbar[slot], policy);
+        };
+        int seg_ord = 0;          // ordinal of the segment being scored
+        int next_seg_k = -1;      // segment whose q is loading in the other slot
+        if (lane == 0) q_copy(0, con.k);
+        {
+            // next segment after the first one, if the range reaches it
+            if (con.seg_end < x1) {
+                next_seg_k = seg_of(sm.prefix, K, con.seg_end);
+                if (lane == 0) q_copy(1, next_seg_k);
+            }
+        }
+
+        float2 q2[G][8];
+        float m[G], l[G];
+        uint32_t seg_status = 0;
+        uint32_t full_phase = 0, q_phase = 0;
+        bool seg_start = true;
+        bool pending_scales = false;   // nxt ids loaded, scales not yet
+
+        for (int i = 0; i < ngran; ++i) {
+            const int s = i % ST;
+            if (seg_start) {
+                seg_status = 0;
+                const int slot = seg_ord & 1;
+                if (!mbar_wait_bounded(&P.qbar[slot], (q_phase >> slot) & 1u)) seg_status |= kStatusTimeout;
+                q_phase ^= 1u << slot;
+                const __nv_bfloat16 *qs = &P.q[slot][0][0];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16);
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16 + 8);
+                    const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 f = bf16x2_to_float2(ws[e]);
+                        q2[g][e] = make_float2(f.x * a.q_scale, f.y * a.q_scale);
+                    }
+                    m[g] = -INFINITY;
+                    l[g] = 0.f;
+                }
+                __syncwarp();
+                // the slot just read is free: prefetch the segment after next
+                if (next_seg_k >= 0) {
+                    const long long e = min((long long)sm.prefix[next_seg_k + 1], x1);
+                    const int k2 = e < x1 ? seg_of(sm.prefix, K, e) : -1;
+                    if (k2 >= 0 && lane == 0) {
+                        fence_proxy_async_smem();
+                        q_copy(slot, k2);
+                    }
+                    next_seg_k = k2;
+                }
+                seg_start = false;
+            }
+            // metadata window upkeep
+            if (pending_scales) {
+                load_scales(nphys, nks, nvs);
+                pending_scales = false;
+            }
+            if (con.x >= base + 32) {
+                base += 32;
+                cphys = nphys; cks = nks; cvs = nvs; cbad = nbad;
+                load_ids(base + 32, nphys, nbad);
+                pending_scales = true;
+            }
+            const int n_units = (int)min((long long)2, con.seg_end - con.x);
+            const int ph0 = unit_phys(con.x);
+            const int ph1 = n_units == 2 ? unit_phys(con.x + 1) : -2;
+            const bool u0 = ph0 >= 0, u1 = ph1 >= 0;
+            seg_status |= unit_bad(con.x) | (n_units == 2 ? unit_bad(con.x + 1) : 0u);
+            // tokens per unit: 16, except the segment's last unit
+            const long long seg_last = (long long)sm.prefix[con.k + 1] - 1;
+            const int lnv = sm.last_nv[con.k];
+            const int nv0 = u0 ? (con.x == seg_last ? lnv : kPage) : 0;
+            const int nv1 = u1 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
+            const float ks0 = unit_ks(con.x), ks1 = n_units == 2 ? unit_ks(con.x + 1) : 0.f;
+            const float vs0 = unit_vs(con.x), vs1 = n_units == 2 ? unit_vs(con.x + 1) : 0.f;
+
+            // wait for the K/V tiles (or the empty marker) of this granule
+            if (!mbar_wait_bounded(&P.full[s], (full_phase >> s) & 1u)) seg_status |= kStatusTimeout;
+            full_phase ^= 1u << s;
+            const uint8_t *stage = P.ring[s];
+
+            // ---- partial dot products: slice vc, token 4r + vt ----
+            float part[8][G];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int row = 4 * (r & 3) + vt;
+                const uint8_t *krow = stage + (r >> 2) * C::UNITB + row * C::ROWB;
+                const uint4 wv = *reinterpret_cast<const uint4 *>(krow + ((vc ^ (row & 7)) << 4));
+                float2 kf[8];
+                pdequant16(wv, kf);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float2 acc = __fmul2_rn(q2[g][0], kf[0]);
+#pragma unroll
+                    for (int e = 1; e < 8; ++e) acc = __ffma2_rn(q2[g][e], kf[e], acc);
+                    part[r][g] = acc.x + acc.y;
+                }
+            }
+            // ---- reduce-scatter: lane vc gets token 4 vc + vt ----
+            const bool bA = vc & 4, bB = vc & 2, bC = vc & 1;
+            float r1[4][G], r2[2][G], sc[G];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float snd = bA ? part[r][g] : part[r + 4][g];
+                    const float kp = bA ? part[r + 4][g] : part[r][g];
+                    r1[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 4);
+                }
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float snd = bB ? r1[r][g] : r1[r + 2][g];
+                    const float kp = bB ? r1[r + 2][g] : r1[r][g];
+                    r2[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 2);
+                }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float snd = bC ? r2[0][g] : r2[1][g];
+                const float kp = bC ? r2[1][g] : r2[0][g];
+                sc[g] = kp + __shfl_xor_sync(0xffffffffu, snd, 1);
+            }
+            const int my_tok = 4 * vc + vt;   // 0..31
+            const int my_u = vc >> 2;
+            const int my_row = my_tok & 15;
+            const bool ok = my_row < (my_u ? nv1 : nv0);
+            const float ksc = my_u ? ks1 : ks0;
+#pragma unroll
+            for (int g = 0; g < G; ++g) sc[g] = ok ? sc[g] * ksc : -INFINITY;
+
+            // ---- online softmax over the granule ----
+            typename C::PBuf &pb = P.pb[s];
+            float mb[G];
+            bool grow = false;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                mb[g] = pwarp_max(sc[g]);
+                grow |= mb[g] > m[g] + kLazy;
+            }
+            int flags = 0;
+            if (grow) {
+                flags |= C::F_RESCALE;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float mn = fmaxf(m[g], mb[g]);
+                    const float alpha = m[g] == -INFINITY ? 0.f : pexp2(m[g] - mn);
+                    m[g] = mn;
+                    l[g] *= alpha;
+                    if (lane == 0) pb.alpha[g] = alpha;
+                }
+            }
+            {
+                const float vsc = my_u ? vs1 : vs0;
+                float pp[2 * G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float p = ok ? pexp2(sc[g] - m[g]) : 0.f;
+                    l[g] += p;
+                    pp[2 * g] = pp[2 * g + 1] = p * vsc;
+                }
+                // rows transposed (t, c) -> 8 t + c so that a quarter-warp's
+                // stores land in consecutive rows
+                float *dstp = pb.p[8 * vt + vc];
+                if constexpr (G >= 2) {
+#pragma unroll
+                    for (int x = 0; x < G / 2; ++x)
+                        reinterpret_cast<float4 *>(dstp)[x] =
+                            make_float4(pp[4 * x], pp[4 * x + 1], pp[4 * x + 2], pp[4 * x + 3]);
+                } else {
+                    *reinterpret_cast<float2 *>(dstp) = make_float2(pp[0], pp[1]);
+                }
+            }
+            const bool seg_end = con.x + n_units >= con.seg_end;
+            if (seg_end) {
+                flags |= C::F_SEGEND;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float lt = l[g];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+                    if (lane == 0) {
+                        pb.m[g] = m[g];
+                        pb.l[g] = lt;
+                    }
+                }
+            }
+            // the granule ST ahead, for the value warp to load into this stage
+            int tr0 = -1, tr1 = -1;
+            if (i + ST < ngran) {
+                const int n = granule_rows(iss, tr0, tr1);
+                cursor_next(iss, n);
+            }
+            if (lane == 0) {
+                pb.flags = flags;
+                pb.nv0 = nv0;
+                pb.nv1 = nv1;
+                pb.row = con.k + w;
+                pb.status = seg_status;
+                pb.tma_row0 = tr0;
+                pb.tma_row1 = tr1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&P.pready[s]);
+            // advance
+            cursor_next(con, n_units);
+            if (seg_end) {
+                seg_start = true;
+                ++seg_ord;
+            }
+        }
+    } else {
+        // ===================== value warp =====================
+        float2 o[G][8];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
+        uint32_t pr_phase = 0;
+        uint32_t vstatus = 0;
+        for (int i = 0; i < ngran; ++i) {
+            const int s = i % ST;
+            if (!mbar_wait_bounded(&P.pready[s], (pr_phase >> s) & 1u)) vstatus |= kStatusTimeout;
+            pr_phase ^= 1u << s;
+            const typename C::PBuf &pb = P.pb[s];
+            const int flags = pb.flags;
+            if (flags & C::F_RESCALE) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float al = pb.alpha[g];
+                    const float2 a2 = make_float2(al, al);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[g][e] = __fmul2_rn(o[g][e], a2);
+                }
+            }
+            const uint8_t *stage = P.ring[s];
+            const int nv0 = pb.nv0, nv1 = pb.nv1;
+            auto value_pass = [&](int r) {
+                const int row = 4 * (r & 3) + vt;
+                const uint8_t *vrow = stage + 2 * C::UNITB + (r >> 2) * C::UNITB + row * C::ROWB;
+                const uint4 wv = *reinterpret_cast<const uint4 *>(vrow + ((vc ^ (row & 7)) << 4));
+                float2 vf[8];
+                pdequant16(wv, vf);
+                // token 4r + vt was scored by lane (t = vt, c = r): row 8 vt + r
+                const float2 *ps = reinterpret_cast<const float2 *>(pb.p[8 * vt + r]);
+                float2 pg[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) pg[g] = ps[g];
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[g][e] = __ffma2_rn(pg[g], vf[e], o[g][e]);
+            };
+            if (nv0 == kPage && nv1 == kPage) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) value_pass(r);
+            } else {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int row = 4 * (r & 3) + vt;
+                    if (row < ((r >> 2) ? nv1 : nv0)) value_pass(r);
+                }
+            }
+            if (flags & C::F_SEGEND) {
+                // finish the segment: sum the token lanes, normalise, write the row
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+#pragma unroll
+                        for (int off = 8; off < 32; off <<= 1) {
+                            o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, off);
+                            o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, off);
+                        }
+                const int row = pb.row;
+                if (vt == 0) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float L = pb.l[g];
+                        const float inv = L > 0.f ? 1.f / L : 0.f;
+                        float4 *dst = reinterpret_cast<float4 *>(a.o + ((long long)row * G + g) * C::D + vc * 16);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_float4(o[g][2 * e].x * inv, o[g][2 * e].y * inv,
+                                                 o[g][2 * e + 1].x * inv, o[g][2 * e + 1].y * inv);
+                    }
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float L = pb.l[g];
+                        a.lse[(long long)row * G + g] = L > 0.f ? pb.m[g] + plog2(L) : -INFINITY;
+                    }
+                    a.status[row] = pb.status | vstatus;
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
+                vstatus = 0;
+            }
+            // refill this stage with the granule ST ahead
+            const int tr0 = pb.tma_row0, tr1 = pb.tma_row1;
+            __syncwarp();
+            if (lane == 0 && i + ST < ngran) {
+                fence_proxy_async_smem();
+                if (tr0 < 0 && tr1 < 0) {
+                    mbar_arrive(&P.full[s]);
+                } else {
+                    uint8_t *dst = P.ring[s];
+                    mbar_arrive_expect_tx(&P.full[s], (tr0 >= 0 ? 2 * C::UNITB : 0) + (tr1 >= 0 ? 2 * C::UNITB : 0));
+                    if (tr0 >= 0) {
+                        ptma_2d(dst, &tmk, 0, tr0, &P.full[s], policy);
+                        ptma_2d(dst + 2 * C::UNITB, &tmv, 0, tr0, &P.full[s], policy);
+                    }
+                    if (tr1 >= 0) {
+                        ptma_2d(dst + C::UNITB, &tmk, 0, tr1, &P.full[s], policy);
+                        ptma_2d(dst + 3 * C::UNITB, &tmv, 0, tr1, &P.full[s], policy);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// combine for the persistent layout: rows of segment k are k + p for the
+// workers p that touched it
+// --------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(D) decode_combine_pers_kernel(DecodeArgs a, int Hkv, int G,
+                                                                 int nchunks, int W,
+                                                                 const int *ws_prefix) {
+    __shared__ uint32_t s_flags;
+    __shared__ float s_red[D / 32];
+    const int Hq = Hkv * G;
+    const int b = blockIdx.x / Hq, hq = blockIdx.x - b * Hq, h = hq / G, g = hq - h * G;
+    const int tid = threadIdx.x;
+    const int K = gridDim.x / Hq * Hkv * nchunks;  // B * Hkv * nchunks
+    const long long U = ws_prefix[K];
+    W = (int)min((long long)W, U);  // as in the split kernel
+    if (tid == 0) s_flags = 0;
+    __syncthreads();
+    uint32_t f = 0;
+    for (int i = tid; i < Hkv; i += D) {
+        const int ni = a.seq_lens[(long long)b * a.len_sb + (long long)i * a.len_sh];
+        if (ni < 0 || (long long)ni > (long long)a.max_pages * kPage || ni > a.max_seq_len)
+            f |= PFKV_FLAG_BAD_LENGTH;
+        if (a.hflags) f |= a.hflags[b * Hkv + i];
+    }
+    if (f) atomicOr(&s_flags, f);
+    __syncthreads();
+    if (s_flags == 0 && U > 0) {
+        f = 0;
+        for (int i = 0; i < Hkv; ++i) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int k = (b * Hkv + i) * nchunks + c;
+                const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+                if (u1 == u0) continue;
+                const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
+                for (int p = p0 + tid; p <= p1; p += D) f |= a.status[k + p];
+            }
+        }
+        if (f) atomicOr(&s_flags, f);
+        __syncthreads();
+    }
+    const uint32_t flags = s_flags;
+    if (hq == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
+    __nv_bfloat16 *out = a.out + ((long long)b * Hq + hq) * D;
+    const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+    if (flags != 0 || n == 0 || U == 0) {
+        out[tid] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    // maximum log2-sum-exp over this head's rows
+    float M = -INFINITY;
+    for (int c = 0; c < nchunks; ++c) {
+        const int k = (b * Hkv + h) * nchunks + c;
+        const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+        if (u1 == u0) continue;
+        const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
+        for (int p = p0 + tid; p <= p1; p += D) M = fmaxf(M, a.lse[(long long)(k + p) * G + g]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if ((tid & 31) == 0) s_red[tid >> 5] = M;
+    __syncthreads();
+    M = s_red[0];
+#pragma unroll
+    for (int i = 1; i < D / 32; ++i) M = fmaxf(M, s_red[i]);
+    float acc = 0.f, wsum = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+        const int k = (b * Hkv + h) * nchunks + c;
+        const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+        if (u1 == u0) continue;
+        const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
+        for (int p = p0; p <= p1; ++p) {
+            const long long row = k + p;
+            const float lc = a.lse[row * G + g];
+            const float wt = lc == -INFINITY ? 0.f : pexp2(lc - M);
+            wsum += wt;
+            acc = fmaf(wt, a.o[(row * G + g) * D + tid], acc);
+        }
+    }
+    out[tid] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+}
+
+// --------------------------------------------------------------------------
+// host side
+// --------------------------------------------------------------------------
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn_p() {
+    static std::atomic<EncodeFn> fn{nullptr};
+    EncodeFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        f = reinterpret_cast<EncodeFn>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+bool encode_map_p(CUtensorMap *map, const void *pool, long long rows) {
+    EncodeFn f = encode_fn_p();
+    if (!f) return false;
+    cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, (cuuint32_t)kPage};
+    cuuint32_t estr[2] = {1, 1};
+    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int G>
+cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    using C = PersCfg<G>;
+    const size_t smem = sizeof(typename C::Smem) + 1024;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(decode_split_pers_kernel<G>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    CUtensorMap tk, tv;
+    const long long rows = (long long)a.num_pages * p.Hkv * kPage;
+    if (!encode_map_p(&tk, a.k_pages, rows) || !encode_map_p(&tv, a.v_pages, rows))
+        return cudaErrorInvalidValue;
+    decode_split_pers_kernel<G><<<p.pers_ctas, C::NT, smem, s>>>(
+        tk, tv, a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int pers_workers_per_cta() { return PersCfg<4>::PAIRS; }
+
+bool pers_supported(const DecodePlan &p, int num_pages) {
+    const long long rows = (long long)num_pages * p.Hkv * kPage;
+    const long long K = (long long)p.B * p.Hkv * p.nchunks;
+    return p.dtype == PFKV_KV_FP8_E4M3 && p.D == 128 && p.G <= 4 && rows < (1LL << 31) &&
+           K <= PersCfg<4>::MAXK && p.B <= PersCfg<4>::MAXB;
+}
+
+cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    switch (p.G) {
+        case 1: return launch_pers_g<1>(a, p, s);
+        case 2: return launch_pers_g<2>(a, p, s);
+        case 4: return launch_pers_g<4>(a, p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    decode_combine_pers_kernel<128><<<(unsigned)(p.B * p.Hq), 128, 0, s>>>(
+        a, p.Hkv, p.G, p.nchunks, p.pers_ctas * PersCfg<4>::PAIRS, a.ws_prefix);
+    return cudaGetLastError();
+}
+
+}  // namespace pfkv

@@ -29,8 +29,14 @@ struct DecodePlan {
     int chunk_tokens;   // tokens per split-KV chunk (multiple of 16)
     int nchunks;        // ceil(max_seq_len / chunk_tokens), >= 1
     bool tags;
+    // kind 0: one CTA per (request, kv head, chunk), workspace rows indexed
+    //         [b][hq][chunk];
+    // kind 1: persistent balanced workers (FP8, head_dim 128, G <= 4), rows
+    //         indexed segment + worker, pers_ctas CTAs
+    int kind;
+    int pers_ctas, workers;
     // workspace layout (byte offsets, 256-aligned)
-    size_t off_hflags, off_status, off_lse, off_o, total;
+    size_t off_hflags, off_status, off_lse, off_o, off_prefix, total;
 };
 
 struct DecodeArgs {
@@ -56,6 +62,7 @@ struct DecodeArgs {
     uint32_t *status;   // [B][Hkv][nchunks]
     float *lse;         // [B][Hq][nchunks]  log2-sum-exp of the chunk
     float *o;           // [B][Hq][nchunks][D] chunk output (normalised)
+    int *ws_prefix;     // persistent kind: exclusive unit prefix per segment
 };
 
 struct AppendArgs {
@@ -78,6 +85,12 @@ struct AppendArgs {
 cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s);
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+bool swz_supported(const DecodePlan &p, int num_pages);
+bool pers_supported(const DecodePlan &p, int num_pages);
+int pers_workers_per_cta();
+cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_split_swz(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *out, cudaStream_t s);
 cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStream_t s);

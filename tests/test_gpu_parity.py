@@ -219,3 +219,12 @@ def test_repeat_calls_are_deterministic(B):
         db.attend()
     torch.cuda.synchronize()
     assert torch.equal(first, db.out)
+
+
+def test_many_segments_fallback_path(B):
+    """More (request, kv head, chunk) segments than the persistent kernel's
+    prefix table holds: the per-chunk kernel takes over; same results."""
+    lens = np.array([3000, 2900, 2950], dtype=np.int32)
+    spec = W.Spec("manyseg", B=3, Hq=32, Hkv=8, D=128, kv_dtype="fp8", num_pages=1024,
+                  lens=lens, tags=True, split_tokens=16, seed=404)
+    run_and_compare(spec, label="many-segments")
