@@ -221,6 +221,37 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
                                           uint8_t *flags, uint32_t stages, void *stream);
 
 /*
+ * pfkv_paged_decode_attn_noalloc -- pfkv_paged_decode_attn without a
+ * caller-provided workspace.  (The source pages have no counterpart to this
+ * call; it exists for callers, not for the method.)
+ *
+ * For callers that cannot allocate device memory when they decode: an engine
+ * that has already given all GPU memory to its weights and KV page pool, a
+ * plugin whose host framework owns every device allocation, or a decode loop
+ * that must not call cudaMalloc/cudaFree because they can synchronise the
+ * device.  The workspace is instead a file-scope device array of
+ * PFKV_NOALLOC_WORKSPACE_BYTES inside this library; every GPU that loads the
+ * library holds it until the process exits.  This call allocates nothing.
+ *
+ * Arguments, results and errors are those of pfkv_paged_decode_attn, plus:
+ *  - a call that would need more than PFKV_NOALLOC_WORKSPACE_BYTES of
+ *    workspace (pfkv_decode_workspace_size) returns PFKV_ERR_WORKSPACE and
+ *    enqueues nothing;
+ *  - the first call with a given device current looks up the array's device
+ *    address (cudaGetSymbolAddress) for that device; make that first call
+ *    before capturing the stream into a CUDA graph;
+ *  - all calls share the one array, which keeps the previous call's contents
+ *    (this is harmless: the workspace's contents on entry are ignored).  Two
+ *    calls whose work overlaps on the GPU (different streams, or different
+ *    host threads without ordering) race on it and may return wrong results.
+ */
+#define PFKV_NOALLOC_WORKSPACE_BYTES (16u << 20)
+pfkv_status pfkv_paged_decode_attn_noalloc(const pfkv_cache *cache, const pfkv_pages *pages,
+                                           const void *q, int32_t num_q_heads, float sm_scale,
+                                           int32_t split_tokens, int32_t max_seq_len, void *out,
+                                           uint8_t *flags, void *stream);
+
+/*
  * pfkv_e4m3_encode -- out[i] = e4m3 code of x[i] (fp32), round to nearest
  * even, saturating to +-448, NaN -> 0x7F: the conversion kv_append uses.
  * x: fp32 [n], out: uint8 [n] (device).  n >= 0.

@@ -41,7 +41,7 @@ PFKV_STAGE_ALL = 0x7
 
 # every symbol include/pfkv.h declares
 EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",
-            "pfkv_paged_decode_attn_stages", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string", "pfkv_abi_version")
+            "pfkv_paged_decode_attn_stages", "pfkv_paged_decode_attn_noalloc", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string", "pfkv_abi_version")
 
 
 class PfkvError(RuntimeError):
@@ -95,6 +95,10 @@ def lib() -> ctypes.CDLL:
                                                     ctypes.c_float, I32, I32, P, ctypes.c_size_t,
                                                     P, P, ctypes.c_uint32, P]
         L.pfkv_paged_decode_attn_stages.restype = ctypes.c_int
+        L.pfkv_paged_decode_attn_noalloc.argtypes = [ctypes.POINTER(_CCache),
+                                                     ctypes.POINTER(_CPages), P, I32,
+                                                     ctypes.c_float, I32, I32, P, P, P]
+        L.pfkv_paged_decode_attn_noalloc.restype = ctypes.c_int
         L.pfkv_e4m3_encode.argtypes = [P, I64, P, P]
         L.pfkv_e4m3_encode.restype = ctypes.c_int
         L.pfkv_e4m3_decode.argtypes = [P, I64, P, P]
@@ -238,6 +242,23 @@ def pfkv_paged_decode_attn_stages(cache: Cache, pages: Pages, q: torch.Tensor, s
         ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
         int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), _ptr(flags), int(stages), _stream(stream)), "pfkv_paged_decode_attn_stages")
+
+
+# bytes of the library's own workspace used by pfkv_paged_decode_attn_noalloc
+PFKV_NOALLOC_WORKSPACE_BYTES = 16 << 20
+
+
+def pfkv_paged_decode_attn_noalloc(cache: Cache, pages: Pages, q: torch.Tensor, sm_scale: float,
+                                   split_tokens: int, max_seq_len: int, out: torch.Tensor,
+                                   flags: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pfkv_paged_decode_attn with the library's built-in workspace, for
+    callers that cannot allocate device memory (see include/pfkv.h)."""
+    c, p = cache.c_struct(), pages.c_struct()
+    Hq = int(q.shape[1])
+    _check(lib().pfkv_paged_decode_attn_noalloc(
+        ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
+        int(max_seq_len), _ptr(out), _ptr(flags), _stream(stream)),
+        "pfkv_paged_decode_attn_noalloc")
 
 
 def pfkv_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:

@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert names == sorted(["pfkv_abi_version", "pfkv_decode_workspace_size", "pfkv_e4m3_decode",
                             "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_paged_decode_attn",
-                            "pfkv_paged_decode_attn_stages", "pfkv_status_string"])
+                            "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
+                            "pfkv_status_string"])
 
 
 def test_library_exports_every_declared_symbol(B):
