@@ -178,6 +178,30 @@ class PreparedStep:
             raise RuntimeError(f"pfkv_paged_decode_attn_stages: status {st}")
 
 
+def profiled_traffic(bytes_per_launch: float):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    scaled to this run's algorithmic bytes; None if the kernel source changed
+    since the capture (or there is no summary)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_split_pers_llama8b_fp8.md")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        parts = line.strip().split(": ", 1)
+        if len(parts) == 2:
+            kv[parts[0]] = parts[1]
+    try:
+        src = os.path.join(ROOT, kv["kernel_source"])
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if digest != kv["kernel_source_sha256_16"]:
+            return None
+        return float(kv["dram_bytes_per_launch"]) * bytes_per_launch / float(
+            kv["algorithmic_bytes_per_launch"])
+    except (KeyError, OSError, ValueError):
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -303,7 +327,9 @@ def run_gpu(args):
             "pct_of_hbm_peak": round(100 * value / world / peak, 2),
             "roofline": {"kernel": "decode_split", "bound": "hbm",
                          "achieved": round(split_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(split_gbs / peak, 4), "traffic": None,
+                         "frac": round(split_gbs / peak, 4),
+                         "traffic": (None if profiled_traffic(split_bytes) is None
+                                     else int(profiled_traffic(split_bytes))),
                          "peak_kind": peak_kind, "avg_launch_us": round(split_avg * 1e6, 3),
                          "bytes_per_launch": int(split_bytes)},
             "e2e": e2e, "gpu_launches": K * (3 if args.no_tags else 4),
@@ -401,9 +427,9 @@ def _time_oracle(oracle, cache, pages, q, sub, batch):
 def cpu_baseline(db, target_s: float = 15.0):
     """Oracle KV GB/s on host cores over a bounded sample of the workload."""
     spec = db.spec
-    oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, 2, spec.Hkv, spec.seed + 555)
+    oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, 4, spec.Hkv, spec.seed + 555)
     t = _time_oracle(oracle, cache, pages, q, sub, batch)
-    reps = max(1, min(50, int(target_s / max(t, 1e-3))))
+    reps = max(1, min(400, int(target_s / max(t, 1e-3))))
     total = t
     for _ in range(reps - 1):
         total += _time_oracle(oracle, cache, pages, q, sub, batch)
