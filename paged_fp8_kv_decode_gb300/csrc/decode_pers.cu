@@ -17,8 +17,9 @@
 // segment it touches, at row index segment + worker, which is unique.
 //
 // Workers.  A worker is a pair of warps sharing a 3-stage shared-memory ring
-// (8 KB per stage: K and V slabs of a 2-unit granule, TMA tile loads with the
-// 128-byte swizzle):
+// (8 KB per stage: K and V slabs of a 2-unit granule, each slab one 2 KB 1-D
+// bulk copy; a quarter-warp reads one 128-byte row, so the linear layout is
+// free of bank conflicts):
 //  * the score warp holds a 16-dim slice of the G query heads in registers
 //    (lane (t, c): slice c, token 4r + t in pass r), converts K bytes to fp32
 //    pairs, takes packed fp32x2 dot products, finishes each score with a
@@ -33,7 +34,6 @@
 // Splitting scores and values over two warps halves the registers each needs,
 // so 12 warps fit an SM, and the two phases of neighbouring granules overlap.
 #include <atomic>
-#include <cuda.h>
 
 #include "pfkv_internal.cuh"
 
@@ -57,15 +57,6 @@ __device__ __forceinline__ float pwarp_max(float x) {
     float m;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(x));
     return m;
-}
-
-__device__ __forceinline__ void ptma_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                        uint64_t *bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
@@ -119,26 +110,23 @@ struct PersCfg {
     static constexpr int NT = PAIRS * 64;
     static constexpr int MAXK = 4096;            // segments (prefix array in smem)
     static constexpr int MAXB = 4096;            // requests
-    enum : int { F_RESCALE = 1, F_SEGEND = 2 };
-    struct alignas(16) PBuf {
-        float p[GT][2 * G];   // [token row][g pairs]: probability x V scale, twice
-        float alpha[G];
-        float m[G], l[G];
-        int flags, nv0, nv1, row;
-        int tma_row0, tma_row1;  // K/V tile rows of the granule ST ahead (-1: none)
-        uint32_t status;
-        int pad[1];
+    // raw scores of one granule, row = the writing lane (lane (t, c) holds
+    // token 4c + t), handed from the score warp to the value warp
+    struct alignas(16) SBuf {
+        float s[GT][G];
     };
     struct Pair {
         alignas(1024) uint8_t ring[STAGES][STAGEB];
-        alignas(16) PBuf pb[STAGES];
+        alignas(16) SBuf sb[STAGES];
+        alignas(16) float p[GT][2 * G];   // value warp: probability x V scale, as pairs
         alignas(16) __nv_bfloat16 q[2][G][D];
         alignas(8) uint64_t full[STAGES];
-        alignas(8) uint64_t pready[STAGES];
+        alignas(8) uint64_t sready[STAGES];
         alignas(8) uint64_t qbar[2];
         int ngran;
+        uint32_t score_status;            // timeouts seen by the score warp
     };
-    static_assert(sizeof(PBuf) % 16 == 0, "vector stores into every stage buffer");
+    static_assert(sizeof(SBuf) % 16 == 0, "vector stores into every stage buffer");
     struct Smem {
         Pair pair[PAIRS];
         int prefix[MAXK + 1];
@@ -162,9 +150,8 @@ __device__ __forceinline__ int seg_of(const int *prefix, int K, long long x) {
 
 template <int G>
 __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
-    decode_split_pers_kernel(const __grid_constant__ CUtensorMap tmk,
-                             const __grid_constant__ CUtensorMap tmv, DecodeArgs a, int Hkv,
-                             int B, int nchunks, int chunk_tokens, int *ws_prefix) {
+    decode_split_pers_kernel(DecodeArgs a, int Hkv, int B, int nchunks, int chunk_tokens,
+                             int *ws_prefix) {
     using C = PersCfg<G>;
     constexpr int ST = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -238,18 +225,37 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     if (U == 0) return;
 
     // ---------------- the worker ----------------
+    // Warps map to the SM's four sub-partitions by warp index mod 4; score
+    // warps are 0..PAIRS-1 and value warps PAIRS..2*PAIRS-1 so that the
+    // FMA-heavy score warps spread over all four sub-partitions.
     const int warp = tid >> 5, lane = tid & 31;
-    const int pi = warp >> 1;           // pair index in the CTA
-    const bool is_score = (warp & 1) == 0;
+    const int pi = warp % C::PAIRS;     // pair index in the CTA
+    const bool is_score = warp < C::PAIRS;
     typename C::Pair &P = sm.pair[pi];
     const int w = blockIdx.x * C::PAIRS + pi;
     const long long x0 = w < W ? ((long long)w * U + W - 1) / W : U;
     const long long x1 = w < W ? ((long long)(w + 1) * U + W - 1) / W : U;
     const int vt = lane >> 3, vc = lane & 7;
-    const uint64_t policy = l2_policy_evict_first();
+
+    // granule cursor (2 units, never across a segment), shared logic of both warps
+    struct Cursor {
+        long long x, seg_end;
+        int k;
+    };
+    auto cursor_init = [&](Cursor &c) {
+        c.x = x0;
+        c.k = seg_of(sm.prefix, K, x0);
+        c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
+    };
+    auto cursor_next = [&](Cursor &c, int n) {
+        c.x += n;
+        if (c.x >= c.seg_end && c.x < x1) {
+            c.k = seg_of(sm.prefix, K, c.x);
+            c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
+        }
+    };
 
     if (is_score) {
-        // count this worker's granules (2 units each, never across a segment)
         int ngran = 0;
         if (x0 < x1) {
             long long x = x0;
@@ -264,9 +270,10 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
         }
         if (lane == 0) {
             P.ngran = ngran;
+            P.score_status = 0;
             for (int s = 0; s < ST; ++s) {
                 mbar_init(&P.full[s], 1);
-                mbar_init(&P.pready[s], 1);
+                mbar_init(&P.sready[s], 1);
             }
             mbar_init(&P.qbar[0], 1);
             mbar_init(&P.qbar[1], 1);
@@ -276,15 +283,137 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     named_sync(1 + pi, 64);
     const int ngran = P.ngran;
     if (ngran == 0) return;
+    const uint64_t policy = l2_policy_evict_first();
 
     if (is_score) {
         // ===================== score warp =====================
+        // q slice of the current segment in registers; K dot products; the
+        // reduce-scatter; raw scores to the value warp.
+        Cursor con;
+        cursor_init(con);
+        auto q_copy = [&](int slot, int k) {  // lane 0
+            const int bh = k / nchunks;
+            const __nv_bfloat16 *src = a.q + (long long)bh * G * C::D;  // (b*Hkv + h)*G rows
+            mbar_arrive_expect_tx(&P.qbar[slot], G * C::D * 2);
+            bulk_g2s(&P.q[slot][0][0], src, G * C::D * 2, &P.qbar[slot], policy);
+        };
+        int seg_ord = 0;
+        int next_seg_k = -1;
+        if (lane == 0) q_copy(0, con.k);
+        if (con.seg_end < x1) {
+            next_seg_k = seg_of(sm.prefix, K, con.seg_end);
+            if (lane == 0) q_copy(1, next_seg_k);
+        }
+        float2 q2[G][8];
+        uint32_t full_phase = 0, q_phase = 0, status = 0;
+        bool seg_start = true;
+        for (int i = 0; i < ngran; ++i) {
+            const int s = i % ST;
+            if (seg_start) {
+                const int slot = seg_ord & 1;
+                if (!mbar_wait_bounded(&P.qbar[slot], (q_phase >> slot) & 1u)) status |= kStatusTimeout;
+                q_phase ^= 1u << slot;
+                const __nv_bfloat16 *qs = &P.q[slot][0][0];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16);
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16 + 8);
+                    const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 f = bf16x2_to_float2(ws[e]);
+                        q2[g][e] = make_float2(f.x * a.q_scale, f.y * a.q_scale);
+                    }
+                }
+                __syncwarp();
+                // the slot just read is free: prefetch the segment after next
+                if (next_seg_k >= 0) {
+                    const long long e = min((long long)sm.prefix[next_seg_k + 1], x1);
+                    const int k2 = e < x1 ? seg_of(sm.prefix, K, e) : -1;
+                    if (k2 >= 0 && lane == 0) {
+                        fence_proxy_async_smem();
+                        q_copy(slot, k2);
+                    }
+                    next_seg_k = k2;
+                }
+                seg_start = false;
+            }
+            const int n_units = (int)min((long long)2, con.seg_end - con.x);
+            if (!mbar_wait_bounded(&P.full[s], (full_phase >> s) & 1u)) status |= kStatusTimeout;
+            full_phase ^= 1u << s;
+            const uint8_t *stage = P.ring[s];
+
+            // ---- partial dot products: slice vc, token 4r + vt ----
+            // Passes r and r + 4 are computed together and folded at once by the
+            // first reduce-scatter level (xor 4), so at most 24 partials are live.
+            const bool bA = vc & 4, bB = vc & 2, bC = vc & 1;
+            float r1[4][G], r2[2][G], sc[G];
+            auto dot_pass = [&](int r, float (&pr)[G]) {
+                const int row = 4 * (r & 3) + vt;
+                const uint8_t *krow = stage + (r >> 2) * C::UNITB + row * C::ROWB;
+                const uint4 wv = *reinterpret_cast<const uint4 *>(krow + (vc << 4));
+                float2 kf[8];
+                pdequant16(wv, kf);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float2 acc = __fmul2_rn(q2[g][0], kf[0]);
+#pragma unroll
+                    for (int e = 1; e < 8; ++e) acc = __ffma2_rn(q2[g][e], kf[e], acc);
+                    pr[g] = acc.x + acc.y;
+                }
+            };
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float lo[G], hi[G];
+                dot_pass(r, lo);
+                dot_pass(r + 4, hi);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float snd = bA ? lo[g] : hi[g];
+                    const float kp = bA ? hi[g] : lo[g];
+                    r1[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 4);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float snd = bB ? r1[r][g] : r1[r + 2][g];
+                    const float kp = bB ? r1[r + 2][g] : r1[r][g];
+                    r2[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 2);
+                }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float snd = bC ? r2[0][g] : r2[1][g];
+                const float kp = bC ? r2[1][g] : r2[0][g];
+                sc[g] = kp + __shfl_xor_sync(0xffffffffu, snd, 1);
+            }
+            // lane (vt, vc) now holds the G raw scores of token 4 vc + vt
+            if constexpr (G == 4) {
+                *reinterpret_cast<float4 *>(P.sb[s].s[lane]) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+            } else if constexpr (G == 2) {
+                *reinterpret_cast<float2 *>(P.sb[s].s[lane]) = make_float2(sc[0], sc[1]);
+            } else {
+                P.sb[s].s[lane][0] = sc[0];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&P.sready[s]);
+            const bool seg_end = con.x + n_units >= con.seg_end;
+            cursor_next(con, n_units);
+            if (seg_end) {
+                seg_start = true;
+                ++seg_ord;
+            }
+        }
+        if (status && lane == 0) atomicOr(&P.score_status, status);
+    } else {
+        // ===================== value warp =====================
         // unit metadata window: lane l holds unit base + l (cur) and
         // base + 32 + l (nxt): page id (-1 bad, -2 absent) and the two scales
         long long base = x0;
         int cphys, nphys;
         float cks, cvs, nks, nvs;
-        uint32_t cbad, nbad;  // bad-page bit of the lane's unit
+        uint32_t cbad, nbad;
         auto load_ids = [&](long long bx, int &phys, uint32_t &bad) {
             const long long x = bx + lane;
             phys = -2;
@@ -299,7 +428,7 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                     phys = -1;
                     bad = kStatusBadPage;
                 } else {
-                    phys = id * Hkv + h;  // unit index = tile row / 16
+                    phys = id * Hkv + h;  // unit index
                 }
             }
         };
@@ -312,7 +441,6 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
         load_ids(base + 32, nphys, nbad);
         load_scales(cphys, cks, cvs);
         load_scales(nphys, nks, nvs);
-        // metadata of unit x (must lie in [base, base + 64))
         // (uniform branches, not selects: a select would wait for the next
         // window's loads even when only the current one is read)
         auto unit_phys = [&](long long x) {
@@ -335,118 +463,49 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
             if (d < 32) return __shfl_sync(0xffffffffu, cbad, d);
             return __shfl_sync(0xffffffffu, nbad, d - 32);
         };
-
-        // cursors over the granule sequence
-        struct Cursor {
-            long long x, seg_end;
-            int k;
-        };
-        auto cursor_init = [&](Cursor &c) {
-            c.x = x0;
-            c.k = seg_of(sm.prefix, K, x0);
-            c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
-        };
-        auto cursor_next = [&](Cursor &c, int n) {
-            c.x += n;
-            if (c.x >= c.seg_end && c.x < x1) {
-                c.k = seg_of(sm.prefix, K, c.x);
-                c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
-            }
-        };
         Cursor iss, con;
         cursor_init(iss);
         cursor_init(con);
-        // tile rows (unit index * 16) of the granule at cursor c, -1 if absent/bad
-        auto granule_rows = [&](const Cursor &c, int &r0, int &r1) {
+        // load (or mark empty) the granule at cursor c into stage s; lane 0 issues
+        auto issue_at = [&](const Cursor &c, int s) {
             const int n = (int)min((long long)2, c.seg_end - c.x);
             const int p0 = unit_phys(c.x);
             const int p1 = n == 2 ? unit_phys(c.x + 1) : -2;
-            r0 = p0 >= 0 ? p0 * kPage : -1;
-            r1 = p1 >= 0 ? p1 * kPage : -1;
+            if (lane == 0) {
+                if (p0 < 0 && p1 < 0) {
+                    mbar_arrive(&P.full[s]);
+                } else {
+                    uint8_t *dst = P.ring[s];
+                    const uint8_t *kp = static_cast<const uint8_t *>(a.k_pages);
+                    const uint8_t *vp = static_cast<const uint8_t *>(a.v_pages);
+                    mbar_arrive_expect_tx(&P.full[s], (p0 >= 0 ? 2 * C::UNITB : 0) + (p1 >= 0 ? 2 * C::UNITB : 0));
+                    if (p0 >= 0) {
+                        bulk_g2s(dst, kp + (long long)p0 * C::UNITB, C::UNITB, &P.full[s], policy);
+                        bulk_g2s(dst + 2 * C::UNITB, vp + (long long)p0 * C::UNITB, C::UNITB, &P.full[s], policy);
+                    }
+                    if (p1 >= 0) {
+                        bulk_g2s(dst + C::UNITB, kp + (long long)p1 * C::UNITB, C::UNITB, &P.full[s], policy);
+                        bulk_g2s(dst + 3 * C::UNITB, vp + (long long)p1 * C::UNITB, C::UNITB, &P.full[s], policy);
+                    }
+                }
+            }
             return n;
         };
-        auto issue = [&](int s, int r0, int r1) {  // lane 0: load or mark empty
-            if (r0 < 0 && r1 < 0) {
-                mbar_arrive(&P.full[s]);
-                return;
-            }
-            uint8_t *dst = P.ring[s];
-            mbar_arrive_expect_tx(&P.full[s], (r0 >= 0 ? 2 * C::UNITB : 0) + (r1 >= 0 ? 2 * C::UNITB : 0));
-            if (r0 >= 0) {
-                ptma_2d(dst, &tmk, 0, r0, &P.full[s], policy);
-                ptma_2d(dst + 2 * C::UNITB, &tmv, 0, r0, &P.full[s], policy);
-            }
-            if (r1 >= 0) {
-                ptma_2d(dst + C::UNITB, &tmk, 0, r1, &P.full[s], policy);
-                ptma_2d(dst + 3 * C::UNITB, &tmv, 0, r1, &P.full[s], policy);
-            }
-        };
-        // prime the ring
-        for (int j = 0; j < ST && j < ngran; ++j) {
-            int r0, r1;
-            const int n = granule_rows(iss, r0, r1);
-            if (lane == 0) issue(j, r0, r1);
-            cursor_next(iss, n);
-        }
-        // query of the first segment (and the next) into the two q slots
-        auto q_copy = [&](int slot, int k) {  // lane 0
-            const int bh = k / nchunks;
-            const __nv_bfloat16 *src = a.q + (long long)bh * G * C::D;  // (b*Hkv + h)*G rows
-            mbar_arrive_expect_tx(&P.qbar[slot], G * C::D * 2);
-            bulk_g2s(&P.q[slot][0][0], src, G * C::D * 2, &P.qbar[slot], policy);
-        };
-        int seg_ord = 0;          // ordinal of the segment being scored
-        int next_seg_k = -1;      // segment whose q is loading in the other slot
-        if (lane == 0) q_copy(0, con.k);
-        {
-            // next segment after the first one, if the range reaches it
-            if (con.seg_end < x1) {
-                next_seg_k = seg_of(sm.prefix, K, con.seg_end);
-                if (lane == 0) q_copy(1, next_seg_k);
-            }
-        }
+        for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
 
-        float2 q2[G][8];
         float m[G], l[G];
-        uint32_t seg_status = 0;
-        uint32_t full_phase = 0, q_phase = 0;
-        bool seg_start = true;
-        bool pending_scales = false;   // nxt ids loaded, scales not yet
-
+        float2 o[G][8];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
+        }
+        uint32_t sr_phase = 0, seg_status = 0;
+        bool pending_scales = false;
         for (int i = 0; i < ngran; ++i) {
             const int s = i % ST;
-            if (seg_start) {
-                seg_status = 0;
-                const int slot = seg_ord & 1;
-                if (!mbar_wait_bounded(&P.qbar[slot], (q_phase >> slot) & 1u)) seg_status |= kStatusTimeout;
-                q_phase ^= 1u << slot;
-                const __nv_bfloat16 *qs = &P.q[slot][0][0];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const uint4 w0 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16);
-                    const uint4 w1 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16 + 8);
-                    const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float2 f = bf16x2_to_float2(ws[e]);
-                        q2[g][e] = make_float2(f.x * a.q_scale, f.y * a.q_scale);
-                    }
-                    m[g] = -INFINITY;
-                    l[g] = 0.f;
-                }
-                __syncwarp();
-                // the slot just read is free: prefetch the segment after next
-                if (next_seg_k >= 0) {
-                    const long long e = min((long long)sm.prefix[next_seg_k + 1], x1);
-                    const int k2 = e < x1 ? seg_of(sm.prefix, K, e) : -1;
-                    if (k2 >= 0 && lane == 0) {
-                        fence_proxy_async_smem();
-                        q_copy(slot, k2);
-                    }
-                    next_seg_k = k2;
-                }
-                seg_start = false;
-            }
             // metadata window upkeep
             if (pending_scales) {
                 load_scales(nphys, nks, nvs);
@@ -461,73 +520,33 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
             const int n_units = (int)min((long long)2, con.seg_end - con.x);
             const int ph0 = unit_phys(con.x);
             const int ph1 = n_units == 2 ? unit_phys(con.x + 1) : -2;
-            const bool u0 = ph0 >= 0, u1 = ph1 >= 0;
             seg_status |= unit_bad(con.x) | (n_units == 2 ? unit_bad(con.x + 1) : 0u);
-            // tokens per unit: 16, except the segment's last unit
             const long long seg_last = (long long)sm.prefix[con.k + 1] - 1;
             const int lnv = sm.last_nv[con.k];
-            const int nv0 = u0 ? (con.x == seg_last ? lnv : kPage) : 0;
-            const int nv1 = u1 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
+            const int nv0 = ph0 >= 0 ? (con.x == seg_last ? lnv : kPage) : 0;
+            const int nv1 = ph1 >= 0 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
             const float ks0 = unit_ks(con.x), ks1 = n_units == 2 ? unit_ks(con.x + 1) : 0.f;
             const float vs0 = unit_vs(con.x), vs1 = n_units == 2 ? unit_vs(con.x + 1) : 0.f;
 
-            // wait for the K/V tiles (or the empty marker) of this granule
-            if (!mbar_wait_bounded(&P.full[s], (full_phase >> s) & 1u)) seg_status |= kStatusTimeout;
-            full_phase ^= 1u << s;
-            const uint8_t *stage = P.ring[s];
+            if (!mbar_wait_bounded(&P.sready[s], (sr_phase >> s) & 1u)) seg_status |= kStatusTimeout;
+            sr_phase ^= 1u << s;
 
-            // ---- partial dot products: slice vc, token 4r + vt ----
-            float part[8][G];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int row = 4 * (r & 3) + vt;
-                const uint8_t *krow = stage + (r >> 2) * C::UNITB + row * C::ROWB;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(krow + ((vc ^ (row & 7)) << 4));
-                float2 kf[8];
-                pdequant16(wv, kf);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float2 acc = __fmul2_rn(q2[g][0], kf[0]);
-#pragma unroll
-                    for (int e = 1; e < 8; ++e) acc = __ffma2_rn(q2[g][e], kf[e], acc);
-                    part[r][g] = acc.x + acc.y;
-                }
-            }
-            // ---- reduce-scatter: lane vc gets token 4 vc + vt ----
-            const bool bA = vc & 4, bB = vc & 2, bC = vc & 1;
-            float r1[4][G], r2[2][G], sc[G];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float snd = bA ? part[r][g] : part[r + 4][g];
-                    const float kp = bA ? part[r + 4][g] : part[r][g];
-                    r1[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 4);
-                }
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float snd = bB ? r1[r][g] : r1[r + 2][g];
-                    const float kp = bB ? r1[r + 2][g] : r1[r][g];
-                    r2[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 2);
-                }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float snd = bC ? r2[0][g] : r2[1][g];
-                const float kp = bC ? r2[1][g] : r2[0][g];
-                sc[g] = kp + __shfl_xor_sync(0xffffffffu, snd, 1);
-            }
-            const int my_tok = 4 * vc + vt;   // 0..31
-            const int my_u = vc >> 2;
-            const int my_row = my_tok & 15;
+            // ---- online softmax over the granule (lane: token 4 vc + vt) ----
+            const int my_u = vc >> 2, my_row = (4 * vc + vt) & 15;
             const bool ok = my_row < (my_u ? nv1 : nv0);
             const float ksc = my_u ? ks1 : ks0;
+            float sc[G];
+            if constexpr (G == 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(P.sb[s].s[lane]);
+                sc[0] = v4.x; sc[1] = v4.y; sc[2] = v4.z; sc[3] = v4.w;
+            } else if constexpr (G == 2) {
+                const float2 v2 = *reinterpret_cast<const float2 *>(P.sb[s].s[lane]);
+                sc[0] = v2.x; sc[1] = v2.y;
+            } else {
+                sc[0] = P.sb[s].s[lane][0];
+            }
 #pragma unroll
             for (int g = 0; g < G; ++g) sc[g] = ok ? sc[g] * ksc : -INFINITY;
-
-            // ---- online softmax over the granule ----
-            typename C::PBuf &pb = P.pb[s];
             float mb[G];
             bool grow = false;
 #pragma unroll
@@ -535,16 +554,16 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 mb[g] = pwarp_max(sc[g]);
                 grow |= mb[g] > m[g] + kLazy;
             }
-            int flags = 0;
             if (grow) {
-                flags |= C::F_RESCALE;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float mn = fmaxf(m[g], mb[g]);
                     const float alpha = m[g] == -INFINITY ? 0.f : pexp2(m[g] - mn);
+                    const float2 a2 = make_float2(alpha, alpha);
                     m[g] = mn;
                     l[g] *= alpha;
-                    if (lane == 0) pb.alpha[g] = alpha;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[g][e] = __fmul2_rn(o[g][e], a2);
                 }
             }
             {
@@ -552,13 +571,13 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 float pp[2 * G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float p = ok ? pexp2(sc[g] - m[g]) : 0.f;
-                    l[g] += p;
-                    pp[2 * g] = pp[2 * g + 1] = p * vsc;
+                    const float pr = ok ? pexp2(sc[g] - m[g]) : 0.f;
+                    l[g] += pr;
+                    pp[2 * g] = pp[2 * g + 1] = pr * vsc;
                 }
-                // rows transposed (t, c) -> 8 t + c so that a quarter-warp's
-                // stores land in consecutive rows
-                float *dstp = pb.p[8 * vt + vc];
+                // rows transposed (t, c) -> 8 t + c: a quarter-warp's stores land
+                // in consecutive rows
+                float *dstp = P.p[8 * vt + vc];
                 if constexpr (G >= 2) {
 #pragma unroll
                     for (int x = 0; x < G / 2; ++x)
@@ -568,78 +587,18 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                     *reinterpret_cast<float2 *>(dstp) = make_float2(pp[0], pp[1]);
                 }
             }
-            const bool seg_end = con.x + n_units >= con.seg_end;
-            if (seg_end) {
-                flags |= C::F_SEGEND;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float lt = l[g];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-                    if (lane == 0) {
-                        pb.m[g] = m[g];
-                        pb.l[g] = lt;
-                    }
-                }
-            }
-            // the granule ST ahead, for the value warp to load into this stage
-            int tr0 = -1, tr1 = -1;
-            if (i + ST < ngran) {
-                const int n = granule_rows(iss, tr0, tr1);
-                cursor_next(iss, n);
-            }
-            if (lane == 0) {
-                pb.flags = flags;
-                pb.nv0 = nv0;
-                pb.nv1 = nv1;
-                pb.row = con.k + w;
-                pb.status = seg_status;
-                pb.tma_row0 = tr0;
-                pb.tma_row1 = tr1;
-            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&P.pready[s]);
-            // advance
-            cursor_next(con, n_units);
-            if (seg_end) {
-                seg_start = true;
-                ++seg_ord;
-            }
-        }
-    } else {
-        // ===================== value warp =====================
-        float2 o[G][8];
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
-        uint32_t pr_phase = 0;
-        uint32_t vstatus = 0;
-        for (int i = 0; i < ngran; ++i) {
-            const int s = i % ST;
-            if (!mbar_wait_bounded(&P.pready[s], (pr_phase >> s) & 1u)) vstatus |= kStatusTimeout;
-            pr_phase ^= 1u << s;
-            const typename C::PBuf &pb = P.pb[s];
-            const int flags = pb.flags;
-            if (flags & C::F_RESCALE) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float al = pb.alpha[g];
-                    const float2 a2 = make_float2(al, al);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[g][e] = __fmul2_rn(o[g][e], a2);
-                }
-            }
+
+            // ---- values: lane (vt, vc) accumulates slice vc over tokens 4r + vt ----
             const uint8_t *stage = P.ring[s];
-            const int nv0 = pb.nv0, nv1 = pb.nv1;
             auto value_pass = [&](int r) {
                 const int row = 4 * (r & 3) + vt;
                 const uint8_t *vrow = stage + 2 * C::UNITB + (r >> 2) * C::UNITB + row * C::ROWB;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(vrow + ((vc ^ (row & 7)) << 4));
+                const uint4 wv = *reinterpret_cast<const uint4 *>(vrow + (vc << 4));
                 float2 vf[8];
                 pdequant16(wv, vf);
                 // token 4r + vt was scored by lane (t = vt, c = r): row 8 vt + r
-                const float2 *ps = reinterpret_cast<const float2 *>(pb.p[8 * vt + r]);
+                const float2 *ps = reinterpret_cast<const float2 *>(P.p[8 * vt + r]);
                 float2 pg[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) pg[g] = ps[g];
@@ -652,70 +611,55 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
 #pragma unroll
                 for (int r = 0; r < 8; ++r) value_pass(r);
             } else {
+                // tokens past the sequence end or in a missing unit are skipped:
+                // their rows may hold stale bytes (even NaN codes)
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int row = 4 * (r & 3) + vt;
                     if (row < ((r >> 2) ? nv1 : nv0)) value_pass(r);
                 }
             }
-            if (flags & C::F_SEGEND) {
-                // finish the segment: sum the token lanes, normalise, write the row
+            const bool seg_end = con.x + n_units >= con.seg_end;
+            if (seg_end) {
+                // finish the segment: sum the lanes, normalise, write the row
+                const int row = con.k + w;
 #pragma unroll
-                for (int g = 0; g < G; ++g)
+                for (int g = 0; g < G; ++g) {
+                    float lt = l[g];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
+                    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+                    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
 #pragma unroll
                         for (int off = 8; off < 32; off <<= 1) {
                             o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, off);
                             o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, off);
                         }
-                const int row = pb.row;
-                if (vt == 0) {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float L = pb.l[g];
-                        const float inv = L > 0.f ? 1.f / L : 0.f;
+                    }
+                    if (vt == 0) {
                         float4 *dst = reinterpret_cast<float4 *>(a.o + ((long long)row * G + g) * C::D + vc * 16);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             dst[e] = make_float4(o[g][2 * e].x * inv, o[g][2 * e].y * inv,
                                                  o[g][2 * e + 1].x * inv, o[g][2 * e + 1].y * inv);
                     }
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float L = pb.l[g];
-                        a.lse[(long long)row * G + g] = L > 0.f ? pb.m[g] + plog2(L) : -INFINITY;
-                    }
-                    a.status[row] = pb.status | vstatus;
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g)
+                    if (lane == 0) a.lse[(long long)row * G + g] = lt > 0.f ? m[g] + plog2(lt) : -INFINITY;
+                    m[g] = -INFINITY;
+                    l[g] = 0.f;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
-                vstatus = 0;
+                }
+                if (lane == 0) a.status[row] = seg_status | P.score_status;
+                seg_status = 0;
             }
             // refill this stage with the granule ST ahead
-            const int tr0 = pb.tma_row0, tr1 = pb.tma_row1;
             __syncwarp();
-            if (lane == 0 && i + ST < ngran) {
-                fence_proxy_async_smem();
-                if (tr0 < 0 && tr1 < 0) {
-                    mbar_arrive(&P.full[s]);
-                } else {
-                    uint8_t *dst = P.ring[s];
-                    mbar_arrive_expect_tx(&P.full[s], (tr0 >= 0 ? 2 * C::UNITB : 0) + (tr1 >= 0 ? 2 * C::UNITB : 0));
-                    if (tr0 >= 0) {
-                        ptma_2d(dst, &tmk, 0, tr0, &P.full[s], policy);
-                        ptma_2d(dst + 2 * C::UNITB, &tmv, 0, tr0, &P.full[s], policy);
-                    }
-                    if (tr1 >= 0) {
-                        ptma_2d(dst + C::UNITB, &tmk, 0, tr1, &P.full[s], policy);
-                        ptma_2d(dst + 3 * C::UNITB, &tmv, 0, tr1, &P.full[s], policy);
-                    }
-                }
+            if (i + ST < ngran) {
+                if (lane == 0) fence_proxy_async_smem();
+                cursor_next(iss, issue_at(iss, s));
             }
+            cursor_next(con, n_units);
         }
     }
 }
@@ -807,41 +751,6 @@ __global__ void __launch_bounds__(D) decode_combine_pers_kernel(DecodeArgs a, in
 // --------------------------------------------------------------------------
 namespace {
 
-using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn_p() {
-    static std::atomic<EncodeFn> fn{nullptr};
-    EncodeFn f = fn.load(std::memory_order_acquire);
-    if (!f) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !p) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        f = reinterpret_cast<EncodeFn>(p);
-        fn.store(f, std::memory_order_release);
-    }
-    return f;
-}
-
-bool encode_map_p(CUtensorMap *map, const void *pool, long long rows) {
-    EncodeFn f = encode_fn_p();
-    if (!f) return false;
-    cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {128, (cuuint32_t)kPage};
-    cuuint32_t estr[2] = {1, 1};
-    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int G>
 cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     using C = PersCfg<G>;
@@ -857,12 +766,8 @@ cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    CUtensorMap tk, tv;
-    const long long rows = (long long)a.num_pages * p.Hkv * kPage;
-    if (!encode_map_p(&tk, a.k_pages, rows) || !encode_map_p(&tv, a.v_pages, rows))
-        return cudaErrorInvalidValue;
     decode_split_pers_kernel<G><<<p.pers_ctas, C::NT, smem, s>>>(
-        tk, tv, a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
+        a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
     return cudaGetLastError();
 }
 
