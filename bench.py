@@ -262,8 +262,12 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     K = args.steps
+    # the split kernel is timed with events around its stage launch on every
+    # EVERY-th step (events between kernels would break the programmatic
+    # dependent launch chain of the other steps)
+    EVERY = 4
     ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(K)]
+                for _ in range((K + EVERY - 1) // EVERY)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     sampler = None
@@ -277,7 +281,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(K):
-        one_step(reps[i % len(reps)], ev_split[i])
+        one_step(reps[i % len(reps)], ev_split[i // EVERY] if i % EVERY == 0 else None)
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -331,7 +335,8 @@ def run_gpu(args):
                          "traffic": (None if profiled_traffic(split_bytes) is None
                                      else int(profiled_traffic(split_bytes))),
                          "peak_kind": peak_kind, "avg_launch_us": round(split_avg * 1e6, 3),
-                         "bytes_per_launch": int(split_bytes)},
+                         "bytes_per_launch": int(split_bytes),
+                         "timed_launches": len(split_ms)},
             "e2e": e2e, "gpu_launches": K * (3 if args.no_tags else 4),
             "clocks": clocks, "cpu_baseline": cpu,
         }

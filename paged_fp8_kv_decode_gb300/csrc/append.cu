@@ -20,6 +20,7 @@ constexpr int kAppendWarps = 4;
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(AppendArgs a) {
     constexpr int EPL = D / 32;  // elements per lane per row (4 or 2)
+    pdl_enter();
     const int bh = blockIdx.x;
     const int b = bh / a.Hkv, h = bh - b * a.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,13 +123,11 @@ cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
     dim3 grid((unsigned)(B * a.Hkv), (unsigned)((units + kAppendWarps - 1) / kAppendWarps));
     dim3 block(kAppendWarps * 32);
     if (a.dtype == PFKV_KV_FP8_E4M3) {
-        if (a.D == 128) kv_append_kernel<128, true><<<grid, block, 0, s>>>(a);
-        else kv_append_kernel<64, true><<<grid, block, 0, s>>>(a);
-    } else {
-        if (a.D == 128) kv_append_kernel<128, false><<<grid, block, 0, s>>>(a);
-        else kv_append_kernel<64, false><<<grid, block, 0, s>>>(a);
+        if (a.D == 128) return launch_pdl(kv_append_kernel<128, true>, grid, block, 0, s, a);
+        return launch_pdl(kv_append_kernel<64, true>, grid, block, 0, s, a);
     }
-    return cudaGetLastError();
+    if (a.D == 128) return launch_pdl(kv_append_kernel<128, false>, grid, block, 0, s, a);
+    return launch_pdl(kv_append_kernel<64, false>, grid, block, 0, s, a);
 }
 
 // --------------------------------------------------------------------------
@@ -138,6 +137,7 @@ cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
 // hflags[b][h]; the attention kernels read them after this kernel completes.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) validate_kernel(DecodeArgs a, int Hkv) {
+    pdl_enter();
     const int bh = blockIdx.x;
     const int b = bh / Hkv, h = bh - b * Hkv;
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
@@ -167,8 +167,7 @@ __global__ void __launch_bounds__(256) validate_kernel(DecodeArgs a, int Hkv) {
 }
 
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    validate_kernel<<<p.B * p.Hkv, 256, 0, s>>>(a, p.Hkv);
-    return cudaGetLastError();
+    return launch_pdl(validate_kernel, dim3(p.B * p.Hkv), dim3(256), 0, s, a, p.Hkv);
 }
 
 // --------------------------------------------------------------------------

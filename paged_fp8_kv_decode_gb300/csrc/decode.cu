@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(SplitCfg<D, G, FP8>::NWARPS * 32)
     constexpr int NW = C::NWARPS, ST = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     typename C::Smem &sm = *reinterpret_cast<typename C::Smem *>(smem_raw);
+    pdl_enter();
 
     const int BH = gridDim.x / nchunks;
     const int chunk = blockIdx.x / BH;
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int Hkv
                                                             int chunk_tokens, int nchunks) {
     __shared__ uint32_t s_flags;
     __shared__ float s_red[D / 32];
+    pdl_enter();
     const int Hq = Hkv * G;
     const int b = blockIdx.x / Hq, hq = blockIdx.x - b * Hq, h = hq / G;
     const int tid = threadIdx.x;
@@ -464,9 +466,8 @@ static cudaError_t launch_split_t(const DecodeArgs &a, const DecodePlan &p, cuda
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const long long items = (long long)p.B * p.Hkv * p.nchunks;
-    decode_split_kernel<D, G, FP8><<<(unsigned)items, C::NWARPS * 32, smem, s>>>(
-        a, p.Hkv, p.chunk_tokens, p.nchunks);
-    return cudaGetLastError();
+    return launch_pdl(decode_split_kernel<D, G, FP8>, dim3((unsigned)items), dim3(C::NWARPS * 32),
+                      smem, s, a, p.Hkv, p.chunk_tokens, p.nchunks);
 }
 
 template <int D, int G>
@@ -496,10 +497,10 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodePlan &p, cudaStream_
     if (p.kind == 1) return launch_combine_pers(a, p, s);
     const unsigned grid = (unsigned)(p.B * p.Hq);
     if (p.D == 128)
-        decode_combine_kernel<128><<<grid, 128, 0, s>>>(a, p.Hkv, p.G, p.chunk_tokens, p.nchunks);
-    else
-        decode_combine_kernel<64><<<grid, 64, 0, s>>>(a, p.Hkv, p.G, p.chunk_tokens, p.nchunks);
-    return cudaGetLastError();
+        return launch_pdl(decode_combine_kernel<128>, dim3(grid), dim3(128), 0, s, a, p.Hkv, p.G,
+                          p.chunk_tokens, p.nchunks);
+    return launch_pdl(decode_combine_kernel<64>, dim3(grid), dim3(64), 0, s, a, p.Hkv, p.G,
+                      p.chunk_tokens, p.nchunks);
 }
 
 }  // namespace pfkv

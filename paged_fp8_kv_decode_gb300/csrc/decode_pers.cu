@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int K = B * Hkv * nchunks;
+    pdl_enter();
 
     // ---------------- prologue: request flags, unit prefix sums ----------------
     for (int b = tid; b < B; b += C::NT) {
@@ -665,85 +666,88 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
 }
 
 // --------------------------------------------------------------------------
-// combine for the persistent layout: rows of segment k are k + p for the
-// workers p that touched it
+// combine for the persistent layout: the rows of segment k are k + p for the
+// workers p that touched it.  One CTA per (request b, kv head h), one warp per
+// query head of the group, lane l owning dims [4l, 4l + 4); the request's
+// flags come from every segment of the request, looked up in parallel.
 // --------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(D) decode_combine_pers_kernel(DecodeArgs a, int Hkv, int G,
-                                                                 int nchunks, int W,
-                                                                 const int *ws_prefix) {
+template <int G>
+__global__ void __launch_bounds__(32 * G) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
+                                                                     int nchunks, int W,
+                                                                     const int *ws_prefix) {
+    constexpr int D = 128, NT = 32 * G;
     __shared__ uint32_t s_flags;
-    __shared__ float s_red[D / 32];
-    const int Hq = Hkv * G;
-    const int b = blockIdx.x / Hq, hq = blockIdx.x - b * Hq, h = hq / G, g = hq - h * G;
-    const int tid = threadIdx.x;
-    const int K = gridDim.x / Hq * Hkv * nchunks;  // B * Hkv * nchunks
+    pdl_enter();
+    const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = gridDim.x / Hkv;
+    const int K = B * Hkv * nchunks;
     const long long U = ws_prefix[K];
     W = (int)min((long long)W, U);  // as in the split kernel
     if (tid == 0) s_flags = 0;
     __syncthreads();
     uint32_t f = 0;
-    for (int i = tid; i < Hkv; i += D) {
+    for (int i = tid; i < Hkv; i += NT) {
         const int ni = a.seq_lens[(long long)b * a.len_sb + (long long)i * a.len_sh];
         if (ni < 0 || (long long)ni > (long long)a.max_pages * kPage || ni > a.max_seq_len)
             f |= PFKV_FLAG_BAD_LENGTH;
         if (a.hflags) f |= a.hflags[b * Hkv + i];
     }
+    // rows of the request's segments (requests the validation rejected have none)
+    if (U > 0) {
+        for (int it = tid; it < Hkv * nchunks; it += NT) {
+            const int k = b * Hkv * nchunks + it;
+            const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+            if (u1 == u0) continue;
+            const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
+            for (int p = p0; p <= p1; ++p) f |= a.status[k + p];
+        }
+    }
     if (f) atomicOr(&s_flags, f);
     __syncthreads();
-    if (s_flags == 0 && U > 0) {
-        f = 0;
-        for (int i = 0; i < Hkv; ++i) {
-            for (int c = 0; c < nchunks; ++c) {
-                const int k = (b * Hkv + i) * nchunks + c;
-                const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
-                if (u1 == u0) continue;
-                const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
-                for (int p = p0 + tid; p <= p1; p += D) f |= a.status[k + p];
-            }
-        }
-        if (f) atomicOr(&s_flags, f);
-        __syncthreads();
-    }
     const uint32_t flags = s_flags;
-    if (hq == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
-    __nv_bfloat16 *out = a.out + ((long long)b * Hq + hq) * D;
+    if (h == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
+    const int hq = h * G + warp;
+    uint2 *out = reinterpret_cast<uint2 *>(a.out + ((long long)b * Hkv * G + hq) * D + lane * 4);
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
     if (flags != 0 || n == 0 || U == 0) {
-        out[tid] = __float2bfloat16_rn(0.f);
+        *out = make_uint2(0u, 0u);
         return;
     }
-    // maximum log2-sum-exp over this head's rows
     float M = -INFINITY;
     for (int c = 0; c < nchunks; ++c) {
         const int k = (b * Hkv + h) * nchunks + c;
         const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
         if (u1 == u0) continue;
         const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
-        for (int p = p0 + tid; p <= p1; p += D) M = fmaxf(M, a.lse[(long long)(k + p) * G + g]);
+        for (int p = p0 + lane; p <= p1; p += 32) M = fmaxf(M, a.lse[(long long)(k + p) * G + warp]);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if ((tid & 31) == 0) s_red[tid >> 5] = M;
-    __syncthreads();
-    M = s_red[0];
-#pragma unroll
-    for (int i = 1; i < D / 32; ++i) M = fmaxf(M, s_red[i]);
-    float acc = 0.f, wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
     for (int c = 0; c < nchunks; ++c) {
         const int k = (b * Hkv + h) * nchunks + c;
         const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
         if (u1 == u0) continue;
         const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
+#pragma unroll 4
         for (int p = p0; p <= p1; ++p) {
-            const long long row = k + p;
-            const float lc = a.lse[row * G + g];
+            const long long row = (long long)(k + p) * G + warp;
+            const float lc = a.lse[row];
             const float wt = lc == -INFINITY ? 0.f : pexp2(lc - M);
+            const float4 ov = *reinterpret_cast<const float4 *>(a.o + row * D + lane * 4);
             wsum += wt;
-            acc = fmaf(wt, a.o[(row * G + g) * D + tid], acc);
+            acc.x = fmaf(wt, ov.x, acc.x);
+            acc.y = fmaf(wt, ov.y, acc.y);
+            acc.z = fmaf(wt, ov.z, acc.z);
+            acc.w = fmaf(wt, ov.w, acc.w);
         }
     }
-    out[tid] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    *out = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
 }
 
 // --------------------------------------------------------------------------
@@ -766,9 +770,8 @@ cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    decode_split_pers_kernel<G><<<p.pers_ctas, C::NT, smem, s>>>(
-        a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
-    return cudaGetLastError();
+    return launch_pdl(decode_split_pers_kernel<G>, dim3(p.pers_ctas), dim3(C::NT), smem, s, a,
+                      p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
 }
 
 }  // namespace
@@ -792,9 +795,14 @@ cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStre
 }
 
 cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    decode_combine_pers_kernel<128><<<(unsigned)(p.B * p.Hq), 128, 0, s>>>(
-        a, p.Hkv, p.G, p.nchunks, p.pers_ctas * PersCfg<4>::PAIRS, a.ws_prefix);
-    return cudaGetLastError();
+    const int W = p.pers_ctas * PersCfg<4>::PAIRS;
+    const dim3 grid((unsigned)(p.B * p.Hkv));
+    switch (p.G) {
+        case 1: return launch_pdl(decode_combine_pers_kernel<1>, grid, dim3(32), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+        case 2: return launch_pdl(decode_combine_pers_kernel<2>, grid, dim3(64), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+        case 4: return launch_pdl(decode_combine_pers_kernel<4>, grid, dim3(128), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pfkv

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(SwzCfg<G>::NWARPS * 32)
     extern __shared__ uint8_t smem_raw[];
     typename C::Smem &sm = *reinterpret_cast<typename C::Smem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    pdl_enter();
 
     const int BH = gridDim.x / nchunks;
     const int chunk = blockIdx.x / BH;
@@ -504,9 +505,8 @@ cudaError_t launch_swz_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t 
     if (!encode_pool_map(&tk, a.k_pages, rows) || !encode_pool_map(&tv, a.v_pages, rows))
         return cudaErrorInvalidValue;
     const long long items = (long long)p.B * p.Hkv * p.nchunks;
-    decode_split_swz_kernel<G><<<(unsigned)items, C::NWARPS * 32, smem, s>>>(
-        tk, tv, a, p.Hkv, p.chunk_tokens, p.nchunks);
-    return cudaGetLastError();
+    return launch_pdl(decode_split_swz_kernel<G>, dim3((unsigned)items), dim3(C::NWARPS * 32), smem,
+                      s, tk, tv, a, p.Hkv, p.chunk_tokens, p.nchunks);
 }
 
 }  // namespace

@@ -81,6 +81,27 @@ struct AppendArgs {
     uint8_t *flags;
 };
 
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the previous kernel in the stream still runs.  Every kernel
+// of this library starts with pdl_enter(), which waits for the previous
+// kernel's completion and memory before anything else, so the overlap is
+// limited to launch latency and is safe whatever precedes it in the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // launchers (defined in the .cu files)
 cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s);
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
@@ -99,6 +120,13 @@ cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStre
 // device helpers
 // --------------------------------------------------------------------------
 #if defined(__CUDACC__)
+
+// Wait for the previous kernel in the stream (completion and memory), then
+// let the next one launch.  A no-op without programmatic dependent launch.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
