@@ -138,7 +138,7 @@ struct PersCfg {
 
 // The segment containing global unit x (prefix: exclusive sums, K segments;
 // segments with no units never contain a unit).
-__device__ __forceinline__ int seg_of(const int *prefix, int K, long long x) {
+__device__ __forceinline__ int seg_of(const int *prefix, int K, int x) {
     int lo = 0, hi = K;  // prefix[lo] <= x < prefix[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -216,10 +216,10 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
         }
     }
     __syncthreads();
-    const long long U = sm.prefix[K];
+    const int U = sm.prefix[K];  // unit counts stay far below 2^31 (rows < 2^31 / 16)
     // never more workers than units: every worker then owns at least one unit,
     // so all workers between a segment's first and last unit write its rows
-    const int W = (int)min((long long)gridDim.x * C::PAIRS, U);
+    const int W = min((int)gridDim.x * C::PAIRS, U);
     if (blockIdx.x == 0) {
         for (int k = tid; k <= K; k += C::NT) ws_prefix[k] = sm.prefix[k];
     }
@@ -234,36 +234,35 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     const bool is_score = warp < C::PAIRS;
     typename C::Pair &P = sm.pair[pi];
     const int w = blockIdx.x * C::PAIRS + pi;
-    const long long x0 = w < W ? ((long long)w * U + W - 1) / W : U;
-    const long long x1 = w < W ? ((long long)(w + 1) * U + W - 1) / W : U;
+    const int x0 = w < W ? (int)(((long long)w * U + W - 1) / W) : U;
+    const int x1 = w < W ? (int)(((long long)(w + 1) * U + W - 1) / W) : U;
     const int vt = lane >> 3, vc = lane & 7;
 
     // granule cursor (2 units, never across a segment), shared logic of both warps
     struct Cursor {
-        long long x, seg_end;
-        int k;
+        int x, seg_end, k;
     };
     auto cursor_init = [&](Cursor &c) {
         c.x = x0;
         c.k = seg_of(sm.prefix, K, x0);
-        c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
+        c.seg_end = min(sm.prefix[c.k + 1], x1);
     };
     auto cursor_next = [&](Cursor &c, int n) {
         c.x += n;
         if (c.x >= c.seg_end && c.x < x1) {
             c.k = seg_of(sm.prefix, K, c.x);
-            c.seg_end = min((long long)sm.prefix[c.k + 1], x1);
+            c.seg_end = min(sm.prefix[c.k + 1], x1);
         }
     };
 
     if (is_score) {
         int ngran = 0;
         if (x0 < x1) {
-            long long x = x0;
+            int x = x0;
             int k = seg_of(sm.prefix, K, x);
             while (x < x1) {
-                const long long e = min((long long)sm.prefix[k + 1], x1);
-                ngran += (int)((e - x + 1) / 2);
+                const int e = min(sm.prefix[k + 1], x1);
+                ngran += (e - x + 1) / 2;
                 x = e;
                 ++k;
                 while (k < K && sm.prefix[k + 1] == sm.prefix[k]) ++k;
@@ -306,10 +305,11 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
             if (lane == 0) q_copy(1, next_seg_k);
         }
         float2 q2[G][8];
-        uint32_t full_phase = 0, q_phase = 0, status = 0;
+        uint32_t q_phase = 0, status = 0;
+        uint32_t parity = 0;  // every stage completes one phase per round of ST granules
+        int s = 0;
         bool seg_start = true;
         for (int i = 0; i < ngran; ++i) {
-            const int s = i % ST;
             if (seg_start) {
                 const int slot = seg_ord & 1;
                 if (!mbar_wait_bounded(&P.qbar[slot], (q_phase >> slot) & 1u)) status |= kStatusTimeout;
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 __syncwarp();
                 // the slot just read is free: prefetch the segment after next
                 if (next_seg_k >= 0) {
-                    const long long e = min((long long)sm.prefix[next_seg_k + 1], x1);
+                    const int e = min(sm.prefix[next_seg_k + 1], x1);
                     const int k2 = e < x1 ? seg_of(sm.prefix, K, e) : -1;
                     if (k2 >= 0 && lane == 0) {
                         fence_proxy_async_smem();
@@ -339,9 +339,8 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 }
                 seg_start = false;
             }
-            const int n_units = (int)min((long long)2, con.seg_end - con.x);
-            if (!mbar_wait_bounded(&P.full[s], (full_phase >> s) & 1u)) status |= kStatusTimeout;
-            full_phase ^= 1u << s;
+            const int n_units = min(2, con.seg_end - con.x);
+            if (!mbar_wait_bounded(&P.full[s], parity)) status |= kStatusTimeout;
             const uint8_t *stage = P.ring[s];
 
             // ---- partial dot products: slice vc, token 4r + vt ----
@@ -405,18 +404,22 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 seg_start = true;
                 ++seg_ord;
             }
+            if (++s == ST) {
+                s = 0;
+                parity ^= 1u;
+            }
         }
         if (status && lane == 0) atomicOr(&P.score_status, status);
     } else {
         // ===================== value warp =====================
         // unit metadata window: lane l holds unit base + l (cur) and
         // base + 32 + l (nxt): page id (-1 bad, -2 absent) and the two scales
-        long long base = x0;
+        int base = x0;
         int cphys, nphys;
         float cks, cvs, nks, nvs;
         uint32_t cbad, nbad;
-        auto load_ids = [&](long long bx, int &phys, uint32_t &bad) {
-            const long long x = bx + lane;
+        auto load_ids = [&](int bx, int &phys, uint32_t &bad) {
+            const int x = bx + lane;
             phys = -2;
             bad = 0;
             if (x < x1) {
@@ -442,34 +445,41 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
         load_ids(base + 32, nphys, nbad);
         load_scales(cphys, cks, cvs);
         load_scales(nphys, nks, nvs);
-        // (uniform branches, not selects: a select would wait for the next
-        // window's loads even when only the current one is read)
-        auto unit_phys = [&](long long x) {
-            const int d = (int)(x - base);
+        // metadata of unit x (in [base, base + 64)).  One uniform branch picks
+        // the window half (a select would wait for the next half's loads even
+        // when only the current one is read).
+        struct UnitMeta {
+            int phys;
+            float ks, vs;
+            uint32_t bad;
+        };
+        auto unit_meta = [&](int x) {
+            UnitMeta m;
+            const int d = x - base;
+            if (d < 32) {
+                m.phys = __shfl_sync(0xffffffffu, cphys, d);
+                m.ks = __shfl_sync(0xffffffffu, cks, d);
+                m.vs = __shfl_sync(0xffffffffu, cvs, d);
+                m.bad = __shfl_sync(0xffffffffu, cbad, d);
+            } else {
+                m.phys = __shfl_sync(0xffffffffu, nphys, d - 32);
+                m.ks = __shfl_sync(0xffffffffu, nks, d - 32);
+                m.vs = __shfl_sync(0xffffffffu, nvs, d - 32);
+                m.bad = __shfl_sync(0xffffffffu, nbad, d - 32);
+            }
+            return m;
+        };
+        auto unit_phys = [&](int x) {
+            const int d = x - base;
             if (d < 32) return __shfl_sync(0xffffffffu, cphys, d);
             return __shfl_sync(0xffffffffu, nphys, d - 32);
-        };
-        auto unit_ks = [&](long long x) {
-            const int d = (int)(x - base);
-            if (d < 32) return __shfl_sync(0xffffffffu, cks, d);
-            return __shfl_sync(0xffffffffu, nks, d - 32);
-        };
-        auto unit_vs = [&](long long x) {
-            const int d = (int)(x - base);
-            if (d < 32) return __shfl_sync(0xffffffffu, cvs, d);
-            return __shfl_sync(0xffffffffu, nvs, d - 32);
-        };
-        auto unit_bad = [&](long long x) {
-            const int d = (int)(x - base);
-            if (d < 32) return __shfl_sync(0xffffffffu, cbad, d);
-            return __shfl_sync(0xffffffffu, nbad, d - 32);
         };
         Cursor iss, con;
         cursor_init(iss);
         cursor_init(con);
         // load (or mark empty) the granule at cursor c into stage s; lane 0 issues
         auto issue_at = [&](const Cursor &c, int s) {
-            const int n = (int)min((long long)2, c.seg_end - c.x);
+            const int n = min(2, c.seg_end - c.x);
             const int p0 = unit_phys(c.x);
             const int p1 = n == 2 ? unit_phys(c.x + 1) : -2;
             if (lane == 0) {
@@ -503,10 +513,10 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
         }
-        uint32_t sr_phase = 0, seg_status = 0;
+        uint32_t parity = 0, seg_status = 0;
+        int s = 0;
         bool pending_scales = false;
         for (int i = 0; i < ngran; ++i) {
-            const int s = i % ST;
             // metadata window upkeep
             if (pending_scales) {
                 load_scales(nphys, nks, nvs);
@@ -518,19 +528,18 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 load_ids(base + 32, nphys, nbad);
                 pending_scales = true;
             }
-            const int n_units = (int)min((long long)2, con.seg_end - con.x);
-            const int ph0 = unit_phys(con.x);
-            const int ph1 = n_units == 2 ? unit_phys(con.x + 1) : -2;
-            seg_status |= unit_bad(con.x) | (n_units == 2 ? unit_bad(con.x + 1) : 0u);
-            const long long seg_last = (long long)sm.prefix[con.k + 1] - 1;
+            const int n_units = min(2, con.seg_end - con.x);
+            const UnitMeta u0m = unit_meta(con.x);
+            UnitMeta u1m = {-2, 0.f, 0.f, 0u};
+            if (n_units == 2) u1m = unit_meta(con.x + 1);
+            seg_status |= u0m.bad | u1m.bad;
+            const int seg_last = sm.prefix[con.k + 1] - 1;
             const int lnv = sm.last_nv[con.k];
-            const int nv0 = ph0 >= 0 ? (con.x == seg_last ? lnv : kPage) : 0;
-            const int nv1 = ph1 >= 0 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
-            const float ks0 = unit_ks(con.x), ks1 = n_units == 2 ? unit_ks(con.x + 1) : 0.f;
-            const float vs0 = unit_vs(con.x), vs1 = n_units == 2 ? unit_vs(con.x + 1) : 0.f;
+            const int nv0 = u0m.phys >= 0 ? (con.x == seg_last ? lnv : kPage) : 0;
+            const int nv1 = u1m.phys >= 0 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
+            const float ks0 = u0m.ks, ks1 = u1m.ks, vs0 = u0m.vs, vs1 = u1m.vs;
 
-            if (!mbar_wait_bounded(&P.sready[s], (sr_phase >> s) & 1u)) seg_status |= kStatusTimeout;
-            sr_phase ^= 1u << s;
+            if (!mbar_wait_bounded(&P.sready[s], parity)) seg_status |= kStatusTimeout;
 
             // ---- online softmax over the granule (lane: token 4 vc + vt) ----
             const int my_u = vc >> 2, my_row = (4 * vc + vt) & 15;
@@ -661,6 +670,10 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 cursor_next(iss, issue_at(iss, s));
             }
             cursor_next(con, n_units);
+            if (++s == ST) {
+                s = 0;
+                parity ^= 1u;
+            }
         }
     }
 }
