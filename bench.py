@@ -22,6 +22,14 @@ Reported (one JSON line on rank 0):
   cpu_baseline the oracle (test infrastructure) on a bounded sample, host cores
 
 --impl reference times the oracle alone (CPU), as the reference arm.
+
+--workload {tiny,long,sweep,evict} measures the other workloads instead, one
+JSON line each: the long-context split (B=4, 128K..512K tokens, split 4096),
+the 80 GB-pool sweep (--batch, --kv-dtype; every sequence 32,768 tokens) and
+the eviction batch (per-head tables and lengths, stale tags) with tags on,
+with every tag matching and with tags off.  These run one batch and flush L2
+between steps (a write and then a read of buffers larger than L2) outside the
+timed interval of each step.
 """
 from __future__ import annotations
 
@@ -58,6 +66,12 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--workload", default="llama8b",
+                    choices=["llama8b", "tiny", "long", "sweep", "evict"],
+                    help="llama8b (default): the Llama-shaped layer; the others are the "
+                         "tiny, long-context, 80 GB-pool sweep and eviction + tags workloads")
+    ap.add_argument("--batch", type=int, default=32, help="sweep: batch size")
+    ap.add_argument("--kv-dtype", default="fp8", choices=["fp8", "bf16"], help="sweep: pool dtype")
     return ap.parse_args(argv)
 
 
@@ -150,12 +164,12 @@ class ClockSampler:
 class PreparedStep:
     """The C-ABI calls of one step with their argument structs built once."""
 
-    def __init__(self, db, B, stream_handle):
+    def __init__(self, db, B, stream_handle, cache=None, pages=None):
         self.db, self.B, self.s = db, B, stream_handle
         L = B.lib()
         self.L = L
-        self.c = db.cache.c_struct()
-        self.p = db.pages.c_struct()
+        self.c = (cache or db.cache).c_struct()
+        self.p = (pages or db.pages).c_struct()
         ws = db.workspace
         self.args = (ctypes.byref(self.c), ctypes.byref(self.p), db.q.data_ptr(), db.spec.Hq,
                      ctypes.c_float(db.spec.sm_scale), db.split_tokens, db.max_seq_len,
@@ -396,17 +410,22 @@ def run_e2e(args, reps, B, stream, step_bytes, world, dev):
 # the oracle (test infrastructure) as CPU baseline / reference arm
 # --------------------------------------------------------------------------
 def _oracle_sample(spec, n_requests: int, n_kv_heads: int, seed: int):
-    """A bounded sample of the workload for the oracle: n requests with the
-    workload's lengths, group size and head_dim but only n_kv_heads kv heads
-    (and their G query heads each), quantised by the oracle itself."""
+    """A bounded sample of the workload for the oracle: the first n requests
+    with the workload's lengths, group size and head_dim but only n_kv_heads
+    kv heads (and their G query heads each), quantised by the oracle itself,
+    with every tag matching (attention only)."""
     import dataclasses
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
     from oracle_cases import cache_dict, fill_pool, pages_dict
     from paged_fp8_kv_decode_gb300 import workloads as W
-    sub = dataclasses.replace(spec, B=n_requests, lens=np.asarray(spec.lens[:n_requests]),
+    lens = np.asarray(spec.lens)
+    lens = lens[:n_requests] if lens.ndim == 1 else lens[:n_requests, :n_kv_heads]
+    need = (lens.astype(np.int64) + (1 if spec.append else 0) + 15) // 16
+    num_pages = int(need.sum() if lens.ndim == 1 else need.sum(axis=0).max()) + 16
+    sub = dataclasses.replace(spec, B=n_requests, lens=np.ascontiguousarray(lens),
                               Hkv=n_kv_heads, Hq=spec.G * n_kv_heads, seed=seed,
-                              num_pages=4096)
+                              num_pages=num_pages, stale_per_mille=0.0)
     batch = W.make_batch(sub)
     T = int(batch.fill_lens.max())
     k_rows = W.draw_kv_rows(sub, T, "k")
@@ -419,7 +438,8 @@ def _oracle_sample(spec, n_requests: int, n_kv_heads: int, seed: int):
                          W.bf16_bits(W.draw_new_token(sub, "k")),
                          W.bf16_bits(W.draw_new_token(sub, "v")))
     q = W.bf16_bits(W.draw_q(sub))
-    kv = int(batch.lens_bh("seq").astype(np.int64).sum()) * sub.D * 2
+    el = 2 if sub.kv_dtype == "bf16" else 1
+    kv = int(batch.lens_bh("seq").astype(np.int64).sum()) * sub.D * 2 * el
     return oracle, cache, pages, q, sub, batch, kv
 
 
@@ -429,28 +449,49 @@ def _time_oracle(oracle, cache, pages, q, sub, batch):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(db, target_s: float = 15.0):
-    """Oracle KV GB/s on host cores over a bounded sample of the workload."""
-    spec = db.spec
-    oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, 4, spec.Hkv, spec.seed + 555)
+def _sample_shape(spec, head_tokens: int = 600_000):
+    """Requests and kv heads of a bounded oracle sample: up to 4 requests, as
+    many kv heads as keep (tokens x kv heads) under head_tokens."""
+    lens = np.asarray(spec.lens).astype(np.int64)
+    per_req = lens if lens.ndim == 1 else lens.max(axis=1)
+    n = min(spec.B, 4)
+    while n > 1 and int(per_req[:n].sum()) > head_tokens:
+        n -= 1
+    nh = max(1, min(spec.Hkv, head_tokens // max(1, int(per_req[:n].sum()))))
+    return n, nh
+
+
+def cpu_baseline_spec(spec, target_s: float = 15.0):
+    """Oracle KV GB/s on the host cores over a bounded sample of the workload
+    (and on one core, from a single call)."""
+    n, nh = _sample_shape(spec)
+    oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, n, nh, spec.seed + 555)
+    threads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    t_one = _time_oracle(oracle, cache, pages, q, sub, batch)
+    oracle.set_num_threads(threads)
     t = _time_oracle(oracle, cache, pages, q, sub, batch)
     reps = max(1, min(400, int(target_s / max(t, 1e-3))))
     total = t
     for _ in range(reps - 1):
         total += _time_oracle(oracle, cache, pages, q, sub, batch)
-    return {"value": round(kv * reps / total / 1e9, 4), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{sub.B} of {spec.B} requests ({int(batch.seq_lens.sum())} tokens, all "
-                      f"{sub.Hq} q heads), attention only, {reps} repetitions in {total:.1f} s; "
+    return {"value": round(kv * reps / total / 1e9, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "value_1_core": round(kv / t_one / 1e9, 4),
+            "sample": f"{sub.B} of {spec.B} requests ({int(batch.lens_bh('seq')[:, 0].sum())} "
+                      f"tokens per kv head), {sub.Hkv} of {spec.Hkv} kv heads ({sub.Hq} q heads), "
+                      f"attention only, {reps} repetitions in {total:.1f} s; "
                       f"KV bytes read / oracle time"}
+
+
+def cpu_baseline(db, target_s: float = 15.0):
+    return cpu_baseline_spec(db.spec, target_s)
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    from paged_fp8_kv_decode_gb300 import workloads as W
-    spec = W.spec_llama8b("full")
+    spec = workload_spec(args)
     # per step: one request of the workload, restricted to enough kv heads that
     # warmup + steps fit in about two minutes of oracle time
     oracle, cache, pages, q, sub, batch, kv = _oracle_sample(spec, 1, 1, spec.seed + 777)
@@ -464,16 +505,19 @@ def run_reference(args):
     ts = [_time_oracle(oracle, cache, pages, q, sub, batch) for _ in range(args.steps)]
     total = sum(ts)
     value = kv * len(ts) / total / 1e9
-    sample = (f"1 request ({int(batch.seq_lens[0])} tokens), {sub.Hkv} of {spec.Hkv} kv heads "
+    sample = (f"1 request ({int(batch.lens_bh('seq')[0, 0])} tokens), {sub.Hkv} of {spec.Hkv} kv heads "
               f"({sub.Hq} q heads) per step, attention only; KV bytes read / oracle time")
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT,
+    metric = METRIC if args.workload == "llama8b" else \
+        "paged decode attention KV GB/s (" + spec.name + ")"
+    line = {"impl": "reference", "metric": metric, "value": round(value, 5), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total / len(ts) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 quantiser",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": spec.B, "num_q_heads": spec.Hq,
+            "config": {"workload": WORKLOAD if args.workload == "llama8b" else spec.name + "-full",
+                       "batch": spec.B, "num_q_heads": spec.Hq,
                        "num_kv_heads": spec.Hkv, "head_dim": spec.D, "page_size": 16,
-                       "kv_dtype": "fp8"},
+                       "kv_dtype": spec.kv_dtype},
             "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -481,10 +525,244 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def workload_spec(args, rank: int = 0):
+    """The spec of --workload (each rank draws its own data)."""
+    from paged_fp8_kv_decode_gb300 import workloads as W
+    seed_of = {"tiny": W.BASE_SEED + 1, "long": W.BASE_SEED + 3, "sweep": W.BASE_SEED + 4,
+               "evict": W.BASE_SEED + 5, "llama8b": W.BASE_SEED + 2}
+    seed = rank_seed(seed_of[args.workload], rank, 0)
+    if args.workload == "tiny":
+        return W.spec_tiny(seed=seed)
+    if args.workload == "long":
+        return W.spec_long("full", seed=seed)
+    if args.workload == "sweep":
+        return W.spec_sweep(args.batch, args.kv_dtype, seed=seed)
+    if args.workload == "evict":
+        return W.spec_evict("full", seed=seed)
+    return W.spec_llama8b("full", seed=seed)
+
+
+def sweep_admissible(spec, pool_bytes: float = 80e9, layers: int = N_LAYERS) -> int:
+    """Largest batch whose KV for every layer of a 32-layer model fits an 80 GB
+    pool, with every sequence at this workload's length."""
+    el = 2 if spec.kv_dtype == "bf16" else 1
+    per_token = 2 * spec.Hkv * spec.D * el + (2 * spec.Hkv * 4 / 16 if spec.kv_dtype == "fp8" else 0)
+    return int(pool_bytes // (int(spec.lens[0]) * layers * per_token))
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes one buffer larger than L2, then
+    reads another so that the written lines are clean (their write-back
+    happens here, not inside the next step)."""
+
+    def __init__(self, dev, mb: int = 512):
+        import torch
+        self.w = torch.empty(mb << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones((mb << 20) // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.max()
+
+
+def _median_times(ms):
+    ms = sorted(ms)
+    q = lambda f: ms[min(len(ms) - 1, int(f * (len(ms) - 1) + 0.5))]
+    return q(0.5), q(0.1), q(0.9)
+
+
+def run_workload(args):
+    """One JSON line for --workload tiny/long/sweep/evict (see module docstring)."""
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_fp8_kv_decode_gb300 import binding as B
+    from paged_fp8_kv_decode_gb300 import workloads as W
+    from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
+
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    spec = workload_spec(args, rank)
+    db = DeviceBatch(W.make_batch(spec), device=dev)
+    variants = [("tags" if spec.tags else "no_tags", PreparedStep(db, B, sh), spec.tags)]
+    if args.workload == "evict":
+        # every live unit carrying the tag its request expects (no request aborted)
+        batch = db.batch
+        match = batch.page_tags.copy()
+        bt, ex = batch.block_tables, batch.expected_tags
+        lens = batch.lens_bh("seq")
+        for b in range(spec.B):
+            for h in range(spec.Hkv):
+                k = (int(lens[b, h]) + 15) // 16
+                match[bt[b, h, :k], h] = ex[b, h, :k]
+        match_t = torch.from_numpy(match.view(np.int32)).to(dev)
+        c_match = B.Cache(db.cache.k_pages, db.cache.v_pages, db.cache.k_scale, db.cache.v_scale,
+                          match_t)
+        p_off = B.Pages(db.pages.batch, db.pages.max_pages, db.pages.block_tables,
+                        db.pages.bt_stride_b, db.pages.bt_stride_h, db.pages.seq_lens,
+                        db.pages.len_stride_b, db.pages.len_stride_h, None)
+        variants.append(("tags_all_match", PreparedStep(db, B, sh, cache=c_match), True))
+        variants.append(("no_tags", PreparedStep(db, B, sh, cache=db.cache_untracked,
+                                                 pages=p_off), False))
+    flush = L2Flush(dev)
+    S_ALL = B.PFKV_STAGE_ALL
+    S_V, S_S, S_C = B.PFKV_STAGE_VALIDATE, B.PFKV_STAGE_SPLIT, B.PFKV_STAGE_COMBINE
+    K = args.steps
+
+    def timed(p, split_only=False):
+        for _ in range(args.warmup):
+            flush()
+            p.append()
+            p.stage(S_ALL)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for i in range(K):
+            flush()
+            if split_only:
+                p.append()
+                p.stage(S_V)
+                evs[i][0].record(stream)
+                p.stage(S_S)
+                evs[i][1].record(stream)
+                p.stage(S_C)
+            else:
+                evs[i][0].record(stream)
+                p.append()
+                p.stage(S_ALL)
+                evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    append_bytes = (spec.B * spec.Hkv * spec.D * (2 * 2 + 2 * (2 if spec.kv_dtype == "bf16" else 1))
+                    + (spec.B * spec.Hkv * 8 if spec.kv_dtype == "fp8" else 0)) if spec.append else 0
+    sampler = None
+    if rank == 0 and not args.no_clocks:
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    results = {}
+    for name, p, tags in variants:
+        ms = timed(p)
+        flags = db.flags[:spec.B].cpu().numpy()
+        skip = flags != 0
+        by = db.algorithmic_bytes(skip=skip, tags=tags) + append_bytes
+        med, p10, p90 = _median_times(ms)
+        med = reduce_max(med, world, dev)
+        results[name] = {"ms_per_step": round(med, 5), "p10_ms": round(p10, 5),
+                         "p90_ms": round(p90, 5), "bytes_per_step": int(by),
+                         "gbs": round(by * world / (med / 1e3) / 1e9, 2),
+                         "requests_aborted": int(skip.sum())}
+    name0, p0, tags0 = variants[0]
+    split_ms = timed(p0, split_only=True)
+    clocks = sampler.stop() if sampler else None
+    split_med = _median_times(split_ms)[0]
+    flags = db.flags[:spec.B].cpu().numpy()
+    skip = flags != 0
+    lens = db._lens(skip)
+    split_bytes = (db.kv_bytes(skip) + int(((lens + 15) // 16).sum())
+                   * (4 + (8 if spec.kv_dtype == "fp8" else 0)) + 2 * spec.B * spec.Hq * spec.D * 2)
+    split_gbs = split_bytes / (split_med / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    r0 = results[name0]
+    med_s = r0["ms_per_step"] / 1e3
+    cfg = {"workload": f"{spec.name}" + ("-full" if args.workload != "tiny" else ""),
+           "batch": spec.B, "num_q_heads": spec.Hq, "num_kv_heads": spec.Hkv,
+           "head_dim": spec.D, "page_size": 16, "num_pages": spec.num_pages,
+           "kv_dtype": spec.kv_dtype, "tags": tags0, "split_tokens": spec.split_tokens,
+           "per_head_tables": spec.per_head, "append": spec.append,
+           "live_kv_mb": round(db.kv_bytes() / 1e6, 1),
+           "l2": "L2 flushed between timed steps (512 MB write + 512 MB read, outside the "
+                 "timed interval)",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if args.workload == "sweep":
+        adm = sweep_admissible(spec)
+        cfg["seq_len"] = int(spec.lens[0])
+        cfg["admissible_batch_80gb_32_layers"] = adm
+        cfg["admissible"] = spec.B <= adm
+    line = {
+        "metric": "paged decode attention KV GB/s (" + spec.name + ")",
+        "value": round(r0["gbs"], 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": r0["ms_per_step"], "p10_ms": r0["p10_ms"],
+        "p90_ms": r0["p90_ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": f"{'fp8_e4m3' if spec.kv_dtype == 'fp8' else 'bf16'} KV, fp32 accumulate, bf16 q/out",
+        "data": "synthetic", "config": cfg,
+        "tokens_per_s": round(world * spec.B / (N_LAYERS * med_s), 1),
+        "tokens_per_s_per_layer": round(world * spec.B / med_s, 1),
+        "pct_of_hbm_peak": round(100 * r0["gbs"] / world / peak, 2),
+        "roofline": {"kernel": "decode_split", "bound": "hbm", "achieved": round(split_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(split_gbs / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind,
+                     "avg_launch_us": round(split_med * 1e3, 3), "stat": "median",
+                     "bytes_per_launch": int(split_bytes), "timed_launches": len(split_ms)},
+        "variants": results if len(results) > 1 else None,
+        "gpu_launches": K * (len(variants) * (3 if spec.append else 2) + 3) + sum(
+            K for _, _, t in variants if t),
+        "clocks": clocks,
+    }
+    if "tags_all_match" in results and "no_tags" in results:
+        a, b = results["tags_all_match"]["ms_per_step"], results["no_tags"]["ms_per_step"]
+        line["tag_overhead_pct"] = round(100 * (a - b) / b, 2)
+    line["e2e"] = run_e2e_flushed(args, p0, B, stream, r0["bytes_per_step"], world, dev, flush)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_spec(spec)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e_flushed(args, p, B, stream, step_bytes, world, dev, flush):
+    """End to end through the public API with host buffers, L2 flushed before
+    each step outside the host-timed interval."""
+    import torch
+    K = max(1, min(args.e2e_steps, args.steps))
+    db = p.db
+    d_in = [db.q, db.positions, db.seq_lens, db.block_tables]
+    if db.spec.append:
+        d_in += [db.k_new, db.v_new]
+    if db.cache.page_tags is not None:
+        d_in.append(db.expected_tags)
+    h_in = [t.detach().cpu().pin_memory() for t in d_in]
+    h_out = [torch.empty_like(db.out, device="cpu").pin_memory(),
+             torch.empty_like(db.flags, device="cpu").pin_memory()]
+    total = 0.0
+    for i in range(K + 2):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        p.append()
+        p.stage(B.PFKV_STAGE_ALL)
+        h_out[0].copy_(db.out, non_blocking=True)
+        h_out[1].copy_(db.flags, non_blocking=True)
+        stream.synchronize()
+        if i >= 2:
+            total += time.perf_counter() - t0
+    total = reduce_max(total, world, dev)
+    return {"value": round(aggregate(step_bytes, K, total, world), 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_in)),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out)),
+            "steps": K, "ms_per_step": round(total / K * 1e3, 4)}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "llama8b":
+        run_workload(args)
     else:
         run_gpu(args)
 

@@ -24,13 +24,13 @@
 //    (lane (t, c): slice c, token 4r + t in pass r), converts K bytes to fp32
 //    pairs, takes packed fp32x2 dot products, finishes each score with a
 //    reduce-scatter over the 8 lanes of a token group (so lane (t, c) ends with
-//    the G scores of token 4c + t), runs the online softmax per granule and
-//    hands the value warp the probabilities times the unit's V scale, as
-//    ready-made pairs, plus rescale factors and segment totals;
-//  * the value warp accumulates its 16-dim slice of the output in registers,
-//    writes the partial row at the end of each segment, and refills the stage
-//    it has just finished with the TMA loads of the granule ST ahead, whose
-//    page ids the score warp wrote next to the probabilities.
+//    the G scores of token 4c + t) and hands the value warp the raw scores;
+//  * the value warp keeps a window of unit metadata (page id, K and V scales,
+//    bad-id bit) for the next 64 units in registers, turns the raw scores into
+//    probabilities (online softmax per granule, lazy rescale), accumulates
+//    its 16-dim slice of the output in registers, writes the partial row at
+//    the end of each segment, and refills the stage it has just finished
+//    with the bulk copies of the granule ST ahead.
 // Splitting scores and values over two warps halves the registers each needs,
 // so 12 warps fit an SM, and the two phases of neighbouring granules overlap.
 #include <atomic>

@@ -117,19 +117,29 @@ class DeviceBatch:
         self.attend(stream)
 
     # ------------------------------------------------------------------
-    def kv_bytes(self) -> int:
-        """Bytes of K and V the attention must read (partial pages count only
-        their tokens)."""
+    def _lens(self, skip=None) -> np.ndarray:
         lens = self.batch.lens_bh("seq").astype(np.int64)
-        el = 2 if self.spec.kv_dtype == "bf16" else 1
-        return int(lens.sum()) * self.spec.D * el * 2
+        if skip is not None:
+            lens = lens * ~np.asarray(skip, dtype=bool)[:, None]
+        return lens
 
-    def algorithmic_bytes(self) -> int:
+    def kv_bytes(self, skip=None) -> int:
+        """Bytes of K and V the attention must read (partial pages count only
+        their tokens).  ``skip``: bool per request, True for requests whose
+        pages are not read (aborted by the tag check)."""
+        el = 2 if self.spec.kv_dtype == "bf16" else 1
+        return int(self._lens(skip).sum()) * self.spec.D * el * 2
+
+    def algorithmic_bytes(self, skip=None, tags: Optional[bool] = None) -> int:
         """KV bytes + per-live-page table entry, FP8 scales and tags + q, out
-        and flags: what one attention call must move at minimum."""
+        and flags: what one attention call must move at minimum.  Table
+        entries and tags of every live page are read whatever the outcome; a
+        skipped request's KV and scales are not."""
         spec = self.spec
-        lens = self.batch.lens_bh("seq").astype(np.int64)
-        pages = (lens + W.PAGE_SIZE - 1) // W.PAGE_SIZE
-        per_page = 4 + (8 if spec.kv_dtype == "fp8" else 0) + (8 if self.cache.page_tags is not None else 0)
-        return (self.kv_bytes() + int(pages.sum()) * per_page
+        tags = self.cache.page_tags is not None if tags is None else tags
+        all_pages = int(((self._lens() + W.PAGE_SIZE - 1) // W.PAGE_SIZE).sum())
+        read_pages = int(((self._lens(skip) + W.PAGE_SIZE - 1) // W.PAGE_SIZE).sum())
+        return (self.kv_bytes(skip) + 4 * all_pages
+                + (8 * read_pages if spec.kv_dtype == "fp8" else 0)
+                + (8 * all_pages if tags else 0)
                 + 2 * spec.B * spec.Hq * spec.D * 2 + spec.B)

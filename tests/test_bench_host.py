@@ -1,0 +1,66 @@
+"""Host-side logic of the benchmark that needs no GPU: workload selection, the
+80 GB admissibility figure of the sweep, byte accounting and the oracle
+sample shapes."""
+import sys
+import os
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from paged_fp8_kv_decode_gb300 import workloads as W  # noqa: E402
+
+
+def test_sweep_admissible_batch_for_an_80_gb_pool_over_32_layers():
+    # 32,768 tokens x 32 layers x (2 x 8 heads x 128 dims x 2 B) = 4.29 GB per
+    # BF16 sequence -> 18 fit in 80 GB; FP8 (+ two fp32 scales per 16-token
+    # unit and kv head) = 2.15 GB -> 37 fit.
+    assert bench.sweep_admissible(W.spec_sweep(1, "bf16")) == 18
+    assert bench.sweep_admissible(W.spec_sweep(1, "fp8")) == 37
+
+
+def test_workload_spec_names_and_sizes():
+    a = bench.parse_args(["--workload", "sweep", "--batch", "16", "--kv-dtype", "bf16"])
+    s = bench.workload_spec(a)
+    assert (s.B, s.kv_dtype, int(s.lens[0])) == (16, "bf16", 32768)
+    assert s.num_pages == W.sweep_pool_pages("bf16")
+    s = bench.workload_spec(bench.parse_args(["--workload", "long"]))
+    assert s.split_tokens == 4096 and list(s.lens) == [131072, 262144, 393216, 524288]
+    s = bench.workload_spec(bench.parse_args(["--workload", "evict"]))
+    assert s.per_head and s.lens.shape == (16, 8) and s.stale_per_mille == 1.0
+    s = bench.workload_spec(bench.parse_args([]))
+    assert s.name == "llama8b" and s.B == 32 and s.append
+
+
+def test_sample_shape_bounds_the_oracle_work():
+    for spec in (W.spec_llama8b("full"), W.spec_long("full"), W.spec_evict("full"),
+                 W.spec_sweep(64, "fp8")):
+        n, nh = bench._sample_shape(spec)
+        assert 1 <= n <= min(4, spec.B) and 1 <= nh <= spec.Hkv
+        lens = np.asarray(spec.lens).astype(np.int64)
+        per_req = lens if lens.ndim == 1 else lens.max(axis=1)
+        assert int(per_req[:n].sum()) * nh <= 600_000 or (n == 1 and nh == 1)
+
+
+def test_aborted_requests_drop_their_kv_and_scales_but_not_their_tags():
+    class FakeDB:
+        pass
+    from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
+    spec = W.spec_evict("small")
+    db = FakeDB()
+    db.spec, db.batch = spec, W.make_batch(spec)
+    db.cache = type("C", (), {"page_tags": object()})()
+    for name in ("_lens", "kv_bytes", "algorithmic_bytes"):
+        setattr(db, name, getattr(DeviceBatch, name).__get__(db))
+    lens = db.batch.lens_bh("seq").astype(np.int64)
+    pages = (lens + 15) // 16
+    skip = np.zeros(spec.B, bool)
+    skip[1] = True
+    full = db.algorithmic_bytes()
+    part = db.algorithmic_bytes(skip=skip)
+    kv1 = int(lens[1].sum()) * spec.D * 2
+    assert full - part == kv1 + 8 * int(pages[1].sum())
+    assert db.algorithmic_bytes(tags=False) == full - 8 * int(pages.sum())
