@@ -128,13 +128,14 @@ pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_he
         q.nchunks = max_seq_len > 0 ? (max_seq_len + q.chunk_tokens - 1) / q.chunk_tokens : 1;
         q.pers_ctas = q.workers = 0;
     }
+    q.htiles = max(1, (p->max_pages + kValTile - 1) / kValTile);
     const long long items = (long long)q.B * q.Hkv * q.nchunks;
     if (items > 0x7fffffffLL || (long long)q.B * q.Hq > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
     // rows of partial results: one per (b, hq, chunk), or segment + worker
     const size_t rows_kv = q.kind == 1 ? (size_t)items + q.workers : (size_t)items;
     size_t off = 0;
     q.off_hflags = off;
-    off = align256(off + (q.tags ? sizeof(uint32_t) * q.B * q.Hkv : 0));
+    off = align256(off + (q.tags ? sizeof(uint32_t) * q.B * q.Hkv * q.htiles : 0));
     q.off_prefix = off;
     off = align256(off + (q.kind == 1 ? sizeof(int) * ((size_t)items + 1) : 0));
     q.off_status = off;
@@ -286,6 +287,7 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
     a.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): scores in log2 units
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.hflags = plan.tags ? reinterpret_cast<uint32_t *>(ws + plan.off_hflags) : nullptr;
+    a.htiles = plan.htiles;
     a.status = reinterpret_cast<uint32_t *>(ws + plan.off_status);
     a.lse = reinterpret_cast<float *>(ws + plan.off_lse);
     a.o = reinterpret_cast<float *>(ws + plan.off_o);

@@ -131,14 +131,16 @@ cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
 }
 
 // --------------------------------------------------------------------------
-// validate: one CTA per (request, kv head).  Bits for the live entries of the
-// row: LEN for a bad length, PAGE for an id outside the pool, TAG when the
-// pool's tag differs from the expected one.  Written (not OR-ed) to
-// hflags[b][h]; the attention kernels read them after this kernel completes.
+// validate: one CTA per (request, kv head, tile of kValTile table entries).
+// Bits for the live entries of the tile: LEN for a bad length, PAGE for an id
+// outside the pool, TAG when the pool's tag differs from the expected one.
+// Written (not OR-ed) to hflags[b][h][tile]; the attention kernels read them
+// after this kernel completes.  A thread loads all of its page ids, then all
+// of their tags and expected tags, so a tile costs two memory round trips.
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) validate_kernel(DecodeArgs a, int Hkv) {
+__global__ void __launch_bounds__(kValThreads) validate_kernel(DecodeArgs a, int Hkv) {
     pdl_enter();
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x, tile = blockIdx.y;
     const int b = bh / Hkv, h = bh - b * Hkv;
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
     uint32_t bits = 0;
@@ -146,28 +148,44 @@ __global__ void __launch_bounds__(256) validate_kernel(DecodeArgs a, int Hkv) {
         bits = PFKV_FLAG_BAD_LENGTH;
     } else {
         const int np = (n + kPage - 1) / kPage;
+        const int p0 = tile * kValTile + threadIdx.x;
         const long long row = (long long)b * a.bt_sb + (long long)h * a.bt_sh;
-        for (int p = threadIdx.x; p < np; p += blockDim.x) {
-            const int phys = a.block_tables[row + p];
-            if (phys < 0 || phys >= a.num_pages) {
-                bits |= PFKV_FLAG_BAD_PAGE;
-            } else if (a.page_tags[(long long)phys * Hkv + h] != a.expected_tags[row + p]) {
-                bits |= PFKV_FLAG_TAG_MISMATCH;
-            }
+        int id[kValPer];
+#pragma unroll
+        for (int j = 0; j < kValPer; ++j) {
+            const int p = p0 + j * kValThreads;
+            id[j] = p < np ? a.block_tables[row + p] : 0;
         }
+        uint32_t tag[kValPer], want[kValPer];
+#pragma unroll
+        for (int j = 0; j < kValPer; ++j) {
+            const int p = p0 + j * kValThreads;
+            const bool live = p < np;
+            const bool in_pool = id[j] >= 0 && id[j] < a.num_pages;
+            if (live && !in_pool) bits |= PFKV_FLAG_BAD_PAGE;
+            const bool check = live && in_pool;
+            tag[j] = check ? a.page_tags[(long long)id[j] * Hkv + h] : 0u;
+            want[j] = check ? a.expected_tags[row + p] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < kValPer; ++j)
+            if (tag[j] != want[j]) bits |= PFKV_FLAG_TAG_MISMATCH;
     }
+    const int any_len = __syncthreads_or(bits & PFKV_FLAG_BAD_LENGTH);
     const int any_page = __syncthreads_or(bits & PFKV_FLAG_BAD_PAGE);
     const int any_tag = __syncthreads_or(bits & PFKV_FLAG_TAG_MISMATCH);
     if (threadIdx.x == 0) {
-        uint32_t f = bits & PFKV_FLAG_BAD_LENGTH;
+        uint32_t f = 0;
+        if (any_len) f |= PFKV_FLAG_BAD_LENGTH;
         if (any_page) f |= PFKV_FLAG_BAD_PAGE;
         if (any_tag) f |= PFKV_FLAG_TAG_MISMATCH;
-        a.hflags[bh] = f;
+        a.hflags[(long long)bh * gridDim.y + tile] = f;
     }
 }
 
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    return launch_pdl(validate_kernel, dim3(p.B * p.Hkv), dim3(256), 0, s, a, p.Hkv);
+    return launch_pdl(validate_kernel, dim3(p.B * p.Hkv, p.htiles), dim3(kValThreads), 0, s, a,
+                      p.Hkv);
 }
 
 // --------------------------------------------------------------------------

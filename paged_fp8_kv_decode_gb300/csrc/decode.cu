@@ -150,11 +150,7 @@ __global__ void __launch_bounds__(SplitCfg<D, G, FP8>::NWARPS * 32)
     if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) return;
     const int tok0 = chunk * chunk_tokens;
     if (tok0 >= n) return;  // empty item
-    if (a.hflags) {         // request rejected by the validation kernel
-        uint32_t f = 0;
-        for (int i = 0; i < Hkv; ++i) f |= a.hflags[b * Hkv + i];
-        if (f) return;
-    }
+    if (request_rejected_cta(a, b, Hkv)) return;  // rejected by the validation kernel
     const int tok1 = min(n, tok0 + chunk_tokens);
     const int p_begin = tok0 / kPage;
     const int npages = (tok1 - tok0 + kPage - 1) / kPage;
@@ -394,8 +390,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int Hkv
         const int ni = a.seq_lens[(long long)b * a.len_sb + (long long)i * a.len_sh];
         if (ni < 0 || (long long)ni > (long long)a.max_pages * kPage || ni > a.max_seq_len)
             f |= PFKV_FLAG_BAD_LENGTH;
-        if (a.hflags) f |= a.hflags[b * Hkv + i];
     }
+    if (a.hflags)
+        for (int i = tid; i < Hkv * a.htiles; i += D) f |= a.hflags[(long long)b * Hkv * a.htiles + i];
     if (f) atomicOr(&s_flags, f);
     __syncthreads();
     // ... then the split kernel's per-chunk status (only written for live

@@ -162,11 +162,12 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     pdl_enter();
 
     // ---------------- prologue: request flags, unit prefix sums ----------------
-    for (int b = tid; b < B; b += C::NT) {
-        uint32_t f = 0;
-        if (a.hflags)
-            for (int i = 0; i < Hkv; ++i) f |= a.hflags[b * Hkv + i];
-        sm.rflag[b] = f ? 1 : 0;
+    for (int b = tid; b < B; b += C::NT) sm.rflag[b] = 0;
+    __syncthreads();
+    if (a.hflags) {  // [B][Hkv][htiles], read in parallel
+        const int per_req = Hkv * a.htiles;
+        for (int i = tid; i < B * per_req; i += C::NT)
+            if (a.hflags[i]) sm.rflag[i / per_req] = 1;
     }
     __syncthreads();
     const int per = (K + C::NT - 1) / C::NT;
@@ -680,87 +681,206 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
 
 // --------------------------------------------------------------------------
 // combine for the persistent layout: the rows of segment k are k + p for the
-// workers p that touched it.  One CTA per (request b, kv head h), one warp per
-// query head of the group, lane l owning dims [4l, 4l + 4); the request's
-// flags come from every segment of the request, looked up in parallel.
+// workers p that touched it.  One CTA of 8 warps per (request b, kv head h):
+//  1. the request's flags: lengths and validation bits of every kv head and
+//     the status rows of every segment of the request, in parallel;
+//  2. the rows of (b, h), flattened: chunk c owns rows [cstart[c], cstart[c+1])
+//     of the flat order, the first at workspace row cbase[c];
+//  3. M = max lse per query head, over all rows, in parallel;
+//  4. each warp accumulates exp2(lse - M)-weighted rows j = warp, warp + 8, ...
+//     (lane l owns dims [4l, 4l + 4) of every query head of the group);
+//  5. the warps' sums meet in shared memory; out = sum / weight, bf16.
 // --------------------------------------------------------------------------
+constexpr int kCombThreads = 256;
+constexpr int kCombWarps = kCombThreads / 32;
+constexpr int kCombMaxChunks = PersCfg<1>::MAXK;  // segments per (b, h) <= all segments
+
 template <int G>
-__global__ void __launch_bounds__(32 * G) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
-                                                                     int nchunks, int W,
-                                                                     const int *ws_prefix) {
-    constexpr int D = 128, NT = 32 * G;
-    __shared__ uint32_t s_flags;
+struct CombSmem {
+    union {
+        struct {
+            int cstart[kCombMaxChunks + 1];
+            int cbase[kCombMaxChunks];
+        } rows;
+        struct {
+            float acc[kCombWarps][G][128];
+            float wsum[kCombWarps][G];
+        } red;
+    } u;
+    int part[kCombThreads];
+    float mred[kCombWarps][G];
+    uint32_t flags;
+};
+
+template <int G>
+__global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
+                                                                          int nchunks, int W,
+                                                                          const int *ws_prefix) {
+    constexpr int D = 128, NT = kCombThreads, NW = kCombWarps;
+    __shared__ CombSmem<G> sm;
     pdl_enter();
     const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = gridDim.x / Hkv;
     const int K = B * Hkv * nchunks;
-    const long long U = ws_prefix[K];
-    W = (int)min((long long)W, U);  // as in the split kernel
-    if (tid == 0) s_flags = 0;
+    const int U = ws_prefix[K];
+    W = min(W, U);  // as in the split kernel
+    if (tid == 0) sm.flags = 0;
     __syncthreads();
+
+    // ---- 1. request flags ----
     uint32_t f = 0;
     for (int i = tid; i < Hkv; i += NT) {
         const int ni = a.seq_lens[(long long)b * a.len_sb + (long long)i * a.len_sh];
         if (ni < 0 || (long long)ni > (long long)a.max_pages * kPage || ni > a.max_seq_len)
             f |= PFKV_FLAG_BAD_LENGTH;
-        if (a.hflags) f |= a.hflags[b * Hkv + i];
     }
-    // rows of the request's segments (requests the validation rejected have none)
-    if (U > 0) {
+    if (a.hflags)
+        for (int i = tid; i < Hkv * a.htiles; i += NT) f |= a.hflags[(long long)b * Hkv * a.htiles + i];
+    if (U > 0) {  // rows of the request's segments (rejected requests have none)
         for (int it = tid; it < Hkv * nchunks; it += NT) {
             const int k = b * Hkv * nchunks + it;
-            const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+            const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
             if (u1 == u0) continue;
             const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
             for (int p = p0; p <= p1; ++p) f |= a.status[k + p];
         }
     }
-    if (f) atomicOr(&s_flags, f);
+    if (f) atomicOr(&sm.flags, f);
     __syncthreads();
-    const uint32_t flags = s_flags;
+    const uint32_t flags = sm.flags;
     if (h == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
-    const int hq = h * G + warp;
-    uint2 *out = reinterpret_cast<uint2 *>(a.out + ((long long)b * Hkv * G + hq) * D + lane * 4);
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+    uint2 *out = reinterpret_cast<uint2 *>(a.out + (long long)(b * Hkv + h) * G * D);
     if (flags != 0 || n == 0 || U == 0) {
-        *out = make_uint2(0u, 0u);
+        for (int i = tid; i < G * D / 4; i += NT) out[i] = make_uint2(0u, 0u);
         return;
     }
-    float M = -INFINITY;
-    for (int c = 0; c < nchunks; ++c) {
-        const int k = (b * Hkv + h) * nchunks + c;
-        const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
-        if (u1 == u0) continue;
-        const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
-        for (int p = p0 + lane; p <= p1; p += 32) M = fmaxf(M, a.lse[(long long)(k + p) * G + warp]);
+
+    // ---- 2. flat row order: per-thread chunk ranges, scanned by one warp ----
+    const int kbase = (b * Hkv + h) * nchunks;
+    const int per = (nchunks + NT - 1) / NT;
+    const int c0 = min(nchunks, tid * per), c1 = min(nchunks, c0 + per);
+    int local = 0;
+    for (int c = c0; c < c1; ++c) {
+        const int k = kbase + c;
+        const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+        int cnt = 0, base = 0;
+        if (u1 > u0) {
+            const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
+            cnt = p1 - p0 + 1;
+            base = k + p0;
+        }
+        sm.u.rows.cstart[c] = cnt;  // the count, turned into the start below
+        sm.u.rows.cbase[c] = base;
+        local += cnt;
     }
+    sm.part[tid] = local;
+    __syncthreads();
+    if (tid < 32) {
+        int carry = 0;
+        for (int base = 0; base < NT; base += 32) {
+            const int v = sm.part[base + tid];
+            int x = v;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
-        const int k = (b * Hkv + h) * nchunks + c;
-        const long long u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
-        if (u1 == u0) continue;
-        const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
-#pragma unroll 4
-        for (int p = p0; p <= p1; ++p) {
-            const long long row = (long long)(k + p) * G + warp;
-            const float lc = a.lse[row];
-            const float wt = lc == -INFINITY ? 0.f : pexp2(lc - M);
-            const float4 ov = *reinterpret_cast<const float4 *>(a.o + row * D + lane * 4);
-            wsum += wt;
-            acc.x = fmaf(wt, ov.x, acc.x);
-            acc.y = fmaf(wt, ov.y, acc.y);
-            acc.z = fmaf(wt, ov.z, acc.z);
-            acc.w = fmaf(wt, ov.w, acc.w);
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (tid >= off) x += y;
+            }
+            sm.part[base + tid] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (tid == 0) sm.u.rows.cstart[nchunks] = carry;
+    }
+    __syncthreads();
+    {
+        int run = sm.part[tid];
+        for (int c = c0; c < c1; ++c) {
+            const int cnt = sm.u.rows.cstart[c];
+            sm.u.rows.cstart[c] = run;
+            run += cnt;
         }
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    *out = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    __syncthreads();
+    const int R = sm.u.rows.cstart[nchunks];
+    // workspace row of flat row j (chunks with no rows never contain j)
+    auto row_of = [&](int j) {
+        int lo = 0, hi = nchunks;  // cstart[lo] <= j < cstart[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (sm.u.rows.cstart[mid] <= j) lo = mid;
+            else hi = mid;
+        }
+        return sm.u.rows.cbase[lo] + (j - sm.u.rows.cstart[lo]);
+    };
+
+    // ---- 3. M per query head (thread tid always sees head tid % G) ----
+    const int gm = tid % G;
+    float mx = -INFINITY;
+    for (int idx = tid; idx < R * G; idx += NT) mx = fmaxf(mx, a.lse[(long long)row_of(idx / G) * G + gm]);
+#pragma unroll
+    for (int off = 16; off >= G; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane < G) sm.mred[warp][lane] = mx;
+    __syncthreads();
+    float M[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        M[g] = sm.mred[0][g];
+#pragma unroll
+        for (int w2 = 1; w2 < NW; ++w2) M[g] = fmaxf(M[g], sm.mred[w2][g]);
+    }
+
+    // ---- 4. weighted sums, rows spread over the warps ----
+    float4 acc[G];
+    float wsum[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        wsum[g] = 0.f;
+    }
+#pragma unroll 2
+    for (int j = warp; j < R; j += NW) {
+        const long long row = row_of(j);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float lc = a.lse[row * G + g];
+            const float wt = lc == -INFINITY ? 0.f : pexp2(lc - M[g]);
+            const float4 ov = *reinterpret_cast<const float4 *>(a.o + (row * G + g) * D + lane * 4);
+            wsum[g] += wt;
+            acc[g].x = fmaf(wt, ov.x, acc[g].x);
+            acc[g].y = fmaf(wt, ov.y, acc[g].y);
+            acc[g].z = fmaf(wt, ov.z, acc[g].z);
+            acc[g].w = fmaf(wt, ov.w, acc[g].w);
+        }
+    }
+    __syncthreads();  // the row tables are dead: their space takes the sums
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        *reinterpret_cast<float4 *>(&sm.u.red.acc[warp][g][lane * 4]) = acc[g];
+        if (lane == 0) sm.u.red.wsum[warp][g] = wsum[g];
+    }
+    __syncthreads();
+
+    // ---- 5. out = sum over warps / weight over warps ----
+    for (int i = tid; i < G * D / 4; i += NT) {
+        const int g = i / (D / 4), d4 = i - g * (D / 4);
+        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float ws = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < NW; ++w2) {
+            const float4 v = *reinterpret_cast<const float4 *>(&sm.u.red.acc[w2][g][d4 * 4]);
+            s4.x += v.x;
+            s4.y += v.y;
+            s4.z += v.z;
+            s4.w += v.w;
+            ws += sm.u.red.wsum[w2][g];
+        }
+        const float inv = ws > 0.f ? 1.f / ws : 0.f;
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x * inv, s4.y * inv);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z * inv, s4.w * inv);
+        out[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                            *reinterpret_cast<const uint32_t *>(&hi));
+    }
 }
 
 // --------------------------------------------------------------------------
@@ -811,9 +931,9 @@ cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaSt
     const int W = p.pers_ctas * PersCfg<4>::PAIRS;
     const dim3 grid((unsigned)(p.B * p.Hkv));
     switch (p.G) {
-        case 1: return launch_pdl(decode_combine_pers_kernel<1>, grid, dim3(32), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
-        case 2: return launch_pdl(decode_combine_pers_kernel<2>, grid, dim3(64), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
-        case 4: return launch_pdl(decode_combine_pers_kernel<4>, grid, dim3(128), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+        case 1: return launch_pdl(decode_combine_pers_kernel<1>, grid, dim3(kCombThreads), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+        case 2: return launch_pdl(decode_combine_pers_kernel<2>, grid, dim3(kCombThreads), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+        case 4: return launch_pdl(decode_combine_pers_kernel<4>, grid, dim3(kCombThreads), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
     }
     return cudaErrorInvalidValue;
 }

@@ -141,11 +141,7 @@ __global__ void __launch_bounds__(SwzCfg<G>::NWARPS * 32)
     if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) return;
     const int tok0 = chunk * chunk_tokens;
     if (tok0 >= n) return;
-    if (a.hflags) {
-        uint32_t f = 0;
-        for (int i = 0; i < Hkv; ++i) f |= a.hflags[b * Hkv + i];
-        if (f) return;
-    }
+    if (request_rejected_cta(a, b, Hkv)) return;  // rejected by the validation kernel
     const int tok1 = min(n, tok0 + chunk_tokens);
     const int p_begin = tok0 / kPage;
     const int nunits = (tok1 - tok0 + kPage - 1) / kPage;

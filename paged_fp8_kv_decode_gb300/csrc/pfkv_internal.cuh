@@ -16,6 +16,11 @@ constexpr int kPage = PFKV_PAGE_SIZE;
 // per-(request, kv head, chunk) status bits written by the split kernel
 constexpr uint32_t kStatusBadPage = PFKV_FLAG_BAD_PAGE;
 constexpr uint32_t kStatusTimeout = PFKV_FLAG_DEVICE_TIMEOUT;
+// validation: a CTA checks kValTile live entries of one table row, each of its
+// kValThreads threads kValPer of them with all loads issued before any is used
+constexpr int kValThreads = 256;
+constexpr int kValPer = 8;
+constexpr int kValTile = kValThreads * kValPer;
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 100ull * 1000ull * 1000ull;
@@ -35,6 +40,7 @@ struct DecodePlan {
     //         indexed segment + worker, pers_ctas CTAs
     int kind;
     int pers_ctas, workers;
+    int htiles;         // validation tiles per table row: ceil(max_pages / kValTile)
     // workspace layout (byte offsets, 256-aligned)
     size_t off_hflags, off_status, off_lse, off_o, off_prefix, total;
 };
@@ -58,7 +64,8 @@ struct DecodeArgs {
     uint8_t *flags;
     float q_scale;      // sm_scale * log2(e): scores are kept in log2 units
     // workspace
-    uint32_t *hflags;   // [B][Hkv] tag/bounds bits from the validation kernel
+    uint32_t *hflags;   // [B][Hkv][htiles] tag/bounds bits from the validation kernel
+    int htiles;
     uint32_t *status;   // [B][Hkv][nchunks]
     float *lse;         // [B][Hq][nchunks]  log2-sum-exp of the chunk
     float *o;           // [B][Hq][nchunks][D] chunk output (normalised)
@@ -100,6 +107,18 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Whether the validation kernel flagged request b (any kv head, any tile).
+// Computed by the whole CTA: every thread must call it.
+__device__ __forceinline__ bool request_rejected_cta(const DecodeArgs &a, int b, int Hkv) {
+    int f = 0;
+    if (a.hflags) {
+        const int n = Hkv * a.htiles;
+        const uint32_t *src = a.hflags + (long long)b * n;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) f |= src[i] != 0u;
+    }
+    return __syncthreads_or(f) != 0;
 }
 
 // launchers (defined in the .cu files)
