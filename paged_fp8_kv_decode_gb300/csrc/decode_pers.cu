@@ -21,10 +21,11 @@
 // bulk copy; a quarter-warp reads one 128-byte row, so the linear layout is
 // free of bank conflicts):
 //  * the score warp holds a 16-dim slice of the G query heads in registers
-//    (lane (t, c): slice c, token 4r + t in pass r), converts K bytes to fp32
-//    pairs, takes packed fp32x2 dot products, finishes each score with a
-//    reduce-scatter over the 8 lanes of a token group (so lane (t, c) ends with
-//    the G scores of token 4c + t) and hands the value warp the raw scores;
+//    (lane (t, c): slice c, row 4r + t of a unit in pass r), converts K bytes
+//    to fp32 pairs, takes packed fp32x2 dot products, finishes each score with
+//    a select-free reduce-scatter over the 8 lanes of a token group (so lane
+//    (t, c) ends with the G scores of token 4c + t) and hands the value warp
+//    the raw scores;
 //  * the value warp keeps a window of unit metadata (page id, K and V scales,
 //    bad-id bit) for the next 64 units in registers, turns the raw scores into
 //    probabilities (online softmax per granule, lazy rescale), accumulates
@@ -344,15 +345,23 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
             if (!mbar_wait_bounded(&P.full[s], parity)) status |= kStatusTimeout;
             const uint8_t *stage = P.ring[s];
 
-            // ---- partial dot products: slice vc, token 4r + vt ----
-            // Passes r and r + 4 are computed together and folded at once by the
-            // first reduce-scatter level (xor 4), so at most 24 partials are live.
-            const bool bA = vc & 4, bB = vc & 2, bC = vc & 1;
+            // ---- partial dot products and the reduce-scatter ----
+            // Lane (vt, vc) ends with the scores of token 4 vc + vt, i.e. pass
+            // vc: row 4 (vc & 3) + vt of unit vc >> 2.  The reduce-scatter folds
+            // the 8 passes in three levels (xor 4, 2, 1 between lanes); at each
+            // level a lane keeps the half named by its own bit of vc (bA, bB, bC:
+            // bits 2, 1, 0) and sends the other half.  Computing the passes in a
+            // lane-dependent order puts the kept half and the sent half in fixed
+            // registers, so no level needs a select: level-1 slot j holds row
+            // 4 (j ^ 2 bB ^ bC) + vt, of unit bA (kept) and of unit 1 - bA (sent).
+            // Each pair of passes is folded as soon as it is computed, so at most
+            // 24 partials are live.
+            const int bA = (vc >> 2) & 1, bB = (vc >> 1) & 1, bC = vc & 1;
+            const uint8_t *kkeep = stage + bA * C::UNITB + vt * C::ROWB + (vc << 4);
+            const uint8_t *ksend = stage + (bA ^ 1) * C::UNITB + vt * C::ROWB + (vc << 4);
             float r1[4][G], r2[2][G], sc[G];
-            auto dot_pass = [&](int r, float (&pr)[G]) {
-                const int row = 4 * (r & 3) + vt;
-                const uint8_t *krow = stage + (r >> 2) * C::UNITB + row * C::ROWB;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(krow + (vc << 4));
+            auto dot_row = [&](const uint8_t *krow, float (&pr)[G]) {
+                const uint4 wv = *reinterpret_cast<const uint4 *>(krow);
                 float2 kf[8];
                 pdequant16(wv, kf);
 #pragma unroll
@@ -364,31 +373,21 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 }
             };
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                float lo[G], hi[G];
-                dot_pass(r, lo);
-                dot_pass(r + 4, hi);
+            for (int j = 0; j < 4; ++j) {
+                const int roff = 4 * (j ^ (2 * bB) ^ bC) * C::ROWB;
+                float keep[G], send[G];
+                dot_row(kkeep + roff, keep);
+                dot_row(ksend + roff, send);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float snd = bA ? lo[g] : hi[g];
-                    const float kp = bA ? hi[g] : lo[g];
-                    r1[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 4);
-                }
+                for (int g = 0; g < G; ++g) r1[j][g] = keep[g] + __shfl_xor_sync(0xffffffffu, send[g], 4);
             }
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float snd = bB ? r1[r][g] : r1[r + 2][g];
-                    const float kp = bB ? r1[r + 2][g] : r1[r][g];
-                    r2[r][g] = kp + __shfl_xor_sync(0xffffffffu, snd, 2);
-                }
+                for (int g = 0; g < G; ++g)
+                    r2[j][g] = r1[j][g] + __shfl_xor_sync(0xffffffffu, r1[j + 2][g], 2);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float snd = bC ? r2[0][g] : r2[1][g];
-                const float kp = bC ? r2[1][g] : r2[0][g];
-                sc[g] = kp + __shfl_xor_sync(0xffffffffu, snd, 1);
-            }
+            for (int g = 0; g < G; ++g) sc[g] = r2[0][g] + __shfl_xor_sync(0xffffffffu, r2[1][g], 1);
             // lane (vt, vc) now holds the G raw scores of token 4 vc + vt
             if constexpr (G == 4) {
                 *reinterpret_cast<float4 *>(P.sb[s].s[lane]) = make_float4(sc[0], sc[1], sc[2], sc[3]);
