@@ -63,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--replicas", type=int, default=8)
     ap.add_argument("--split", type=int, default=0, help="split-KV tokens (0 = library choice)")
     ap.add_argument("--no-tags", action="store_true", help="no-op tracker (no tag validation)")
+    ap.add_argument("--fused-tags", action="store_true",
+                    help="tag check inside the attention kernel instead of a separate pass")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -164,8 +166,9 @@ class ClockSampler:
 class PreparedStep:
     """The C-ABI calls of one step with their argument structs built once."""
 
-    def __init__(self, db, B, stream_handle, cache=None, pages=None):
+    def __init__(self, db, B, stream_handle, cache=None, pages=None, fused_tags=False):
         self.db, self.B, self.s = db, B, stream_handle
+        self.opt = B.PFKV_STAGE_FUSED_TAGS if fused_tags else 0
         L = B.lib()
         self.L = L
         self.c = (cache or db.cache).c_struct()
@@ -187,7 +190,7 @@ class PreparedStep:
                 raise RuntimeError(f"pfkv_kv_append: status {st}")
 
     def stage(self, mask):
-        st = self.L.pfkv_paged_decode_attn_stages(*self.args, mask, self.s)
+        st = self.L.pfkv_paged_decode_attn_stages(*self.args, mask | self.opt, self.s)
         if st:
             raise RuntimeError(f"pfkv_paged_decode_attn_stages: status {st}")
 
@@ -248,7 +251,7 @@ def run_gpu(args):
         if args.no_tags:
             spec.tags = False
         db = DeviceBatch(W.make_batch(spec), device=dev)
-        reps.append(PreparedStep(db, B, sh))
+        reps.append(PreparedStep(db, B, sh, fused_tags=args.fused_tags))
     torch.cuda.synchronize()
     spec0 = reps[0].db.spec
     # bytes per step (same shapes in every replica; lengths differ): mean over replicas
@@ -337,6 +340,8 @@ def run_gpu(args):
                        "num_kv_heads": spec0.Hkv, "head_dim": spec0.D, "page_size": 16,
                        "seq_lens": "U[512,8192]+1 appended", "num_pages": spec0.num_pages,
                        "kv_dtype": spec0.kv_dtype, "tags": not args.no_tags,
+                       "tag_check": ("none" if args.no_tags else
+                                     "fused into attention" if args.fused_tags else "separate pass"),
                        "split_tokens": args.split, "replicas": args.replicas,
                        "l2": "inputs larger than L2: %d rotating replicas, %.0f MB live KV each"
                              % (args.replicas, kv_bytes / 1e6),
@@ -351,7 +356,7 @@ def run_gpu(args):
                          "peak_kind": peak_kind, "avg_launch_us": round(split_avg * 1e6, 3),
                          "bytes_per_launch": int(split_bytes),
                          "timed_launches": len(split_ms)},
-            "e2e": e2e, "gpu_launches": K * (3 if args.no_tags else 4),
+            "e2e": e2e, "gpu_launches": K * (3 if (args.no_tags or args.fused_tags) else 4),
             "clocks": clocks, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -608,6 +613,9 @@ def run_workload(args):
                         db.pages.bt_stride_b, db.pages.bt_stride_h, db.pages.seq_lens,
                         db.pages.len_stride_b, db.pages.len_stride_h, None)
         variants.append(("tags_all_match", PreparedStep(db, B, sh, cache=c_match), True))
+        variants.append(("fused_tags_all_match",
+                         PreparedStep(db, B, sh, cache=c_match, fused_tags=True), True))
+        variants.append(("fused_tags", PreparedStep(db, B, sh, fused_tags=True), True))
         variants.append(("no_tags", PreparedStep(db, B, sh, cache=db.cache_untracked,
                                                  pages=p_off), False))
     flush = L2Flush(dev)
@@ -707,12 +715,15 @@ def run_workload(args):
                      "bytes_per_launch": int(split_bytes), "timed_launches": len(split_ms)},
         "variants": results if len(results) > 1 else None,
         "gpu_launches": K * (len(variants) * (3 if spec.append else 2) + 3) + sum(
-            K for _, _, t in variants if t),
+            K for _, p, t in variants if t and not p.opt),
         "clocks": clocks,
     }
     if "tags_all_match" in results and "no_tags" in results:
-        a, b = results["tags_all_match"]["ms_per_step"], results["no_tags"]["ms_per_step"]
+        b = results["no_tags"]["ms_per_step"]
+        a = results["tags_all_match"]["ms_per_step"]
         line["tag_overhead_pct"] = round(100 * (a - b) / b, 2)
+        a = results["fused_tags_all_match"]["ms_per_step"]
+        line["fused_tag_overhead_pct"] = round(100 * (a - b) / b, 2)
     line["e2e"] = run_e2e_flushed(args, p0, B, stream, r0["bytes_per_step"], world, dev, flush)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_spec(spec)

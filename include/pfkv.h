@@ -202,6 +202,10 @@ pfkv_status pfkv_paged_decode_attn(const pfkv_cache *cache, const pfkv_pages *pa
 #define PFKV_STAGE_SPLIT 0x2u     /* per-chunk attention into the workspace       */
 #define PFKV_STAGE_COMBINE 0x4u   /* merge chunks, write out and flags            */
 #define PFKV_STAGE_ALL 0x7u
+/* Not a stage: an option bit of pfkv_paged_decode_attn_stages.  With it the
+ * tag comparison runs inside the SPLIT stage's page loop, as in
+ * pfkv_paged_decode_attn_fused_tags, and VALIDATE launches nothing. */
+#define PFKV_STAGE_FUSED_TAGS 0x8u
 
 /*
  * pfkv_paged_decode_attn_stages -- the same computation as
@@ -212,13 +216,39 @@ pfkv_status pfkv_paged_decode_attn(const pfkv_cache *cache, const pfkv_pages *pa
  * The workspace carries the state between stages; calling a later stage
  * without the earlier ones of the same arguments gives unspecified (but
  * in-bounds) output.  Lets a caller time or interleave the kernels.
- * stages == 0 or containing unknown bits: PFKV_ERR_INVALID_ARG.
+ * PFKV_STAGE_FUSED_TAGS may be added to any mask (see below).
+ * No stage bit, or an unknown bit: PFKV_ERR_INVALID_ARG.
  */
 pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pages *pages,
                                           const void *q, int32_t num_q_heads, float sm_scale,
                                           int32_t split_tokens, int32_t max_seq_len,
                                           void *workspace, size_t workspace_bytes, void *out,
                                           uint8_t *flags, uint32_t stages, void *stream);
+
+/*
+ * pfkv_paged_decode_attn_fused_tags -- pfkv_paged_decode_attn with the
+ * integrity check moved into the attention kernel.
+ *
+ * The tag-check page ("Cloudflare quantizes Kimi and GLM caches ...", 4th
+ * paragraph) keeps the check in a separate batch pass because, fused into its
+ * attention kernel, it would race with the use of the data.  Here no output
+ * is written before the combine stage, and the combine is stream-ordered
+ * after every attention CTA, so the check can run where the page ids are
+ * loaded: each live entry's pool tag is compared with its expected tag, a
+ * mismatching unit is not read, and the mismatch reaches the request's flags
+ * through the per-segment status that the combine ORs.
+ *
+ * Same arguments, workspace size, out and flags as pfkv_paged_decode_attn:
+ * the same bits for the same inputs, and all-zero output for a flagged
+ * request.  One difference is visible only as memory traffic: the matching
+ * pages of a request that has a mismatch elsewhere are still read.  Without
+ * tags (page_tags NULL) the two calls are identical.
+ */
+pfkv_status pfkv_paged_decode_attn_fused_tags(const pfkv_cache *cache, const pfkv_pages *pages,
+                                              const void *q, int32_t num_q_heads, float sm_scale,
+                                              int32_t split_tokens, int32_t max_seq_len,
+                                              void *workspace, size_t workspace_bytes, void *out,
+                                              uint8_t *flags, void *stream);
 
 /*
  * pfkv_paged_decode_attn_noalloc -- pfkv_paged_decode_attn without a

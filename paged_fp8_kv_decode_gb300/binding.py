@@ -38,10 +38,12 @@ PFKV_STAGE_VALIDATE = 0x1
 PFKV_STAGE_SPLIT = 0x2
 PFKV_STAGE_COMBINE = 0x4
 PFKV_STAGE_ALL = 0x7
+PFKV_STAGE_FUSED_TAGS = 0x8
 
 # every symbol include/pfkv.h declares
 EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",
-            "pfkv_paged_decode_attn_stages", "pfkv_paged_decode_attn_noalloc", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string", "pfkv_abi_version")
+            "pfkv_paged_decode_attn_stages", "pfkv_paged_decode_attn_fused_tags",
+            "pfkv_paged_decode_attn_noalloc", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string", "pfkv_abi_version")
 
 
 class PfkvError(RuntimeError):
@@ -95,6 +97,8 @@ def lib() -> ctypes.CDLL:
                                                     ctypes.c_float, I32, I32, P, ctypes.c_size_t,
                                                     P, P, ctypes.c_uint32, P]
         L.pfkv_paged_decode_attn_stages.restype = ctypes.c_int
+        L.pfkv_paged_decode_attn_fused_tags.argtypes = L.pfkv_paged_decode_attn.argtypes
+        L.pfkv_paged_decode_attn_fused_tags.restype = ctypes.c_int
         L.pfkv_paged_decode_attn_noalloc.argtypes = [ctypes.POINTER(_CCache),
                                                      ctypes.POINTER(_CPages), P, I32,
                                                      ctypes.c_float, I32, I32, P, P, P]
@@ -242,6 +246,20 @@ def pfkv_paged_decode_attn_stages(cache: Cache, pages: Pages, q: torch.Tensor, s
         ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
         int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), _ptr(flags), int(stages), _stream(stream)), "pfkv_paged_decode_attn_stages")
+
+
+def pfkv_paged_decode_attn_fused_tags(cache: Cache, pages: Pages, q: torch.Tensor,
+                                      sm_scale: float, split_tokens: int, max_seq_len: int,
+                                      workspace: torch.Tensor, out: torch.Tensor,
+                                      flags: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pfkv_paged_decode_attn with the tag check inside the attention kernel
+    (same outputs and flags; see include/pfkv.h)."""
+    c, p = cache.c_struct(), pages.c_struct()
+    Hq = int(q.shape[1])
+    _check(lib().pfkv_paged_decode_attn_fused_tags(
+        ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
+        int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(flags), _stream(stream)), "pfkv_paged_decode_attn_fused_tags")
 
 
 # bytes of the library's own workspace used by pfkv_paged_decode_attn_noalloc

@@ -243,7 +243,9 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
                                           int32_t split_tokens, int32_t max_seq_len,
                                           void *workspace, size_t workspace_bytes, void *out,
                                           uint8_t *flags, uint32_t stages, void *stream) {
-    if (stages == 0 || (stages & ~PFKV_STAGE_ALL)) return PFKV_ERR_INVALID_ARG;
+    if ((stages & PFKV_STAGE_ALL) == 0 || (stages & ~(PFKV_STAGE_ALL | PFKV_STAGE_FUSED_TAGS)))
+        return PFKV_ERR_INVALID_ARG;
+    const bool fused = (stages & PFKV_STAGE_FUSED_TAGS) != 0;
     pfkv_status st = check_cache(cache);
     if (st != PFKV_OK) return st;
     st = check_pages(cache, pages);
@@ -286,15 +288,16 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
     a.flags = flags;
     a.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): scores in log2 units
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    a.hflags = plan.tags ? reinterpret_cast<uint32_t *>(ws + plan.off_hflags) : nullptr;
+    a.hflags = plan.tags && !fused ? reinterpret_cast<uint32_t *>(ws + plan.off_hflags) : nullptr;
     a.htiles = plan.htiles;
+    a.fuse_tags = plan.tags && fused ? 1 : 0;
     a.status = reinterpret_cast<uint32_t *>(ws + plan.off_status);
     a.lse = reinterpret_cast<float *>(ws + plan.off_lse);
     a.o = reinterpret_cast<float *>(ws + plan.off_o);
     a.ws_prefix = reinterpret_cast<int *>(ws + plan.off_prefix);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((stages & PFKV_STAGE_VALIDATE) && plan.tags && launch_validate(a, plan, s) != cudaSuccess)
+    if ((stages & PFKV_STAGE_VALIDATE) && plan.tags && !fused && launch_validate(a, plan, s) != cudaSuccess)
         return PFKV_ERR_CUDA;
     if ((stages & PFKV_STAGE_SPLIT) && launch_split(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     if ((stages & PFKV_STAGE_COMBINE) && launch_combine(a, plan, s) != cudaSuccess)
@@ -310,6 +313,16 @@ pfkv_status pfkv_paged_decode_attn(const pfkv_cache *cache, const pfkv_pages *pa
     return pfkv_paged_decode_attn_stages(cache, pages, q, num_q_heads, sm_scale, split_tokens,
                                          max_seq_len, workspace, workspace_bytes, out, flags,
                                          PFKV_STAGE_ALL, stream);
+}
+
+pfkv_status pfkv_paged_decode_attn_fused_tags(const pfkv_cache *cache, const pfkv_pages *pages,
+                                              const void *q, int32_t num_q_heads, float sm_scale,
+                                              int32_t split_tokens, int32_t max_seq_len,
+                                              void *workspace, size_t workspace_bytes, void *out,
+                                              uint8_t *flags, void *stream) {
+    return pfkv_paged_decode_attn_stages(cache, pages, q, num_q_heads, sm_scale, split_tokens,
+                                         max_seq_len, workspace, workspace_bytes, out, flags,
+                                         PFKV_STAGE_ALL | PFKV_STAGE_FUSED_TAGS, stream);
 }
 
 pfkv_status pfkv_e4m3_encode(const float *x, int64_t n, uint8_t *out, void *stream) {

@@ -161,10 +161,11 @@ __global__ void __launch_bounds__(SplitCfg<D, G, FP8>::NWARPS * 32)
     // ---- per-warp unit metadata: page ids first (they gate the copies) ----
     uint32_t bad = 0;
     for (int i = lane; i < nmine; i += 32) {
-        const int phys = a.block_tables[bt_row + p_begin + warp + i * NW];
-        const bool ok = phys >= 0 && phys < a.num_pages;
-        if (!ok) bad = kStatusBadPage;
-        sm.phys[warp][i] = ok ? phys : -1;
+        const long long bi = bt_row + p_begin + warp + i * NW;
+        const int phys = a.block_tables[bi];
+        const uint32_t eb = entry_bits(a, phys, h, Hkv, bi);
+        bad |= eb;
+        sm.phys[warp][i] = eb ? -1 : phys;
     }
     if (lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(&sm.bar[warp][s], 1);

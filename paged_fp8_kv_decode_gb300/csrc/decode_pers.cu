@@ -427,13 +427,10 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 const int bh = k / nchunks, c = k - bh * nchunks;
                 const int b = bh / Hkv, h = bh - b * Hkv;
                 const int page = c * (chunk_tokens / kPage) + (int)(x - sm.prefix[k]);
-                const int id = a.block_tables[(long long)b * a.bt_sb + (long long)h * a.bt_sh + page];
-                if (id < 0 || id >= a.num_pages) {
-                    phys = -1;
-                    bad = kStatusBadPage;
-                } else {
-                    phys = id * Hkv + h;  // unit index
-                }
+                const long long bi = (long long)b * a.bt_sb + (long long)h * a.bt_sh + page;
+                const int id = a.block_tables[bi];
+                bad = entry_bits(a, id, h, Hkv, bi);
+                phys = bad ? -1 : id * Hkv + h;  // unit index
             }
         };
         auto load_scales = [&](int phys, float &ks, float &vs) {

@@ -155,9 +155,11 @@ __global__ void __launch_bounds__(SwzCfg<G>::NWARPS * 32)
         const int u = C::GU * (warp + (k / C::GU) * NW) + (k % C::GU);  // unit within chunk
         int phys = -2;                                                    // absent
         if (u < nunits) {
-            phys = a.block_tables[bt_row + p_begin + u];
-            if (phys < 0 || phys >= a.num_pages) {
-                bad |= kStatusBadPage;
+            const long long bi = bt_row + p_begin + u;
+            phys = a.block_tables[bi];
+            const uint32_t eb = entry_bits(a, phys, h, Hkv, bi);
+            if (eb) {
+                bad |= eb;
                 phys = -1;
             }
         }

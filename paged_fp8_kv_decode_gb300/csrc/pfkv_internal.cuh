@@ -66,6 +66,7 @@ struct DecodeArgs {
     // workspace
     uint32_t *hflags;   // [B][Hkv][htiles] tag/bounds bits from the validation kernel
     int htiles;
+    int fuse_tags;      // compare tags where the split kernels load page ids
     uint32_t *status;   // [B][Hkv][nchunks]
     float *lse;         // [B][Hq][nchunks]  log2-sum-exp of the chunk
     float *o;           // [B][Hq][nchunks][D] chunk output (normalised)
@@ -107,6 +108,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Status bits of table entry bt_index naming page `id` of kv head h: BAD_PAGE
+// for an id outside the pool, TAG_MISMATCH (fused check only) for a pool tag
+// that differs from the expected one.  Zero: the unit may be read.
+__device__ __forceinline__ uint32_t entry_bits(const DecodeArgs &a, int id, int h, int Hkv,
+                                               long long bt_index) {
+    if (id < 0 || id >= a.num_pages) return PFKV_FLAG_BAD_PAGE;
+    if (a.fuse_tags && a.page_tags[(long long)id * Hkv + h] != a.expected_tags[bt_index])
+        return PFKV_FLAG_TAG_MISMATCH;
+    return 0u;
 }
 
 // Whether the validation kernel flagged request b (any kv head, any tile).

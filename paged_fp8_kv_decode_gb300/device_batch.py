@@ -24,9 +24,10 @@ def _i32(a: np.ndarray, device) -> torch.Tensor:
 class DeviceBatch:
     def __init__(self, batch: W.Batch, device="cuda", keep_rows: bool = False,
                  tags: Optional[bool] = None, fill_chunk_tokens: int = 8192, rows=None,
-                 q: Optional[torch.Tensor] = None):
+                 q: Optional[torch.Tensor] = None, fused_tags: bool = False):
         spec = batch.spec
         self.spec, self.batch, self.device = spec, batch, device
+        self.fused_tags = fused_tags  # tag check inside the attention kernel
         use_tags = spec.tags if tags is None else tags
         NP, H, D = spec.num_pages, spec.Hkv, spec.D
         if spec.kv_dtype == "bf16":
@@ -106,10 +107,10 @@ class DeviceBatch:
                              flags=self.append_flags, stream=stream)
 
     def attend(self, stream=None, split_tokens: Optional[int] = None):
-        B.pfkv_paged_decode_attn(self.cache, self.pages, self.q, self.spec.sm_scale,
-                                 self.split_tokens if split_tokens is None else split_tokens,
-                                 self.max_seq_len, self.workspace, self.out, self.flags,
-                                 stream=stream)
+        fn = B.pfkv_paged_decode_attn_fused_tags if self.fused_tags else B.pfkv_paged_decode_attn
+        fn(self.cache, self.pages, self.q, self.spec.sm_scale,
+           self.split_tokens if split_tokens is None else split_tokens,
+           self.max_seq_len, self.workspace, self.out, self.flags, stream=stream)
 
     def step(self, stream=None):
         """One decode step: append the new token (if any), then attention."""

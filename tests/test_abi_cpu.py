@@ -31,6 +31,7 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert names == sorted(["pfkv_abi_version", "pfkv_decode_workspace_size", "pfkv_e4m3_decode",
                             "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_paged_decode_attn",
+                            "pfkv_paged_decode_attn_fused_tags",
                             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
                             "pfkv_status_string"])
 
@@ -114,10 +115,25 @@ def test_host_rejects_bad_call_arguments(B):
 def test_stage_mask_is_checked(B):
     c, p = _structs(B)
     L = B.lib()
-    for mask in (0, 8, 0x17):
+    # no stage bit (the fused-tag option alone counts as none), or an unknown bit
+    for mask in (0, 8, 0x17, 0x18):
         assert L.pfkv_paged_decode_attn_stages(ctypes.byref(c), ctypes.byref(p), 0xA0000, 4, 0.125,
                                                0, 64, 0xB0000, 1 << 30, 0xC0000, None, mask,
                                                None) == 1
+
+
+def test_fused_tag_entry_checks_arguments_like_the_plain_one(B):
+    c, p = _structs(B)
+    L = B.lib()
+    def fused(Hq=4, split=0, max_len=64, ws=0xB0000):
+        return L.pfkv_paged_decode_attn_fused_tags(ctypes.byref(c), ctypes.byref(p), 0xA0000, Hq,
+                                                   0.125, split, max_len, ws, 1 << 30, 0xC0000,
+                                                   None, None)
+    assert fused(Hq=6) == 2
+    assert fused(split=24) == 1
+    assert fused(max_len=-1) == 1
+    assert fused(ws=None) == 4
+    assert fused(ws=0xB0010) == 3
 
 
 def test_empty_batch_is_a_no_op(B):

@@ -103,6 +103,11 @@ def _flags_ref(db):
 def _run(spec, samples, B, **kw):
     from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
     db = DeviceBatch(W.make_batch(spec), keep_rows=True, **kw)
+    return _check_run(db, samples)
+
+
+def _check_run(db, samples):
+    spec = db.spec
     db.step()
     torch.cuda.synchronize()
     flags = db.flags.cpu().numpy()[:spec.B]
@@ -141,6 +146,19 @@ def test_evict_full_stale_tags_and_per_head_lengths(B):
         samples.append((b, int(np.argmax(lens[b]))))
     for b, h in samples:
         _check_head(db, b, h, bool(want[b]))
+
+
+def test_evict_full_stale_tags_fused_check(B):
+    """The tag check inside the attention kernel: same flags, sampled heads
+    against the oracle."""
+    spec = W.spec_evict("full")
+    db, want = _run(spec, [], B, fused_tags=True)
+    lens = db.batch.lens_bh()
+    clean = [b for b in range(spec.B) if not want[b]]
+    flagged = [b for b in range(spec.B) if want[b]]
+    for b in clean[:2] + flagged[:1]:
+        _check_head(db, b, int(np.argmin(lens[b])), bool(want[b]))
+        _check_head(db, b, int(np.argmax(lens[b])), bool(want[b]))
 
 
 def test_evict_full_without_tags(B):

@@ -35,11 +35,11 @@ def _db(batch, **kw):
     return DeviceBatch(batch, keep_rows=True, **kw)
 
 
-def run_and_compare(spec, tags=None, rows=None, q=None, label=""):
+def run_and_compare(spec, tags=None, rows=None, q=None, label="", fused_tags=False):
     """Fill, append, attend on the GPU and on the oracle; compare everything."""
     batch = W.make_batch(spec)
     use_tags = spec.tags if tags is None else tags
-    db = _db(batch, tags=use_tags, rows=rows, q=q)
+    db = _db(batch, tags=use_tags, rows=rows, q=q, fused_tags=fused_tags)
     ref = oracle_reference(spec, batch, db.k_rows.cpu(), db.v_rows.cpu(), db.q.cpu(),
                            None if db.k_new is None else db.k_new.cpu(),
                            None if db.v_new is None else db.v_new.cpu(), tags=use_tags)
