@@ -72,6 +72,9 @@ def parse_args(argv=None):
                     choices=["llama8b", "tiny", "long", "sweep", "evict"],
                     help="llama8b (default): the Llama-shaped layer; the others are the "
                          "tiny, long-context, 80 GB-pool sweep and eviction + tags workloads")
+    ap.add_argument("--graph-layers", type=int, default=0,
+                    help="time one decode step of this many Llama-shaped layers, each with its "
+                         "own pool, captured as one CUDA graph (pfkv_step_graph_*)")
     ap.add_argument("--batch", type=int, default=32, help="sweep: batch size")
     ap.add_argument("--kv-dtype", default="fp8", choices=["fp8", "bf16"], help="sweep: pool dtype")
     return ap.parse_args(argv)
@@ -768,10 +771,114 @@ def run_e2e_flushed(args, p, B, stream, step_bytes, world, dev, flush):
             "steps": K, "ms_per_step": round(total / K * 1e3, 4)}
 
 
+def run_graph(args):
+    """One JSON line: decode steps of a stack of --graph-layers layers (the
+    Llama-shaped FP8 layer, each with its own pool and query, shared tables)
+    replayed from one CUDA graph per step."""
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import dataclasses
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_fp8_kv_decode_gb300 import binding as B
+    from paged_fp8_kv_decode_gb300 import workloads as W
+    from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
+    n = args.graph_layers
+    spec = W.spec_llama8b("full", seed=rank_seed(W.BASE_SEED + 2, rank, 0))
+    spec.split_tokens = args.split
+    if args.no_tags:
+        spec.tags = False
+    batch = W.make_batch(spec)
+    T = int(batch.fill_lens.max())
+    dbs = []
+    for l in range(n):
+        sl = dataclasses.replace(spec, seed=spec.seed + 7 * (l + 1))
+        rows = (W.draw_kv_rows(sl, T, "k", device=dev), W.draw_kv_rows(sl, T, "v", device=dev))
+        db = DeviceBatch(batch, device=dev, rows=rows, q=W.draw_q(sl, device=dev))
+        del rows
+        dbs.append(db)
+    torch.cuda.synchronize()
+    d0 = dbs[0]
+    layers = [B.Layer(cache=d.cache, q=d.q, out=d.out, k_new=d.k_new, v_new=d.v_new, flags=d.flags)
+              for d in dbs]
+    graph = B.pfkv_step_graph_create(layers, d0.pages, d0.positions, None, 1, d0.append_flags,
+                                     spec.Hq, spec.sm_scale, spec.split_tokens, d0.max_seq_len,
+                                     d0.workspace, B.PFKV_STAGE_FUSED_TAGS if args.fused_tags else 0)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        graph.launch(stream)
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    sampler = None
+    if rank == 0 and not args.no_clocks:
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        evs[i][0].record(stream)
+        graph.launch(stream)
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    total = reduce_max(t0.elapsed_time(t1) / 1e3, world, dev)
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    med, p10, p90 = _median_times(ms)
+    if any(int(d.flags[:spec.B].sum()) for d in dbs) or int(d0.append_flags[:spec.B].sum()):
+        raise RuntimeError("benchmark workload flagged a request")
+    attn = sum(d.algorithmic_bytes() for d in dbs)
+    append = n * (spec.B * spec.Hkv * spec.D * (2 * 2 + 2) + spec.B * spec.Hkv * 8)
+    step_bytes = attn + append
+    graph.close()
+    if rank == 0:
+        line = {
+            "metric": f"decode tokens/s ({n} Llama-3.1-8B-shaped FP8 attention layers per step, "
+                      f"one CUDA graph per step)",
+            "value": round(world * spec.B * K / total, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": max(3, args.warmup),
+            "ms_per_step": round(total / K * 1e3, 4), "median_ms": round(med, 4),
+            "p10_ms": round(p10, 4), "p90_ms": round(p90, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 KV, fp32 accumulate, bf16 q/out", "data": "synthetic",
+            "config": {"workload": "llama8b-fp8-decode-stack", "layers": n, "batch": spec.B,
+                       "num_q_heads": spec.Hq, "num_kv_heads": spec.Hkv, "head_dim": spec.D,
+                       "page_size": 16, "num_pages_per_layer": spec.num_pages,
+                       "tags": spec.tags, "tag_check": ("none" if not spec.tags else
+                                                        "fused into attention" if args.fused_tags
+                                                        else "separate pass"),
+                       "l2": "inputs larger than L2: %d layers, %.0f MB live KV each"
+                             % (n, dbs[0].kv_bytes() / 1e6),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "kv_gbs": round(world * step_bytes * K / total / 1e9, 2),
+            "per_layer_us": round(total / K / n * 1e6, 3),
+            "gpu_launches": K * n * (3 if (args.no_tags or args.fused_tags) else 4),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.graph_layers > 0:
+        run_graph(args)
     elif args.workload != "llama8b":
         run_workload(args)
     else:

@@ -20,8 +20,10 @@
  *
  * Conventions for every call:
  *  - Memory: every pointer argument not marked "host" is DEVICE memory owned
- *    by the caller.  The library never allocates or frees memory and keeps no
- *    state between calls; calls on different streams are independent.
+ *    by the caller.  The library never allocates device memory for data and
+ *    keeps no state between calls, except the step-graph objects that a caller
+ *    creates and destroys explicitly (CUDA graphs, a driver resource); calls on
+ *    different streams are independent.
  *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
  *    work is enqueued asynchronously on it; no call synchronises the host.
  *  - Alignment: k_pages, v_pages, q, out, k_new and v_new 16-byte aligned;
@@ -280,6 +282,61 @@ pfkv_status pfkv_paged_decode_attn_noalloc(const pfkv_cache *cache, const pfkv_p
                                            const void *q, int32_t num_q_heads, float sm_scale,
                                            int32_t split_tokens, int32_t max_seq_len, void *out,
                                            uint8_t *flags, void *stream);
+
+/*
+ * Step graphs: one decode step of a stack of attention layers captured once
+ * as a CUDA graph and replayed with a single launch.  The Infire page ("How
+ * we built the most efficient inference engine for Cloudflare's network",
+ * section "Rust-precise CUDA kernels", 2nd paragraph) keeps one graph per
+ * batch size, built on first use and cached, because one graph launch costs
+ * less than the kernel launches it replaces; a caller does the same with one
+ * pfkv_step_graph per batch size.
+ *
+ * A graph records, for every layer in order, pfkv_kv_append (when the layer
+ * has new tokens) followed by the attention call (with the separate or the
+ * fused tag check), exactly as the direct calls would enqueue them, with the
+ * pointers and sizes given at creation.  Replaying it reads the CURRENT
+ * contents of every buffer (q, new rows, positions, lengths, tables, tags,
+ * pools), so a caller rewrites those buffers in place between steps.  The
+ * launch configuration is fixed at creation: lengths must stay within
+ * max_seq_len (longer ones are flagged PFKV_FLAG_BAD_LENGTH), and a new batch
+ * size or pool needs a new graph.  All layers share the tables, lengths,
+ * positions and workspace; the workspace must not be used concurrently.
+ */
+typedef struct {
+    pfkv_cache cache;            /* this layer's pool                               */
+    const void *q;               /* bf16 [batch][num_q_heads][head_dim]             */
+    const void *k_new, *v_new;   /* bf16 [batch][num_kv_heads][num_new_tokens][head_dim];
+                                    both NULL: this layer appends nothing          */
+    void *out;                   /* bf16 [batch][num_q_heads][head_dim]             */
+    uint8_t *flags;              /* attention flags of this layer, or NULL          */
+} pfkv_layer;
+
+typedef struct pfkv_step_graph pfkv_step_graph;  /* opaque */
+
+/*
+ * pfkv_step_graph_create -- capture the step for `layers` (host array of
+ * num_layers >= 1 entries) into *graph (host).  Arguments are those of
+ * pfkv_kv_append (positions, new_lens, num_new_tokens, append_flags) and of
+ * pfkv_paged_decode_attn (the rest), shared by every layer; `options` is 0 or
+ * PFKV_STAGE_FUSED_TAGS.  Every argument check of the direct calls is made
+ * here, for every layer, and its status returned (nothing is captured then).
+ * The capture uses a private stream; nothing runs on the device.
+ */
+pfkv_status pfkv_step_graph_create(const pfkv_layer *layers, int32_t num_layers,
+                                   const pfkv_pages *pages, const int32_t *positions,
+                                   const int32_t *new_lens, int32_t num_new_tokens,
+                                   uint8_t *append_flags, int32_t num_q_heads, float sm_scale,
+                                   int32_t split_tokens, int32_t max_seq_len, void *workspace,
+                                   size_t workspace_bytes, uint32_t options,
+                                   pfkv_step_graph **graph);
+
+/* pfkv_step_graph_launch -- enqueue one step (all layers) on `stream`. */
+pfkv_status pfkv_step_graph_launch(pfkv_step_graph *graph, void *stream);
+
+/* pfkv_step_graph_destroy -- free the graph (NULL is a no-op).  The caller
+ * makes sure no launch of it is still running. */
+pfkv_status pfkv_step_graph_destroy(pfkv_step_graph *graph);
 
 /*
  * pfkv_e4m3_encode -- out[i] = e4m3 code of x[i] (fp32), round to nearest

@@ -43,7 +43,9 @@ PFKV_STAGE_FUSED_TAGS = 0x8
 # every symbol include/pfkv.h declares
 EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",
             "pfkv_paged_decode_attn_stages", "pfkv_paged_decode_attn_fused_tags",
-            "pfkv_paged_decode_attn_noalloc", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string", "pfkv_abi_version")
+            "pfkv_paged_decode_attn_noalloc", "pfkv_step_graph_create", "pfkv_step_graph_launch",
+            "pfkv_step_graph_destroy", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string",
+            "pfkv_abi_version")
 
 
 class PfkvError(RuntimeError):
@@ -66,6 +68,11 @@ class _CPages(ctypes.Structure):
                 ("bt_stride_h", ctypes.c_int64), ("seq_lens", ctypes.c_void_p),
                 ("len_stride_b", ctypes.c_int64), ("len_stride_h", ctypes.c_int64),
                 ("expected_tags", ctypes.c_void_p)]
+
+
+class _CLayer(ctypes.Structure):
+    _fields_ = [("cache", _CCache), ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p),
+                ("v_new", ctypes.c_void_p), ("out", ctypes.c_void_p), ("flags", ctypes.c_void_p)]
 
 
 _lib = None
@@ -103,6 +110,15 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.POINTER(_CPages), P, I32,
                                                      ctypes.c_float, I32, I32, P, P, P]
         L.pfkv_paged_decode_attn_noalloc.restype = ctypes.c_int
+        L.pfkv_step_graph_create.argtypes = [ctypes.POINTER(_CLayer), I32, ctypes.POINTER(_CPages),
+                                             P, P, I32, P, I32, ctypes.c_float, I32, I32, P,
+                                             ctypes.c_size_t, ctypes.c_uint32,
+                                             ctypes.POINTER(ctypes.c_void_p)]
+        L.pfkv_step_graph_create.restype = ctypes.c_int
+        L.pfkv_step_graph_launch.argtypes = [P, P]
+        L.pfkv_step_graph_launch.restype = ctypes.c_int
+        L.pfkv_step_graph_destroy.argtypes = [P]
+        L.pfkv_step_graph_destroy.restype = ctypes.c_int
         L.pfkv_e4m3_encode.argtypes = [P, I64, P, P]
         L.pfkv_e4m3_encode.restype = ctypes.c_int
         L.pfkv_e4m3_decode.argtypes = [P, I64, P, P]
@@ -277,6 +293,71 @@ def pfkv_paged_decode_attn_noalloc(cache: Cache, pages: Pages, q: torch.Tensor, 
         ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
         int(max_seq_len), _ptr(out), _ptr(flags), _stream(stream)),
         "pfkv_paged_decode_attn_noalloc")
+
+
+@dataclasses.dataclass
+class Layer:
+    """One attention layer of a step graph: its pool and its q/new rows/out/flags
+    (k_new and v_new both None: no append in this layer)."""
+    cache: Cache
+    q: torch.Tensor
+    out: torch.Tensor
+    k_new: Optional[torch.Tensor] = None
+    v_new: Optional[torch.Tensor] = None
+    flags: Optional[torch.Tensor] = None
+
+    def c_struct(self) -> _CLayer:
+        return _CLayer(self.cache.c_struct(), _ptr(self.q), _ptr(self.k_new), _ptr(self.v_new),
+                       _ptr(self.out), _ptr(self.flags))
+
+
+class StepGraph:
+    """Owner of a pfkv_step_graph handle (destroyed with the object or close())."""
+
+    def __init__(self, handle: int, keep):
+        self.handle, self._keep = handle, keep
+
+    def launch(self, stream=None) -> None:
+        pfkv_step_graph_launch(self, stream)
+
+    def close(self) -> None:
+        if self.handle:
+            h, self.handle = self.handle, 0
+            _check(lib().pfkv_step_graph_destroy(h), "pfkv_step_graph_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def pfkv_step_graph_create(layers, pages: Pages, positions: Optional[torch.Tensor],
+                           new_lens: Optional[torch.Tensor], num_new_tokens: int,
+                           append_flags: Optional[torch.Tensor], num_q_heads: int,
+                           sm_scale: float, split_tokens: int, max_seq_len: int,
+                           workspace: torch.Tensor, options: int = 0) -> StepGraph:
+    """Capture one decode step of ``layers`` (a list of Layer) as a CUDA graph."""
+    arr = (_CLayer * len(layers))(*[l.c_struct() for l in layers])
+    p = pages.c_struct()
+    h = ctypes.c_void_p(0)
+    _check(lib().pfkv_step_graph_create(arr, len(layers), ctypes.byref(p), _ptr(positions),
+                                        _ptr(new_lens), int(num_new_tokens), _ptr(append_flags),
+                                        int(num_q_heads), float(sm_scale), int(split_tokens),
+                                        int(max_seq_len), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        int(options), ctypes.byref(h)), "pfkv_step_graph_create")
+    # the captured pointers stay valid only while these tensors live
+    return StepGraph(int(h.value), (layers, pages, positions, new_lens, append_flags, workspace))
+
+
+def pfkv_step_graph_launch(graph: StepGraph, stream=None) -> None:
+    _check(lib().pfkv_step_graph_launch(graph.handle or None, _stream(stream)),
+           "pfkv_step_graph_launch")
+
+
+def pfkv_step_graph_destroy(graph: StepGraph) -> None:
+    graph.close()
 
 
 def pfkv_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:

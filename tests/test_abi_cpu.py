@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
                             "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_paged_decode_attn",
                             "pfkv_paged_decode_attn_fused_tags",
                             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
-                            "pfkv_status_string"])
+                            "pfkv_status_string", "pfkv_step_graph_create",
+                            "pfkv_step_graph_destroy", "pfkv_step_graph_launch"])
 
 
 def test_library_exports_every_declared_symbol(B):
@@ -134,6 +135,27 @@ def test_fused_tag_entry_checks_arguments_like_the_plain_one(B):
     assert fused(max_len=-1) == 1
     assert fused(ws=None) == 4
     assert fused(ws=0xB0010) == 3
+
+
+def test_step_graph_argument_checks(B):
+    """Checks that need no device: a missing handle pointer, no layers, an
+    unknown option, a layer with only one of k_new / v_new."""
+    c, p = _structs(B)
+    L = B.lib()
+    lay = (B._CLayer * 1)(B._CLayer(c, 0xA0000, 0, 0, 0xC0000, 0))
+    h = ctypes.c_void_p(0)
+    def create(layers=lay, n=1, opts=0, out=ctypes.byref(h)):
+        return L.pfkv_step_graph_create(layers, n, ctypes.byref(p), 0xD0000, None, 1, None, 4,
+                                        0.125, 0, 64, 0xB0000, 1 << 30, opts, out)
+    assert create(out=None) == 1
+    assert create(n=0) == 1
+    assert create(layers=None) == 1
+    assert create(opts=0x4) == 1
+    half = (B._CLayer * 1)(B._CLayer(c, 0xA0000, 0xE0000, 0, 0xC0000, 0))
+    assert create(layers=half) == 1
+    assert h.value is None
+    assert L.pfkv_step_graph_destroy(None) == 0
+    assert L.pfkv_step_graph_launch(None, None) == 1
 
 
 def test_empty_batch_is_a_no_op(B):
