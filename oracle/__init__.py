@@ -64,6 +64,10 @@ def lib():
         L.oracle_paged_decode.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Pages),
                                           ctypes.c_void_p, ctypes.c_int32, ctypes.c_double,
                                           ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_attention_mass.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Pages),
+                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_double,
+                                            ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                            ctypes.c_int64]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -189,6 +193,24 @@ def paged_decode(cache: dict, pages: dict, q, num_q_heads: int, sm_scale: float,
     lib().oracle_paged_decode(ctypes.byref(c), ctypes.byref(p), _ptr(q), int(num_q_heads),
                               float(sm_scale), int(max_seq_len), _ptr(out), _ptr(flags))
     return out, flags[:B]
+
+
+def attention_mass(cache: dict, pages: dict, q, num_q_heads: int, sm_scale: float,
+                   max_seq_len: int, mass=None, mass_strides=None):
+    """fp64 attention mass (see oracle.c): adds, for each (b, h, j), the sum
+    over the group's query heads of token j's softmax weight to ``mass``
+    (float64, C-contiguous; default zeros [B][Hkv][max_seq_len]).  Returns mass."""
+    c = _cache(**cache)
+    p = _pages(**pages)
+    _need(q, np.uint16, "q")
+    B, H = int(pages["batch"]), int(cache["num_kv_heads"])
+    if mass is None:
+        mass = np.zeros((B, H, max(int(max_seq_len), 1)), dtype=np.float64)
+    _need(mass, np.float64, "mass")
+    sb, sh = mass_strides if mass_strides is not None else (mass.strides[0] // 8, mass.strides[1] // 8)
+    lib().oracle_attention_mass(ctypes.byref(c), ctypes.byref(p), _ptr(q), int(num_q_heads),
+                                float(sm_scale), int(max_seq_len), _ptr(mass), int(sb), int(sh))
+    return mass
 
 
 def num_threads() -> int:

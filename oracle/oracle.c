@@ -22,6 +22,10 @@
  *  [I]  "How we built the most efficient inference engine for Cloudflare's
  *       network", section "Batching to feed the Tensor Cores": the KV cache is
  *       split into pages allocated on demand.
+ *  [M]  "Workers AI targets the inference bottleneck", section "KV cache
+ *       compression goes open source", 3rd paragraph: eviction tracks the
+ *       attention each KV entry has received over past steps and evicts the
+ *       entries with the lowest total, like a least-frequently-used cache.
  *  [E]  The OCP 8-bit floating point specification (E4M3 "FN" variant), the
  *       format that [Q] names: 1 sign, 4 exponent (bias 7), 3 mantissa bits,
  *       no infinities, S.1111.111 is NaN, largest finite 448.
@@ -38,6 +42,11 @@
  *  R4 GQA grouping is consecutive: query head hq reads kv head hq / G.
  *  R5 flagged requests and zero-length heads produce all-zero output.
  *  R6 only live table entries p < ceil(len/16) are read or checked.
+ *  R7 attention mass [M]: the mass of token j of kv head h at one decode step
+ *     is the sum, over the G query heads that read kv head h, of the softmax
+ *     weight of token j (weights normalised over the head's n tokens); a call
+ *     adds it to a running total kept by the caller.  Flagged requests and
+ *     zero-length heads add nothing.
  *
  * Precision: attention is computed in fp64 (plain two-pass softmax, natural
  * exp, sequential token order); quantisation decisions are taken in fp32, the
@@ -404,6 +413,56 @@ void oracle_paged_decode(const orc_cache *c, const orc_pages *pg, const uint16_t
         for (int d = 0; d < D; ++d)
             o[d] /= l;
         free(qv);
+        free(s);
+    }
+    free(flags);
+}
+
+/*
+ * Attention mass [M], reading R7: for every (b, h) of an unflagged request with
+ * n > 0 tokens, and every token j < n,
+ *   mass[b*mass_sb + h*mass_sh + j] += sum over g < G of
+ *       exp(s_gj) / sum_i exp(s_gi),   s_gj = sm_scale * q[b, h*G + g] . k_j
+ * in fp64, each query head's softmax taken on its own (max subtracted first).
+ * One (b, h) per iteration, so no two threads add to the same entry.
+ */
+void oracle_attention_mass(const orc_cache *c, const orc_pages *pg, const uint16_t *q,
+                           int32_t num_q_heads, double sm_scale, int32_t max_seq_len,
+                           double *mass, int64_t mass_sb, int64_t mass_sh)
+{
+    const int H = c->num_kv_heads, D = c->head_dim, Hq = num_q_heads;
+    const int G = Hq / H;
+    const int B = pg->batch;
+    uint8_t *flags = (uint8_t *)malloc(B > 0 ? (size_t)B : 1);
+    oracle_validate(c, pg, max_seq_len, flags);
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        int b = (int)(bh / H), h = (int)(bh % H);
+        int32_t n = pg->seq_lens[(int64_t)b * pg->len_stride_b + (int64_t)h * pg->len_stride_h];
+        if (flags[b] != 0 || n <= 0)
+            continue;
+        const int32_t *row = pg->block_tables + (int64_t)b * pg->bt_stride_b + (int64_t)h * pg->bt_stride_h;
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
+        double *mrow = mass + (int64_t)b * mass_sb + (int64_t)h * mass_sh;
+        for (int g = 0; g < G; ++g) {
+            const uint16_t *qg = q + ((int64_t)b * Hq + (int64_t)h * G + g) * D;
+            double m = -INFINITY, l = 0.0;
+            for (int32_t j = 0; j < n; ++j) {
+                int64_t u = unit_index(c, row[j / ORC_PAGE], h);
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d)
+                    acc += (double)bf16_bits_to_float(qg[d]) *
+                           kv_value(c, c->k_pages, c->k_scale, u, j % ORC_PAGE, d);
+                s[j] = sm_scale * acc;
+                if (s[j] > m)
+                    m = s[j];
+            }
+            for (int32_t j = 0; j < n; ++j)
+                l += exp(s[j] - m);
+            for (int32_t j = 0; j < n; ++j)
+                mrow[j] += exp(s[j] - m) / l;
+        }
         free(s);
     }
     free(flags);
