@@ -198,6 +198,31 @@ class PreparedStep:
             raise RuntimeError(f"pfkv_paged_decode_attn_stages: status {st}")
 
 
+class PreparedMassStep(PreparedStep):
+    """A step whose attention also adds every live token's attention mass to a
+    running total (pfkv_paged_decode_attn_mass); stage() runs the whole call."""
+
+    def __init__(self, db, B, stream_handle, cache=None):
+        import torch
+        super().__init__(db, B, stream_handle, cache=cache)
+        L = db.max_seq_len
+        self.ws = torch.empty(B.pfkv_decode_mass_workspace_size(cache or db.cache, db.pages,
+                                                                db.spec.Hq, db.split_tokens, L),
+                              dtype=torch.uint8, device=db.q.device)
+        self.mass = torch.zeros((db.spec.B, db.spec.Hkv, L), dtype=torch.float32,
+                                device=db.q.device)
+        self.margs = (ctypes.byref(self.c), ctypes.byref(self.p), db.q.data_ptr(), db.spec.Hq,
+                      ctypes.c_float(db.spec.sm_scale), db.split_tokens, L, self.ws.data_ptr(),
+                      self.ws.numel(), db.out.data_ptr(), db.flags.data_ptr(),
+                      self.mass.data_ptr(), self.mass.stride(0), self.mass.stride(1), 0,
+                      stream_handle)
+
+    def stage(self, mask):
+        st = self.L.pfkv_paged_decode_attn_mass(*self.margs)
+        if st:
+            raise RuntimeError(f"pfkv_paged_decode_attn_mass: status {st}")
+
+
 def profiled_traffic(bytes_per_launch: float):
     """DRAM bytes per launch of the split kernel from the committed ncu summary,
     scaled to this run's algorithmic bytes; None if the kernel source changed
@@ -619,6 +644,8 @@ def run_workload(args):
         variants.append(("fused_tags_all_match",
                          PreparedStep(db, B, sh, cache=c_match, fused_tags=True), True))
         variants.append(("fused_tags", PreparedStep(db, B, sh, fused_tags=True), True))
+        variants.append(("tags_all_match_attn_mass", PreparedMassStep(db, B, sh, cache=c_match),
+                         True))
         variants.append(("no_tags", PreparedStep(db, B, sh, cache=db.cache_untracked,
                                                  pages=p_off), False))
     flush = L2Flush(dev)
@@ -718,7 +745,8 @@ def run_workload(args):
                      "bytes_per_launch": int(split_bytes), "timed_launches": len(split_ms)},
         "variants": results if len(results) > 1 else None,
         "gpu_launches": K * (len(variants) * (3 if spec.append else 2) + 3) + sum(
-            K for _, p, t in variants if t and not p.opt),
+            K for _, p, t in variants if t and not p.opt) + sum(
+            K for _, p, _ in variants if isinstance(p, PreparedMassStep)),
         "clocks": clocks,
     }
     if "tags_all_match" in results and "no_tags" in results:
@@ -727,6 +755,9 @@ def run_workload(args):
         line["tag_overhead_pct"] = round(100 * (a - b) / b, 2)
         a = results["fused_tags_all_match"]["ms_per_step"]
         line["fused_tag_overhead_pct"] = round(100 * (a - b) / b, 2)
+        a = results["tags_all_match_attn_mass"]["ms_per_step"]
+        c = results["tags_all_match"]["ms_per_step"]
+        line["attn_mass_overhead_pct"] = round(100 * (a - c) / c, 2)
     line["e2e"] = run_e2e_flushed(args, p0, B, stream, r0["bytes_per_step"], world, dev, flush)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_spec(spec)

@@ -284,6 +284,37 @@ pfkv_status pfkv_paged_decode_attn_noalloc(const pfkv_cache *cache, const pfkv_p
                                            uint8_t *flags, void *stream);
 
 /*
+ * pfkv_paged_decode_attn_mass -- pfkv_paged_decode_attn that also adds each
+ * live token's attention mass to a running total kept by the caller.
+ *
+ * Eviction ("Workers AI targets the inference bottleneck", section "KV cache
+ * compression goes open source", 3rd paragraph) tracks how much attention
+ * every KV entry has received over past steps and evicts the entries with
+ * the lowest total.  For every (b, h) of a request that is not flagged, and
+ * every token j < n = seq_lens(b, h):
+ *   attn_mass[b*mass_stride_b + h*mass_stride_h + j] +=
+ *       sum over the G query heads hq of kv head h of softmax_j(sm_scale q_hq . k_j)
+ * (the weights the output uses, normalised over the head's n tokens, fp32).
+ * Flagged requests and zero-length heads add nothing.  Rows of different
+ * (b, h) must not overlap.
+ *
+ *   attn_mass     : float, 4-byte aligned; strides in elements (>= 0)
+ *   options       : 0 or PFKV_STAGE_FUSED_TAGS (tag check inside attention)
+ *   workspace     : >= pfkv_decode_mass_workspace_size(...) bytes, which adds
+ *                   batch x num_q_heads x max_seq_len floats of final scores
+ * out and flags are those of pfkv_paged_decode_attn.
+ */
+pfkv_status pfkv_decode_mass_workspace_size(const pfkv_cache *cache, const pfkv_pages *pages,
+                                            int32_t num_q_heads, int32_t split_tokens,
+                                            int32_t max_seq_len, size_t *bytes);
+pfkv_status pfkv_paged_decode_attn_mass(const pfkv_cache *cache, const pfkv_pages *pages,
+                                        const void *q, int32_t num_q_heads, float sm_scale,
+                                        int32_t split_tokens, int32_t max_seq_len,
+                                        void *workspace, size_t workspace_bytes, void *out,
+                                        uint8_t *flags, float *attn_mass, int64_t mass_stride_b,
+                                        int64_t mass_stride_h, uint32_t options, void *stream);
+
+/*
  * Step graphs: one decode step of a stack of attention layers captured once
  * as a CUDA graph and replayed with a single launch.  The Infire page ("How
  * we built the most efficient inference engine for Cloudflare's network",

@@ -43,7 +43,8 @@ PFKV_STAGE_FUSED_TAGS = 0x8
 # every symbol include/pfkv.h declares
 EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",
             "pfkv_paged_decode_attn_stages", "pfkv_paged_decode_attn_fused_tags",
-            "pfkv_paged_decode_attn_noalloc", "pfkv_step_graph_create", "pfkv_step_graph_launch",
+            "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_mass",
+            "pfkv_decode_mass_workspace_size", "pfkv_step_graph_create", "pfkv_step_graph_launch",
             "pfkv_step_graph_destroy", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string",
             "pfkv_abi_version")
 
@@ -110,6 +111,13 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.POINTER(_CPages), P, I32,
                                                      ctypes.c_float, I32, I32, P, P, P]
         L.pfkv_paged_decode_attn_noalloc.restype = ctypes.c_int
+        L.pfkv_decode_mass_workspace_size.argtypes = L.pfkv_decode_workspace_size.argtypes
+        L.pfkv_decode_mass_workspace_size.restype = ctypes.c_int
+        L.pfkv_paged_decode_attn_mass.argtypes = [ctypes.POINTER(_CCache), ctypes.POINTER(_CPages),
+                                                  P, I32, ctypes.c_float, I32, I32, P,
+                                                  ctypes.c_size_t, P, P, P, I64, I64,
+                                                  ctypes.c_uint32, P]
+        L.pfkv_paged_decode_attn_mass.restype = ctypes.c_int
         L.pfkv_step_graph_create.argtypes = [ctypes.POINTER(_CLayer), I32, ctypes.POINTER(_CPages),
                                              P, P, I32, P, I32, ctypes.c_float, I32, I32, P,
                                              ctypes.c_size_t, ctypes.c_uint32,
@@ -276,6 +284,35 @@ def pfkv_paged_decode_attn_fused_tags(cache: Cache, pages: Pages, q: torch.Tenso
         ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
         int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), _ptr(flags), _stream(stream)), "pfkv_paged_decode_attn_fused_tags")
+
+
+def pfkv_decode_mass_workspace_size(cache: Cache, pages: Pages, num_q_heads: int,
+                                    split_tokens: int, max_seq_len: int) -> int:
+    c, p = cache.c_struct(), pages.c_struct()
+    out = ctypes.c_size_t(0)
+    _check(lib().pfkv_decode_mass_workspace_size(ctypes.byref(c), ctypes.byref(p),
+                                                 int(num_q_heads), int(split_tokens),
+                                                 int(max_seq_len), ctypes.byref(out)),
+           "pfkv_decode_mass_workspace_size")
+    return int(out.value)
+
+
+def pfkv_paged_decode_attn_mass(cache: Cache, pages: Pages, q: torch.Tensor, sm_scale: float,
+                                split_tokens: int, max_seq_len: int, workspace: torch.Tensor,
+                                out: torch.Tensor, flags: Optional[torch.Tensor],
+                                attn_mass: torch.Tensor, options: int = 0, stream=None) -> None:
+    """pfkv_paged_decode_attn plus attn_mass[b][h][j] += the token's summed softmax
+    weight over the group's query heads (attn_mass: float32 CUDA tensor, 3-D
+    [B][Hkv][>= max_seq_len] with any strides)."""
+    c, p = cache.c_struct(), pages.c_struct()
+    Hq = int(q.shape[1])
+    if attn_mass.dtype != torch.float32 or attn_mass.dim() != 3 or attn_mass.stride(2) != 1:
+        raise ValueError("attn_mass: float32 [B][Hkv][L] with unit stride along tokens")
+    _check(lib().pfkv_paged_decode_attn_mass(
+        ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
+        int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(flags), _ptr(attn_mass), int(attn_mass.stride(0)),
+        int(attn_mass.stride(1)), int(options), _stream(stream)), "pfkv_paged_decode_attn_mass")
 
 
 # bytes of the library's own workspace used by pfkv_paged_decode_attn_noalloc

@@ -100,7 +100,8 @@ pfkv_status check_decode_args(const pfkv_cache *c, int32_t num_q_heads, int32_t 
 }
 
 pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_heads,
-                      int32_t split_tokens, int32_t max_seq_len, int num_sms, DecodePlan *plan) {
+                      int32_t split_tokens, int32_t max_seq_len, int num_sms, DecodePlan *plan,
+                      bool mass = false) {
     const pfkv_status st = check_decode_args(c, num_q_heads, split_tokens, max_seq_len);
     if (st != PFKV_OK) return st;
     const int G = num_q_heads / c->num_kv_heads;
@@ -144,6 +145,15 @@ pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_he
     off = align256(off + sizeof(float) * rows_kv * q.G);
     q.off_o = off;
     off = align256(off + sizeof(float) * rows_kv * q.G * q.D);
+    // attention mass: every live token's G final scores, each head's final
+    // log2-sum-exp and the request flags
+    q.mass = mass;
+    q.off_mscore = off;
+    off = align256(off + (mass ? sizeof(float) * q.B * q.Hkv * (size_t)max_seq_len * q.G : 0));
+    q.off_lsefin = off;
+    off = align256(off + (mass ? sizeof(float) * q.B * q.Hq : 0));
+    q.off_rflags = off;
+    off = align256(off + (mass ? (size_t)q.B : 0));
     q.total = off;
     *plan = q;
     return PFKV_OK;
@@ -238,11 +248,21 @@ pfkv_status pfkv_decode_workspace_size(const pfkv_cache *cache, const pfkv_pages
     return PFKV_OK;
 }
 
-pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pages *pages,
-                                          const void *q, int32_t num_q_heads, float sm_scale,
-                                          int32_t split_tokens, int32_t max_seq_len,
-                                          void *workspace, size_t workspace_bytes, void *out,
-                                          uint8_t *flags, uint32_t stages, void *stream) {
+}  // extern "C"
+
+namespace {
+
+struct MassOut {
+    float *mass;
+    int64_t sb, sh;
+};
+
+// The attention call: the stages named in `stages`, plus the attention-mass
+// pass when `mass` is given.
+pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const void *q,
+                      int32_t num_q_heads, float sm_scale, int32_t split_tokens,
+                      int32_t max_seq_len, void *workspace, size_t workspace_bytes, void *out,
+                      uint8_t *flags, uint32_t stages, const MassOut *mass, void *stream) {
     if ((stages & PFKV_STAGE_ALL) == 0 || (stages & ~(PFKV_STAGE_ALL | PFKV_STAGE_FUSED_TAGS)))
         return PFKV_ERR_INVALID_ARG;
     const bool fused = (stages & PFKV_STAGE_FUSED_TAGS) != 0;
@@ -263,7 +283,8 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
     st = device_check(&sms);
     if (st != PFKV_OK) return st;
     DecodePlan plan;
-    st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan);
+    st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan,
+                   mass != nullptr);
     if (st != PFKV_OK) return st;
     if (workspace_bytes < plan.total) return PFKV_ERR_WORKSPACE;
 
@@ -295,6 +316,15 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
     a.lse = reinterpret_cast<float *>(ws + plan.off_lse);
     a.o = reinterpret_cast<float *>(ws + plan.off_o);
     a.ws_prefix = reinterpret_cast<int *>(ws + plan.off_prefix);
+    if (mass) {
+        a.mscore = reinterpret_cast<float *>(ws + plan.off_mscore);
+        a.mlen = max_seq_len;
+        a.lse_fin = reinterpret_cast<float *>(ws + plan.off_lsefin);
+        a.rflags = ws + plan.off_rflags;
+        a.mass = mass->mass;
+        a.mass_sb = mass->sb;
+        a.mass_sh = mass->sh;
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((stages & PFKV_STAGE_VALIDATE) && plan.tags && !fused && launch_validate(a, plan, s) != cudaSuccess)
@@ -302,7 +332,58 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
     if ((stages & PFKV_STAGE_SPLIT) && launch_split(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     if ((stages & PFKV_STAGE_COMBINE) && launch_combine(a, plan, s) != cudaSuccess)
         return PFKV_ERR_CUDA;
+    if (mass && launch_mass(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     return PFKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pages *pages,
+                                          const void *q, int32_t num_q_heads, float sm_scale,
+                                          int32_t split_tokens, int32_t max_seq_len,
+                                          void *workspace, size_t workspace_bytes, void *out,
+                                          uint8_t *flags, uint32_t stages, void *stream) {
+    return attn_impl(cache, pages, q, num_q_heads, sm_scale, split_tokens, max_seq_len,
+                     workspace, workspace_bytes, out, flags, stages, nullptr, stream);
+}
+
+pfkv_status pfkv_decode_mass_workspace_size(const pfkv_cache *cache, const pfkv_pages *pages,
+                                            int32_t num_q_heads, int32_t split_tokens,
+                                            int32_t max_seq_len, size_t *bytes) {
+    if (!bytes) return PFKV_ERR_INVALID_ARG;
+    pfkv_status st = check_cache(cache);
+    if (st != PFKV_OK) return st;
+    st = check_pages(cache, pages);
+    if (st != PFKV_OK) return st;
+    st = check_decode_args(cache, num_q_heads, split_tokens, max_seq_len);
+    if (st != PFKV_OK) return st;
+    int sms = 0;
+    st = device_check(&sms);
+    if (st != PFKV_OK) return st;
+    DecodePlan plan;
+    st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan, true);
+    if (st != PFKV_OK) return st;
+    *bytes = plan.total;
+    return PFKV_OK;
+}
+
+pfkv_status pfkv_paged_decode_attn_mass(const pfkv_cache *cache, const pfkv_pages *pages,
+                                        const void *q, int32_t num_q_heads, float sm_scale,
+                                        int32_t split_tokens, int32_t max_seq_len,
+                                        void *workspace, size_t workspace_bytes, void *out,
+                                        uint8_t *flags, float *attn_mass, int64_t mass_stride_b,
+                                        int64_t mass_stride_h, uint32_t options, void *stream) {
+    if (options & ~PFKV_STAGE_FUSED_TAGS) return PFKV_ERR_INVALID_ARG;
+    if (mass_stride_b < 0 || mass_stride_h < 0) return PFKV_ERR_INVALID_ARG;
+    if (pages && pages->batch > 0) {
+        if (!attn_mass) return PFKV_ERR_INVALID_ARG;
+        if (!aligned(attn_mass, 4)) return PFKV_ERR_ALIGNMENT;
+    }
+    const MassOut m{attn_mass, mass_stride_b, mass_stride_h};
+    return attn_impl(cache, pages, q, num_q_heads, sm_scale, split_tokens, max_seq_len,
+                     workspace, workspace_bytes, out, flags, PFKV_STAGE_ALL | options, &m, stream);
 }
 
 pfkv_status pfkv_paged_decode_attn(const pfkv_cache *cache, const pfkv_pages *pages,

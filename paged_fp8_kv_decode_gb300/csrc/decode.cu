@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(SplitCfg<D, G, FP8>::NWARPS * 32)
                 const bool ok = r * C::TPP + t < valid;
 #pragma unroll
                 for (int g = 0; g < G; ++g) sc[r][g] = ok ? acc[g] * ksc : -INFINITY;
+                if (a.mscore && ok && c == 0) store_scores<G>(a, bh, unit_tok0 + r * C::TPP + t, sc[r]);
             }
             // block maximum and (rare) rescale of the running state
             float mb[G];
@@ -410,6 +411,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int Hkv
     }
     const uint32_t flags = s_flags;
     if (hq == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
+    if (hq == 0 && tid == 0 && a.rflags) a.rflags[b] = (uint8_t)flags;
 
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
     __nv_bfloat16 *out = a.out + ((long long)b * Hq + hq) * D;
@@ -422,6 +424,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int Hkv
     const float *lse = a.lse + row0;
     const float *o = a.o + row0 * D;
     if (nch == 1) {
+        if (a.lse_fin && tid == 0) a.lse_fin[(long long)b * Hq + hq] = lse[0];
         out[tid] = __float2bfloat16_rn(o[tid]);
         return;
     }
@@ -441,6 +444,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int Hkv
         wsum += w;
         acc = fmaf(w, o[(long long)cc * D + tid], acc);
     }
+    if (a.lse_fin && tid == 0)
+        a.lse_fin[(long long)b * Hq + hq] = wsum > 0.f ? M + __log2f(wsum) : -INFINITY;
     out[tid] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
 }
 

@@ -554,6 +554,11 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) sc[g] = ok ? sc[g] * ksc : -INFINITY;
+            if (a.mscore && ok) {  // scores for the attention-mass pass
+                const int bh = con.k / nchunks, c = con.k - bh * nchunks;
+                const int page = c * (chunk_tokens / kPage) + (con.x + my_u - sm.prefix[con.k]);
+                store_scores<G>(a, bh, page * kPage + my_row, sc);
+            }
             float mb[G];
             bool grow = false;
 #pragma unroll
@@ -746,6 +751,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
     __syncthreads();
     const uint32_t flags = sm.flags;
     if (h == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
+    if (h == 0 && tid == 0 && a.rflags) a.rflags[b] = (uint8_t)flags;
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
     uint2 *out = reinterpret_cast<uint2 *>(a.out + (long long)(b * Hkv + h) * G * D);
     if (flags != 0 || n == 0 || U == 0) {
@@ -872,6 +878,8 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
             ws += sm.u.red.wsum[w2][g];
         }
         const float inv = ws > 0.f ? 1.f / ws : 0.f;
+        if (a.lse_fin && d4 == 0)
+            a.lse_fin[(long long)(b * Hkv + h) * G + g] = ws > 0.f ? M[g] + plog2(ws) : -INFINITY;
         const __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x * inv, s4.y * inv);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z * inv, s4.w * inv);
         out[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),

@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(SwzCfg<G>::NWARPS * 32)
                 const float ksc = sm.kscale[warp][C::GU * i + my_u];
 #pragma unroll
                 for (int g = 0; g < G; ++g) sc[g] = ok ? sc[g] * ksc : -INFINITY;
+                if (a.mscore && ok) store_scores<G>(a, bh, gtok0 + my_tok, sc);
             }
             // ---- online softmax over the granule ----
             float mb[G];

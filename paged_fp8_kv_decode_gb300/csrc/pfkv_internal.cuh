@@ -43,6 +43,8 @@ struct DecodePlan {
     int htiles;         // validation tiles per table row: ceil(max_pages / kValTile)
     // workspace layout (byte offsets, 256-aligned)
     size_t off_hflags, off_status, off_lse, off_o, off_prefix, total;
+    bool mass;
+    size_t off_mscore, off_lsefin, off_rflags;
 };
 
 struct DecodeArgs {
@@ -67,6 +69,13 @@ struct DecodeArgs {
     uint32_t *hflags;   // [B][Hkv][htiles] tag/bounds bits from the validation kernel
     int htiles;
     int fuse_tags;      // compare tags where the split kernels load page ids
+    // attention mass (null unless requested)
+    float *mscore;      // [B][Hkv][mlen][G] final scores (log2 units) of live tokens
+    int mlen;           // = max_seq_len
+    float *lse_fin;     // [B][Hq] log2-sum-exp over all of a head's tokens
+    uint8_t *rflags;    // [B] request flags, written by the combine
+    float *mass;        // caller's running totals, mass[b*mass_sb + h*mass_sh + j]
+    long long mass_sb, mass_sh;
     uint32_t *status;   // [B][Hkv][nchunks]
     float *lse;         // [B][Hq][nchunks]  log2-sum-exp of the chunk
     float *o;           // [B][Hq][nchunks][D] chunk output (normalised)
@@ -121,6 +130,23 @@ __device__ __forceinline__ uint32_t entry_bits(const DecodeArgs &a, int id, int 
     return 0u;
 }
 
+// Final scores of one token for the attention-mass pass (a.mscore set).
+template <int G>
+__device__ __forceinline__ void store_scores(const DecodeArgs &a, int bh, int tok,
+                                             const float (&sc)[G]) {
+    float *dst = a.mscore + ((long long)bh * a.mlen + tok) * G;
+    if constexpr (G == 8) {
+        reinterpret_cast<float4 *>(dst)[0] = make_float4(sc[0], sc[1], sc[2], sc[3]);
+        reinterpret_cast<float4 *>(dst)[1] = make_float4(sc[4], sc[5], sc[6], sc[7]);
+    } else if constexpr (G == 4) {
+        *reinterpret_cast<float4 *>(dst) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+    } else if constexpr (G == 2) {
+        *reinterpret_cast<float2 *>(dst) = make_float2(sc[0], sc[1]);
+    } else {
+        dst[0] = sc[0];
+    }
+}
+
 // Whether the validation kernel flagged request b (any kv head, any tile).
 // Computed by the whole CTA: every thread must call it.
 __device__ __forceinline__ bool request_rejected_cta(const DecodeArgs &a, int b, int Hkv) {
@@ -137,6 +163,7 @@ __device__ __forceinline__ bool request_rejected_cta(const DecodeArgs &a, int b,
 cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s);
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_mass(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 bool swz_supported(const DecodePlan &p, int num_pages);
 bool pers_supported(const DecodePlan &p, int num_pages);
 int pers_workers_per_cta();

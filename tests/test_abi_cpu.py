@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert names == sorted(["pfkv_abi_version", "pfkv_decode_workspace_size", "pfkv_e4m3_decode",
                             "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_paged_decode_attn",
-                            "pfkv_paged_decode_attn_fused_tags",
+                            "pfkv_paged_decode_attn_fused_tags", "pfkv_paged_decode_attn_mass",
+                            "pfkv_decode_mass_workspace_size",
                             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
                             "pfkv_status_string", "pfkv_step_graph_create",
                             "pfkv_step_graph_destroy", "pfkv_step_graph_launch"])
@@ -156,6 +157,20 @@ def test_step_graph_argument_checks(B):
     assert h.value is None
     assert L.pfkv_step_graph_destroy(None) == 0
     assert L.pfkv_step_graph_launch(None, None) == 1
+
+
+def test_mass_entry_checks_arguments(B):
+    c, p = _structs(B)
+    L = B.lib()
+    def mass(buf=0xF0000, sb=8 * 64, sh=64, opts=0, Hq=4):
+        return L.pfkv_paged_decode_attn_mass(ctypes.byref(c), ctypes.byref(p), 0xA0000, Hq, 0.125,
+                                             0, 64, 0xB0000, 1 << 30, 0xC0000, None, buf, sb, sh,
+                                             opts, None)
+    assert mass(buf=None) == 1
+    assert mass(buf=0xF0002) == 3
+    assert mass(sb=-1) == 1
+    assert mass(opts=0x2) == 1
+    assert mass(Hq=6) == 2
 
 
 def test_empty_batch_is_a_no_op(B):
