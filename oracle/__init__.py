@@ -68,6 +68,10 @@ def lib():
                                             ctypes.c_void_p, ctypes.c_int32, ctypes.c_double,
                                             ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                                             ctypes.c_int64]
+        L.oracle_paged_decode_multi.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Pages),
+                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_double, ctypes.c_int32, ctypes.c_void_p,
+                                                ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -211,6 +215,23 @@ def attention_mass(cache: dict, pages: dict, q, num_q_heads: int, sm_scale: floa
     lib().oracle_attention_mass(ctypes.byref(c), ctypes.byref(p), _ptr(q), int(num_q_heads),
                                 float(sm_scale), int(max_seq_len), _ptr(mass), int(sb), int(sh))
     return mass
+
+
+def paged_decode_multi(cache: dict, pages: dict, q, num_q_heads: int, kq: int,
+                       sm_scale: float, max_seq_len: int):
+    """fp64 multi-query verify (see oracle.c).  q: uint16 bf16 bits
+    [B][kq][Hq][D].  Returns (out fp64 [B][kq][Hq][D], flags)."""
+    c = _cache(**cache)
+    p = _pages(**pages)
+    _need(q, np.uint16, "q")
+    B = int(pages["batch"])
+    D = int(cache["head_dim"])
+    out = np.zeros((B, int(kq), int(num_q_heads), D), dtype=np.float64)
+    flags = np.zeros(max(B, 1), dtype=np.uint8)
+    lib().oracle_paged_decode_multi(ctypes.byref(c), ctypes.byref(p), _ptr(q), int(num_q_heads),
+                                    int(kq), float(sm_scale), int(max_seq_len), _ptr(out),
+                                    _ptr(flags))
+    return out, flags[:B]
 
 
 def num_threads() -> int:

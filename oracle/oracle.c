@@ -26,6 +26,9 @@
  *       compression goes open source", 3rd paragraph: eviction tracks the
  *       attention each KV entry has received over past steps and evicts the
  *       entries with the lowest total, like a least-frequently-used cache.
+ *  [S]  "Workers AI targets the inference bottleneck", section "Speculative
+ *       decoding: predicting more than one token", 1st paragraph: the model
+ *       verifies all candidate tokens in a single forward pass.
  *  [E]  The OCP 8-bit floating point specification (E4M3 "FN" variant), the
  *       format that [Q] names: 1 sign, 4 exponent (bias 7), 3 mantissa bits,
  *       no infinities, S.1111.111 is NaN, largest finite 448.
@@ -47,6 +50,10 @@
  *     weight of token j (weights normalised over the head's n tokens); a call
  *     adds it to a running total kept by the caller.  Flagged requests and
  *     zero-length heads add nothing.
+ *  R8 multi-query verify [S]: a request's kq candidate tokens are the last kq
+ *     tokens of each of its heads (already written); query token i (0-based)
+ *     attends to the first n - kq + 1 + i tokens of the head (causal among the
+ *     candidates).  A query that would see no token gives zero output.
  *
  * Precision: attention is computed in fp64 (plain two-pass softmax, natural
  * exp, sequential token order); quantisation decisions are taken in fp32, the
@@ -463,6 +470,64 @@ void oracle_attention_mass(const orc_cache *c, const orc_pages *pg, const uint16
             for (int32_t j = 0; j < n; ++j)
                 mrow[j] += exp(s[j] - m) / l;
         }
+        free(s);
+    }
+    free(flags);
+}
+
+/*
+ * Multi-query verify [S], reading R8: q and out are [B][kq][Hq][D]; the
+ * output row of (b, i, hq) is the decode attention of q[b][i][hq] over the
+ * first n - kq + 1 + i tokens of kv head hq / G, n = seq_lens(b, h).  Flags are
+ * those of the request (oracle_validate over its n tokens); flagged requests
+ * give zero rows for every query token.
+ */
+void oracle_paged_decode_multi(const orc_cache *c, const orc_pages *pg, const uint16_t *q,
+                               int32_t num_q_heads, int32_t kq, double sm_scale,
+                               int32_t max_seq_len, double *out, uint8_t *flags_out)
+{
+    const int H = c->num_kv_heads, D = c->head_dim, Hq = num_q_heads;
+    const int G = Hq / H;
+    const int B = pg->batch;
+    uint8_t *flags = (uint8_t *)malloc(B > 0 ? (size_t)B : 1);
+    oracle_validate(c, pg, max_seq_len, flags);
+    if (flags_out)
+        memcpy(flags_out, flags, (size_t)B);
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t row = 0; row < (int64_t)B * kq * Hq; ++row) {
+        int b = (int)(row / ((int64_t)kq * Hq));
+        int i = (int)((row / Hq) % kq), hq = (int)(row % Hq);
+        int h = hq / G;
+        double *o = out + row * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        int32_t n = pg->seq_lens[(int64_t)b * pg->len_stride_b + (int64_t)h * pg->len_stride_h];
+        int64_t seen = (int64_t)n - kq + 1 + i;   /* tokens query i attends to */
+        if (flags[b] != 0 || seen <= 0)
+            continue;
+        const int32_t *trow = pg->block_tables + (int64_t)b * pg->bt_stride_b + (int64_t)h * pg->bt_stride_h;
+        double *s = (double *)malloc(sizeof(double) * (size_t)seen);
+        double m = -INFINITY, l = 0.0;
+        for (int64_t j = 0; j < seen; ++j) {
+            int64_t u = unit_index(c, trow[j / ORC_PAGE], h);
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += (double)bf16_bits_to_float(q[row * D + d]) *
+                       kv_value(c, c->k_pages, c->k_scale, u, (int)(j % ORC_PAGE), d);
+            s[j] = sm_scale * acc;
+            if (s[j] > m)
+                m = s[j];
+        }
+        for (int64_t j = 0; j < seen; ++j) {
+            double p = exp(s[j] - m);
+            int64_t u = unit_index(c, trow[j / ORC_PAGE], h);
+            l += p;
+            for (int d = 0; d < D; ++d)
+                o[d] += p * kv_value(c, c->v_pages, c->v_scale, u, (int)(j % ORC_PAGE), d);
+        }
+        for (int d = 0; d < D; ++d)
+            o[d] /= l;
         free(s);
     }
     free(flags);
