@@ -75,6 +75,9 @@ def parse_args(argv=None):
     ap.add_argument("--graph-layers", type=int, default=0,
                     help="time one decode step of this many Llama-shaped layers, each with its "
                          "own pool, captured as one CUDA graph (pfkv_step_graph_*)")
+    ap.add_argument("--multi", type=int, default=0,
+                    help="multi-query verify: append this many candidate tokens per request "
+                         "and attend with all of them, causally (pfkv_paged_decode_attn_multi)")
     ap.add_argument("--batch", type=int, default=32, help="sweep: batch size")
     ap.add_argument("--kv-dtype", default="fp8", choices=["fp8", "bf16"], help="sweep: pool dtype")
     return ap.parse_args(argv)
@@ -904,10 +907,124 @@ def run_graph(args):
         torch.distributed.destroy_process_group()
 
 
+def run_multi(args):
+    """One JSON line: the verification step of speculative decoding on the
+    Llama-shaped FP8 layer: kv_append of kq candidate tokens per request, then
+    attention of all kq query tokens, causal among them, over rotating layer
+    replicas (inputs larger than L2)."""
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import dataclasses
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_fp8_kv_decode_gb300 import binding as B
+    from paged_fp8_kv_decode_gb300 import workloads as W
+    from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
+    kq = args.multi
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    L = B.lib()
+    reps = []
+    opt = B.PFKV_STAGE_FUSED_TAGS if args.fused_tags else 0
+    for r in range(args.replicas):
+        base = W.spec_llama8b("full", seed=rank_seed(W.BASE_SEED + 2, rank, r))
+        # the cache holds the context and the kq candidates (the step rewrites them)
+        spec = dataclasses.replace(base, append=False, lens=base.lens + kq, split_tokens=args.split,
+                                   tags=not args.no_tags)
+        db = DeviceBatch(W.make_batch(spec), device=dev)
+        g = torch.Generator(device=dev).manual_seed(77 + r)
+        q = torch.randn((spec.B, kq, spec.Hq, spec.D), generator=g, device=dev).to(torch.bfloat16)
+        kn = torch.randn((spec.B, spec.Hkv, kq, spec.D), generator=g, device=dev).to(torch.bfloat16)
+        vn = torch.randn((spec.B, spec.Hkv, kq, spec.D), generator=g, device=dev).to(torch.bfloat16)
+        pos = (db.seq_lens - kq).contiguous()
+        out = torch.empty_like(q)
+        Lmax = db.max_seq_len
+        ws = torch.empty(B.pfkv_decode_multi_workspace_size(db.cache, db.pages, spec.Hq, kq,
+                                                            spec.split_tokens, Lmax),
+                         dtype=torch.uint8, device=dev)
+        c, p = db.cache.c_struct(), db.pages.c_struct()
+        keep = (db, q, kn, vn, pos, out, ws, c, p)
+        app = (ctypes.byref(c), ctypes.byref(p), pos.data_ptr(), None, kq, kn.data_ptr(),
+               vn.data_ptr(), db.append_flags.data_ptr(), sh)
+        att = (ctypes.byref(c), ctypes.byref(p), q.data_ptr(), spec.Hq, kq,
+               ctypes.c_float(spec.sm_scale), spec.split_tokens, Lmax, ws.data_ptr(), ws.numel(),
+               out.data_ptr(), db.flags.data_ptr(), opt, sh)
+        reps.append((keep, app, att))
+    spec0 = reps[0][0][0].spec
+
+    def step(r):
+        _, app, att = r
+        if L.pfkv_kv_append(*app) or L.pfkv_paged_decode_attn_multi(*att):
+            raise RuntimeError("multi-query step failed")
+
+    for i in range(args.warmup):
+        step(reps[i % len(reps)])
+    torch.cuda.synchronize()
+    K = args.steps
+    sampler = None
+    if rank == 0 and not args.no_clocks:
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(reps[i % len(reps)])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    el = reduce_max(t0.elapsed_time(t1) / 1e3, world, dev)
+    for (db, *_), _, _ in reps:
+        if int(db.flags[:spec0.B].sum()) or int(db.append_flags[:spec0.B].sum()):
+            raise RuntimeError("benchmark workload flagged a request")
+    # algorithmic bytes: each request's KV once (all kq queries read the same
+    # pages), tables and scales, kq rows of q and out, the appended candidates
+    attn = statistics.mean(r[0][0].algorithmic_bytes() for r in reps)
+    attn += 2 * spec0.B * (kq - 1) * spec0.Hq * spec0.D * 2
+    append = spec0.B * spec0.Hkv * kq * spec0.D * (2 * 2 + 2) + spec0.B * spec0.Hkv * 8
+    step_bytes = attn + append
+    if rank == 0:
+        line = {
+            "metric": f"multi-query verify KV GB/s (Llama-3.1-8B-shaped FP8 layer, "
+                      f"{kq} candidate tokens per request)",
+            "value": round(aggregate(step_bytes, K, el, world), 2), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(el / K * 1e3, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8_e4m3 KV, fp32 accumulate, bf16 q/out",
+            "data": "synthetic",
+            "config": {"workload": "llama8b-fp8-verify", "batch": spec0.B,
+                       "query_tokens_per_request": kq, "num_q_heads": spec0.Hq,
+                       "num_kv_heads": spec0.Hkv, "head_dim": spec0.D, "page_size": 16,
+                       "seq_lens": f"U[512,8192]+{kq}", "replicas": args.replicas,
+                       "tag_check": ("none" if args.no_tags else "fused into attention"
+                                     if args.fused_tags else "separate pass"),
+                       "l2": "inputs larger than L2: %d rotating replicas" % args.replicas,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "verified_tokens_per_s": round(world * spec0.B * kq / (N_LAYERS * el / K), 1),
+            "gpu_launches": K * (3 if (args.no_tags or args.fused_tags) else 4),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.multi > 0:
+        run_multi(args)
     elif args.graph_layers > 0:
         run_graph(args)
     elif args.workload != "llama8b":

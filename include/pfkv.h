@@ -315,6 +315,40 @@ pfkv_status pfkv_paged_decode_attn_mass(const pfkv_cache *cache, const pfkv_page
                                         int64_t mass_stride_h, uint32_t options, void *stream);
 
 /*
+ * pfkv_paged_decode_attn_multi -- attention of several query tokens per
+ * request, causal among them: the verification pass of speculative
+ * (prompt-lookup) decoding, which checks all candidate tokens in one forward
+ * pass ("Workers AI targets the inference bottleneck", section "Speculative
+ * decoding: predicting more than one token", 1st paragraph).
+ *
+ * The request's num_query_tokens = kq candidate tokens are the LAST kq tokens
+ * of each of its heads (already written, e.g. by pfkv_kv_append with
+ * num_new_tokens = kq).  Query token i (0-based) attends to the first
+ * n - kq + 1 + i tokens of head h, n = seq_lens(b, h): the cached context, the
+ * candidates before it and itself.  A query that would see no token (n < kq)
+ * gives zero output.
+ *
+ *   q, out : bf16 [batch][kq][num_q_heads][head_dim]
+ *   flags  : per request [batch], as in pfkv_paged_decode_attn; a flagged
+ *            request gives zero output for all of its query tokens
+ *   options: 0 or PFKV_STAGE_FUSED_TAGS
+ *   workspace >= pfkv_decode_multi_workspace_size(...) bytes
+ * kq = 1 is pfkv_paged_decode_attn.  The kq queries of a request read the
+ * same pages; the kernels process them side by side so that repeated reads
+ * of a page tend to hit L2.
+ */
+pfkv_status pfkv_decode_multi_workspace_size(const pfkv_cache *cache, const pfkv_pages *pages,
+                                             int32_t num_q_heads, int32_t num_query_tokens,
+                                             int32_t split_tokens, int32_t max_seq_len,
+                                             size_t *bytes);
+pfkv_status pfkv_paged_decode_attn_multi(const pfkv_cache *cache, const pfkv_pages *pages,
+                                         const void *q, int32_t num_q_heads,
+                                         int32_t num_query_tokens, float sm_scale,
+                                         int32_t split_tokens, int32_t max_seq_len,
+                                         void *workspace, size_t workspace_bytes, void *out,
+                                         uint8_t *flags, uint32_t options, void *stream);
+
+/*
  * Step graphs: one decode step of a stack of attention layers captured once
  * as a CUDA graph and replayed with a single launch.  The Infire page ("How
  * we built the most efficient inference engine for Cloudflare's network",

@@ -44,7 +44,8 @@ PFKV_STAGE_FUSED_TAGS = 0x8
 EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",
             "pfkv_paged_decode_attn_stages", "pfkv_paged_decode_attn_fused_tags",
             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_mass",
-            "pfkv_decode_mass_workspace_size", "pfkv_step_graph_create", "pfkv_step_graph_launch",
+            "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
+            "pfkv_decode_multi_workspace_size", "pfkv_step_graph_create", "pfkv_step_graph_launch",
             "pfkv_step_graph_destroy", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string",
             "pfkv_abi_version")
 
@@ -111,6 +112,15 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.POINTER(_CPages), P, I32,
                                                      ctypes.c_float, I32, I32, P, P, P]
         L.pfkv_paged_decode_attn_noalloc.restype = ctypes.c_int
+        L.pfkv_decode_multi_workspace_size.argtypes = [ctypes.POINTER(_CCache),
+                                                       ctypes.POINTER(_CPages), I32, I32, I32,
+                                                       I32, ctypes.POINTER(ctypes.c_size_t)]
+        L.pfkv_decode_multi_workspace_size.restype = ctypes.c_int
+        L.pfkv_paged_decode_attn_multi.argtypes = [ctypes.POINTER(_CCache),
+                                                   ctypes.POINTER(_CPages), P, I32, I32,
+                                                   ctypes.c_float, I32, I32, P, ctypes.c_size_t,
+                                                   P, P, ctypes.c_uint32, P]
+        L.pfkv_paged_decode_attn_multi.restype = ctypes.c_int
         L.pfkv_decode_mass_workspace_size.argtypes = L.pfkv_decode_workspace_size.argtypes
         L.pfkv_decode_mass_workspace_size.restype = ctypes.c_int
         L.pfkv_paged_decode_attn_mass.argtypes = [ctypes.POINTER(_CCache), ctypes.POINTER(_CPages),
@@ -284,6 +294,33 @@ def pfkv_paged_decode_attn_fused_tags(cache: Cache, pages: Pages, q: torch.Tenso
         ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
         int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), _ptr(flags), _stream(stream)), "pfkv_paged_decode_attn_fused_tags")
+
+
+def pfkv_decode_multi_workspace_size(cache: Cache, pages: Pages, num_q_heads: int,
+                                     num_query_tokens: int, split_tokens: int,
+                                     max_seq_len: int) -> int:
+    c, p = cache.c_struct(), pages.c_struct()
+    out = ctypes.c_size_t(0)
+    _check(lib().pfkv_decode_multi_workspace_size(ctypes.byref(c), ctypes.byref(p),
+                                                  int(num_q_heads), int(num_query_tokens),
+                                                  int(split_tokens), int(max_seq_len),
+                                                  ctypes.byref(out)),
+           "pfkv_decode_multi_workspace_size")
+    return int(out.value)
+
+
+def pfkv_paged_decode_attn_multi(cache: Cache, pages: Pages, q: torch.Tensor, sm_scale: float,
+                                 split_tokens: int, max_seq_len: int, workspace: torch.Tensor,
+                                 out: torch.Tensor, flags: Optional[torch.Tensor] = None,
+                                 options: int = 0, stream=None) -> None:
+    """q, out: bf16 [B][kq][Hq][D]: the kq candidate tokens of each request,
+    causal among themselves (see include/pfkv.h)."""
+    c, p = cache.c_struct(), pages.c_struct()
+    kq, Hq = int(q.shape[1]), int(q.shape[2])
+    _check(lib().pfkv_paged_decode_attn_multi(
+        ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, kq, float(sm_scale), int(split_tokens),
+        int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(flags), int(options), _stream(stream)), "pfkv_paged_decode_attn_multi")
 
 
 def pfkv_decode_mass_workspace_size(cache: Cache, pages: Pages, num_q_heads: int,

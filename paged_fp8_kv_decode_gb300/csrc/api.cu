@@ -101,12 +101,15 @@ pfkv_status check_decode_args(const pfkv_cache *c, int32_t num_q_heads, int32_t 
 
 pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_heads,
                       int32_t split_tokens, int32_t max_seq_len, int num_sms, DecodePlan *plan,
-                      bool mass = false) {
+                      bool mass = false, int32_t kq = 1) {
     const pfkv_status st = check_decode_args(c, num_q_heads, split_tokens, max_seq_len);
     if (st != PFKV_OK) return st;
+    if (kq < 1 || (long long)p->batch * kq > 0x7fffffffLL) return PFKV_ERR_INVALID_ARG;
     const int G = num_q_heads / c->num_kv_heads;
     DecodePlan q{};
-    q.B = p->batch;
+    q.Breq = p->batch;
+    q.kq = kq;
+    q.B = p->batch * kq;  // virtual requests: one per (request, query token)
     q.Hkv = c->num_kv_heads;
     q.Hq = num_q_heads;
     q.G = G;
@@ -136,7 +139,7 @@ pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_he
     const size_t rows_kv = q.kind == 1 ? (size_t)items + q.workers : (size_t)items;
     size_t off = 0;
     q.off_hflags = off;
-    off = align256(off + (q.tags ? sizeof(uint32_t) * q.B * q.Hkv * q.htiles : 0));
+    off = align256(off + (q.tags ? sizeof(uint32_t) * q.Breq * q.Hkv * q.htiles : 0));
     q.off_prefix = off;
     off = align256(off + (q.kind == 1 ? sizeof(int) * ((size_t)items + 1) : 0));
     q.off_status = off;
@@ -262,7 +265,9 @@ struct MassOut {
 pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const void *q,
                       int32_t num_q_heads, float sm_scale, int32_t split_tokens,
                       int32_t max_seq_len, void *workspace, size_t workspace_bytes, void *out,
-                      uint8_t *flags, uint32_t stages, const MassOut *mass, void *stream) {
+                      uint8_t *flags, uint32_t stages, const MassOut *mass, void *stream,
+                      int32_t kq = 1) {
+    if (kq < 1 || (mass && kq != 1)) return kq < 1 ? PFKV_ERR_INVALID_ARG : PFKV_ERR_UNSUPPORTED;
     if ((stages & PFKV_STAGE_ALL) == 0 || (stages & ~(PFKV_STAGE_ALL | PFKV_STAGE_FUSED_TAGS)))
         return PFKV_ERR_INVALID_ARG;
     const bool fused = (stages & PFKV_STAGE_FUSED_TAGS) != 0;
@@ -284,7 +289,7 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
     if (st != PFKV_OK) return st;
     DecodePlan plan;
     st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan,
-                   mass != nullptr);
+                   mass != nullptr, kq);
     if (st != PFKV_OK) return st;
     if (workspace_bytes < plan.total) return PFKV_ERR_WORKSPACE;
 
@@ -312,6 +317,7 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
     a.hflags = plan.tags && !fused ? reinterpret_cast<uint32_t *>(ws + plan.off_hflags) : nullptr;
     a.htiles = plan.htiles;
     a.fuse_tags = plan.tags && fused ? 1 : 0;
+    a.kq = plan.kq;
     a.status = reinterpret_cast<uint32_t *>(ws + plan.off_status);
     a.lse = reinterpret_cast<float *>(ws + plan.off_lse);
     a.o = reinterpret_cast<float *>(ws + plan.off_o);
@@ -347,6 +353,42 @@ pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pa
                                           uint8_t *flags, uint32_t stages, void *stream) {
     return attn_impl(cache, pages, q, num_q_heads, sm_scale, split_tokens, max_seq_len,
                      workspace, workspace_bytes, out, flags, stages, nullptr, stream);
+}
+
+pfkv_status pfkv_decode_multi_workspace_size(const pfkv_cache *cache, const pfkv_pages *pages,
+                                             int32_t num_q_heads, int32_t num_query_tokens,
+                                             int32_t split_tokens, int32_t max_seq_len,
+                                             size_t *bytes) {
+    if (!bytes) return PFKV_ERR_INVALID_ARG;
+    pfkv_status st = check_cache(cache);
+    if (st != PFKV_OK) return st;
+    st = check_pages(cache, pages);
+    if (st != PFKV_OK) return st;
+    st = check_decode_args(cache, num_q_heads, split_tokens, max_seq_len);
+    if (st != PFKV_OK) return st;
+    if (num_query_tokens < 1) return PFKV_ERR_INVALID_ARG;
+    int sms = 0;
+    st = device_check(&sms);
+    if (st != PFKV_OK) return st;
+    DecodePlan plan;
+    st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan, false,
+                   num_query_tokens);
+    if (st != PFKV_OK) return st;
+    *bytes = plan.total;
+    return PFKV_OK;
+}
+
+pfkv_status pfkv_paged_decode_attn_multi(const pfkv_cache *cache, const pfkv_pages *pages,
+                                         const void *q, int32_t num_q_heads,
+                                         int32_t num_query_tokens, float sm_scale,
+                                         int32_t split_tokens, int32_t max_seq_len,
+                                         void *workspace, size_t workspace_bytes, void *out,
+                                         uint8_t *flags, uint32_t options, void *stream) {
+    if (options & ~PFKV_STAGE_FUSED_TAGS) return PFKV_ERR_INVALID_ARG;
+    if (num_query_tokens < 1) return PFKV_ERR_INVALID_ARG;
+    return attn_impl(cache, pages, q, num_q_heads, sm_scale, split_tokens, max_seq_len,
+                     workspace, workspace_bytes, out, flags, PFKV_STAGE_ALL | options, nullptr,
+                     stream, num_query_tokens);
 }
 
 pfkv_status pfkv_decode_mass_workspace_size(const pfkv_cache *cache, const pfkv_pages *pages,

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kValThreads) validate_kernel(DecodeArgs a, int
 }
 
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    return launch_pdl(validate_kernel, dim3(p.B * p.Hkv, p.htiles), dim3(kValThreads), 0, s, a,
+    return launch_pdl(validate_kernel, dim3(p.Breq * p.Hkv, p.htiles), dim3(kValThreads), 0, s, a,
                       p.Hkv);
 }
 

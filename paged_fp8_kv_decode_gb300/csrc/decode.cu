@@ -146,16 +146,17 @@ __global__ void __launch_bounds__(SplitCfg<D, G, FP8>::NWARPS * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane / C::LPT, c = lane % C::LPT;
 
-    const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
-    if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) return;
+    // b is the virtual request (see DecodeArgs::kq)
+    const int n = query_len(a, b, h);
+    if (n < 0) return;
     const int tok0 = chunk * chunk_tokens;
     if (tok0 >= n) return;  // empty item
-    if (request_rejected_cta(a, b, Hkv)) return;  // rejected by the validation kernel
+    if (request_rejected_cta(a, b / a.kq, Hkv)) return;  // rejected by the validation kernel
     const int tok1 = min(n, tok0 + chunk_tokens);
     const int p_begin = tok0 / kPage;
     const int npages = (tok1 - tok0 + kPage - 1) / kPage;
     const int nmine = warp < npages ? (npages - warp + NW - 1) / NW : 0;
-    const long long bt_row = (long long)b * a.bt_sb + (long long)h * a.bt_sh;
+    const long long bt_row = table_row(a, b, h);
 
     if (threadIdx.x == 0) sm.status = 0;
     // ---- per-warp unit metadata: page ids first (they gate the copies) ----
@@ -386,34 +387,35 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int Hkv
     if (tid == 0) s_flags = 0;
     __syncthreads();
 
+    // b is the virtual request (see DecodeArgs::kq); the flags belong to the
+    // request rb and cover all of its query tokens
+    const int rb = b / a.kq, v0 = rb * a.kq;
     // request flags: lengths and validation bits of every kv head ...
     uint32_t f = 0;
-    for (int i = tid; i < Hkv; i += D) {
-        const int ni = a.seq_lens[(long long)b * a.len_sb + (long long)i * a.len_sh];
-        if (ni < 0 || (long long)ni > (long long)a.max_pages * kPage || ni > a.max_seq_len)
-            f |= PFKV_FLAG_BAD_LENGTH;
-    }
+    for (int i = tid; i < Hkv; i += D)
+        if (query_len(a, v0, i) < 0) f |= PFKV_FLAG_BAD_LENGTH;
     if (a.hflags)
-        for (int i = tid; i < Hkv * a.htiles; i += D) f |= a.hflags[(long long)b * Hkv * a.htiles + i];
+        for (int i = tid; i < Hkv * a.htiles; i += D) f |= a.hflags[(long long)rb * Hkv * a.htiles + i];
     if (f) atomicOr(&s_flags, f);
     __syncthreads();
     // ... then the split kernel's per-chunk status (only written for live
     // chunks of requests the validation kernel passed)
     if (s_flags == 0) {
         f = 0;
-        for (int i = 0; i < Hkv; ++i) {
-            const int ni = a.seq_lens[(long long)b * a.len_sb + (long long)i * a.len_sh];
-            const int nch = (ni + chunk_tokens - 1) / chunk_tokens;
-            for (int cc = tid; cc < nch; cc += D) f |= a.status[(long long)(b * Hkv + i) * nchunks + cc];
-        }
+        for (int v = v0; v < v0 + a.kq; ++v)
+            for (int i = 0; i < Hkv; ++i) {
+                const int ni = query_len(a, v, i);
+                const int nch = (ni + chunk_tokens - 1) / chunk_tokens;
+                for (int cc = tid; cc < nch; cc += D) f |= a.status[(long long)(v * Hkv + i) * nchunks + cc];
+            }
         if (f) atomicOr(&s_flags, f);
         __syncthreads();
     }
     const uint32_t flags = s_flags;
-    if (hq == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
-    if (hq == 0 && tid == 0 && a.rflags) a.rflags[b] = (uint8_t)flags;
+    if (b == v0 && hq == 0 && tid == 0 && a.flags) a.flags[rb] = (uint8_t)flags;
+    if (b == v0 && hq == 0 && tid == 0 && a.rflags) a.rflags[rb] = (uint8_t)flags;
 
-    const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+    const int n = max(0, query_len(a, b, h));
     __nv_bfloat16 *out = a.out + ((long long)b * Hq + hq) * D;
     if (flags != 0 || n == 0) {
         out[tid] = __float2bfloat16_rn(0.f);

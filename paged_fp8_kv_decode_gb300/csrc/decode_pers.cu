@@ -163,11 +163,13 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     pdl_enter();
 
     // ---------------- prologue: request flags, unit prefix sums ----------------
-    for (int b = tid; b < B; b += C::NT) sm.rflag[b] = 0;
+    // B counts virtual requests (see DecodeArgs::kq); rflag is per request
+    const int Breq = B / a.kq;
+    for (int b = tid; b < Breq; b += C::NT) sm.rflag[b] = 0;
     __syncthreads();
-    if (a.hflags) {  // [B][Hkv][htiles], read in parallel
+    if (a.hflags) {  // [Breq][Hkv][htiles], read in parallel
         const int per_req = Hkv * a.htiles;
-        for (int i = tid; i < B * per_req; i += C::NT)
+        for (int i = tid; i < Breq * per_req; i += C::NT)
             if (a.hflags[i]) sm.rflag[i / per_req] = 1;
     }
     __syncthreads();
@@ -176,11 +178,10 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     int local = 0;
     for (int k = k0; k < k1; ++k) {
         const int bh = k / nchunks, c = k - bh * nchunks;
-        const int b = bh / Hkv, h = bh - b * Hkv;
-        const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+        const int b = bh / Hkv, h = bh - b * Hkv;  // b: virtual request
+        const int n = query_len(a, b, h);
         int units = 0, lastnv = 0;
-        if (!sm.rflag[b] && n >= 0 && (long long)n <= (long long)a.max_pages * kPage &&
-            n <= a.max_seq_len) {
+        if (!sm.rflag[b / a.kq] && n >= 0) {
             const int pages = (n + kPage - 1) / kPage;
             const int cp = chunk_tokens / kPage;
             units = max(0, min(pages, (c + 1) * cp) - c * cp);
@@ -427,7 +428,7 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
                 const int bh = k / nchunks, c = k - bh * nchunks;
                 const int b = bh / Hkv, h = bh - b * Hkv;
                 const int page = c * (chunk_tokens / kPage) + (int)(x - sm.prefix[k]);
-                const long long bi = (long long)b * a.bt_sb + (long long)h * a.bt_sh + page;
+                const long long bi = table_row(a, b, h) + page;
                 const int id = a.block_tables[bi];
                 bad = entry_bits(a, id, h, Hkv, bi);
                 phys = bad ? -1 : id * Hkv + h;  // unit index
@@ -729,18 +730,17 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
     if (tid == 0) sm.flags = 0;
     __syncthreads();
 
-    // ---- 1. request flags ----
+    // ---- 1. request flags (b is a virtual request; the flags belong to the
+    //      request rb and cover all of its query tokens) ----
+    const int rb = b / a.kq, v0 = rb * a.kq;
     uint32_t f = 0;
-    for (int i = tid; i < Hkv; i += NT) {
-        const int ni = a.seq_lens[(long long)b * a.len_sb + (long long)i * a.len_sh];
-        if (ni < 0 || (long long)ni > (long long)a.max_pages * kPage || ni > a.max_seq_len)
-            f |= PFKV_FLAG_BAD_LENGTH;
-    }
+    for (int i = tid; i < Hkv; i += NT)
+        if (query_len(a, v0, i) < 0) f |= PFKV_FLAG_BAD_LENGTH;
     if (a.hflags)
-        for (int i = tid; i < Hkv * a.htiles; i += NT) f |= a.hflags[(long long)b * Hkv * a.htiles + i];
+        for (int i = tid; i < Hkv * a.htiles; i += NT) f |= a.hflags[(long long)rb * Hkv * a.htiles + i];
     if (U > 0) {  // rows of the request's segments (rejected requests have none)
-        for (int it = tid; it < Hkv * nchunks; it += NT) {
-            const int k = b * Hkv * nchunks + it;
+        for (int it = tid; it < a.kq * Hkv * nchunks; it += NT) {
+            const int k = v0 * Hkv * nchunks + it;
             const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
             if (u1 == u0) continue;
             const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
@@ -750,9 +750,9 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
     if (f) atomicOr(&sm.flags, f);
     __syncthreads();
     const uint32_t flags = sm.flags;
-    if (h == 0 && tid == 0 && a.flags) a.flags[b] = (uint8_t)flags;
-    if (h == 0 && tid == 0 && a.rflags) a.rflags[b] = (uint8_t)flags;
-    const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+    if (b == v0 && h == 0 && tid == 0 && a.flags) a.flags[rb] = (uint8_t)flags;
+    if (b == v0 && h == 0 && tid == 0 && a.rflags) a.rflags[rb] = (uint8_t)flags;
+    const int n = max(0, query_len(a, b, h));
     uint2 *out = reinterpret_cast<uint2 *>(a.out + (long long)(b * Hkv + h) * G * D);
     if (flags != 0 || n == 0 || U == 0) {
         for (int i = tid; i < G * D / 4; i += NT) out[i] = make_uint2(0u, 0u);
@@ -919,7 +919,7 @@ bool pers_supported(const DecodePlan &p, int num_pages) {
     const long long rows = (long long)num_pages * p.Hkv * kPage;
     const long long K = (long long)p.B * p.Hkv * p.nchunks;
     return p.dtype == PFKV_KV_FP8_E4M3 && p.D == 128 && p.G <= 4 && rows < (1LL << 31) &&
-           K <= PersCfg<4>::MAXK && p.B <= PersCfg<4>::MAXB;
+           K <= PersCfg<4>::MAXK && p.Breq <= PersCfg<4>::MAXB;
 }
 
 cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {

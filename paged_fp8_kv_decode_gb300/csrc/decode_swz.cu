@@ -137,17 +137,18 @@ __global__ void __launch_bounds__(SwzCfg<G>::NWARPS * 32)
     const int b = bh / Hkv, h = bh - b * Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
-    if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) return;
+    // b is the virtual request (see DecodeArgs::kq)
+    const int n = query_len(a, b, h);
+    if (n < 0) return;
     const int tok0 = chunk * chunk_tokens;
     if (tok0 >= n) return;
-    if (request_rejected_cta(a, b, Hkv)) return;  // rejected by the validation kernel
+    if (request_rejected_cta(a, b / a.kq, Hkv)) return;  // rejected by the validation kernel
     const int tok1 = min(n, tok0 + chunk_tokens);
     const int p_begin = tok0 / kPage;
     const int nunits = (tok1 - tok0 + kPage - 1) / kPage;
     const int ngr = (nunits + C::GU - 1) / C::GU;
     const int nmine = warp < ngr ? (ngr - warp + NW - 1) / NW : 0;
-    const long long bt_row = (long long)b * a.bt_sb + (long long)h * a.bt_sh;
+    const long long bt_row = table_row(a, b, h);
 
     // ---- unit metadata of this warp's granules (page ids gate the copies) ----
     uint32_t bad = 0;

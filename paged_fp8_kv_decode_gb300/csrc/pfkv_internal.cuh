@@ -45,6 +45,7 @@ struct DecodePlan {
     size_t off_hflags, off_status, off_lse, off_o, off_prefix, total;
     bool mass;
     size_t off_mscore, off_lsefin, off_rflags;
+    int Breq, kq;       // requests and query tokens per request (B = Breq * kq)
 };
 
 struct DecodeArgs {
@@ -69,6 +70,11 @@ struct DecodeArgs {
     uint32_t *hflags;   // [B][Hkv][htiles] tag/bounds bits from the validation kernel
     int htiles;
     int fuse_tags;      // compare tags where the split kernels load page ids
+    // query tokens per request (multi-query verify; 1 for plain decode).  The
+    // split and combine kernels see B * kq "virtual requests" v: request
+    // v / kq, query token v % kq, attending to the first n - kq + 1 + v % kq
+    // tokens of each head; q, out and the partial rows are indexed by v.
+    int kq;
     // attention mass (null unless requested)
     float *mscore;      // [B][Hkv][mlen][G] final scores (log2 units) of live tokens
     int mlen;           // = max_seq_len
@@ -117,6 +123,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Tokens of kv head h that virtual request v attends to (see DecodeArgs::kq),
+// or -1 when the request's length is invalid (it is then flagged BAD_LENGTH).
+__device__ __forceinline__ int query_len(const DecodeArgs &a, int v, int h) {
+    const int b = v / a.kq;
+    const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+    if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) return -1;
+    return max(0, n - a.kq + 1 + (v - b * a.kq));
+}
+
+// First block-table entry of kv head h of virtual request v.
+__device__ __forceinline__ long long table_row(const DecodeArgs &a, int v, int h) {
+    return (long long)(v / a.kq) * a.bt_sb + (long long)h * a.bt_sh;
 }
 
 // Status bits of table entry bt_index naming page `id` of kv head h: BAD_PAGE

@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
     assert names == sorted(["pfkv_abi_version", "pfkv_decode_workspace_size", "pfkv_e4m3_decode",
                             "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_paged_decode_attn",
                             "pfkv_paged_decode_attn_fused_tags", "pfkv_paged_decode_attn_mass",
-                            "pfkv_decode_mass_workspace_size",
+                            "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
+                            "pfkv_decode_multi_workspace_size",
                             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
                             "pfkv_status_string", "pfkv_step_graph_create",
                             "pfkv_step_graph_destroy", "pfkv_step_graph_launch"])
@@ -171,6 +172,23 @@ def test_mass_entry_checks_arguments(B):
     assert mass(sb=-1) == 1
     assert mass(opts=0x2) == 1
     assert mass(Hq=6) == 2
+
+
+def test_multi_entry_checks_arguments(B):
+    c, p = _structs(B)
+    L = B.lib()
+    def multi(kq=3, opts=0, Hq=4, ws=0xB0000):
+        return L.pfkv_paged_decode_attn_multi(ctypes.byref(c), ctypes.byref(p), 0xA0000, Hq, kq,
+                                              0.125, 0, 64, ws, 1 << 30, 0xC0000, None, opts,
+                                              None)
+    assert multi(kq=0) == 1
+    assert multi(kq=-2) == 1
+    assert multi(opts=0x1) == 1
+    assert multi(Hq=6) == 2
+    assert multi(ws=None) == 4
+    n = ctypes.c_size_t(0)
+    assert L.pfkv_decode_multi_workspace_size(ctypes.byref(c), ctypes.byref(p), 4, 0, 0, 64,
+                                              ctypes.byref(n)) == 1
 
 
 def test_empty_batch_is_a_no_op(B):
