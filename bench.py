@@ -282,6 +282,7 @@ def run_gpu(args):
         if args.no_tags:
             spec.tags = False
         db = DeviceBatch(W.make_batch(spec), device=dev)
+        db.pack_step_io()  # one host-to-device and one device-to-host copy per e2e step
         reps.append(PreparedStep(db, B, sh, fused_tags=args.fused_tags))
     torch.cuda.synchronize()
     spec0 = reps[0].db.spec
@@ -398,28 +399,37 @@ def run_gpu(args):
 def run_e2e(args, reps, B, stream, step_bytes, world, dev):
     """Same metric through the public API with host buffers: each step copies
     its inputs (q, new K/V rows, positions, lengths, block table, expected
-    tags) from pinned host memory, runs append + attention, and reads the
-    output and flags back."""
+    tags: packed in one buffer) from pinned host memory, runs append +
+    attention, and reads the output and flags (one buffer) back."""
     import torch
     K = max(1, min(args.e2e_steps, args.steps))
     host = []
     for p in reps:
         db = p.db
-        tensors_in = [db.q, db.positions, db.seq_lens, db.block_tables]
-        if db.spec.append:
-            tensors_in += [db.k_new, db.v_new]
-        if db.cache.page_tags is not None:
-            tensors_in.append(db.expected_tags)
+        tensors_in, tensors_out = [db.io_in], [db.io_out]
         h_in = [t.detach().cpu().pin_memory() for t in tensors_in]
-        h_out = [torch.empty_like(db.out, device="cpu").pin_memory(),
-                 torch.empty_like(db.flags, device="cpu").pin_memory()]
-        host.append((tensors_in, h_in, h_out))
-    h2d = sum(t.numel() * t.element_size() for t in host[0][1])
-    d2h = sum(t.numel() * t.element_size() for t in host[0][2])
+        h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in tensors_out]
+        host.append((tensors_in, h_in, h_out, tensors_out))
+    # one single-layer step graph per replica: the step (append + attention)
+    # is then one launch through the public API
+    graphs = []
+    for p in reps:
+        db = p.db
+        layer = B.Layer(cache=db.cache, q=db.q, out=db.out, k_new=db.k_new, v_new=db.v_new,
+                        flags=db.flags)
+        graphs.append(B.pfkv_step_graph_create(
+            [layer], db.pages, db.positions, None, 1 if db.spec.append else 0, db.append_flags,
+            db.spec.Hq, db.spec.sm_scale, db.split_tokens, db.max_seq_len, db.workspace,
+            B.PFKV_STAGE_FUSED_TAGS if args.fused_tags else 0))
+    # bytes the step's tensors hold (the packing's alignment padding excluded)
+    db0 = reps[0].db
+    h2d = sum(t.numel() * t.element_size() for t in
+              [db0.q, db0.positions, db0.seq_lens, db0.block_tables]
+              + ([db0.k_new, db0.v_new] if db0.spec.append else [])
+              + ([db0.expected_tags] if db0.cache.page_tags is not None else []))
+    d2h = db0.out.numel() * db0.out.element_size() + db0.flags.numel()
     for i in range(5):
-        p = reps[i % len(reps)]
-        p.append()
-        p.stage(B.PFKV_STAGE_ALL)
+        graphs[i % len(reps)].launch(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -427,19 +437,22 @@ def run_e2e(args, reps, B, stream, step_bytes, world, dev):
     for i in range(K):
         r = i % len(reps)
         p = reps[r]
-        d_in, h_in, h_out = host[r]
+        d_in, h_in, h_out, d_out = host[r]
         for d, h in zip(d_in, h_in):
             d.copy_(h, non_blocking=True)
-        p.append()
-        p.stage(B.PFKV_STAGE_ALL)
-        h_out[0].copy_(p.db.out, non_blocking=True)
-        h_out[1].copy_(p.db.flags, non_blocking=True)
+        graphs[r].launch(stream)
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
         stream.synchronize()
     el = time.perf_counter() - t0
     el = reduce_max(el, world, dev)
+    for g in graphs:
+        g.close()
     return {"value": round(aggregate(step_bytes, K, el, world), 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K,
-            "ms_per_step": round(el / K * 1e3, 4)}
+            "ms_per_step": round(el / K * 1e3, 4),
+            "api": "inputs and outputs packed (one copy each way); the step is one "
+                   "pfkv_step_graph_launch of a 1-layer graph"}
 
 
 # --------------------------------------------------------------------------
@@ -626,6 +639,7 @@ def run_workload(args):
     sh = stream.cuda_stream
     spec = workload_spec(args, rank)
     db = DeviceBatch(W.make_batch(spec), device=dev)
+    db.pack_step_io()  # one host-to-device and one device-to-host copy per e2e step
     variants = [("tags" if spec.tags else "no_tags", PreparedStep(db, B, sh), spec.tags)]
     if args.workload == "evict":
         # every live unit carrying the tag its request expects (no request aborted)
@@ -776,14 +790,14 @@ def run_e2e_flushed(args, p, B, stream, step_bytes, world, dev, flush):
     import torch
     K = max(1, min(args.e2e_steps, args.steps))
     db = p.db
-    d_in = [db.q, db.positions, db.seq_lens, db.block_tables]
-    if db.spec.append:
-        d_in += [db.k_new, db.v_new]
-    if db.cache.page_tags is not None:
-        d_in.append(db.expected_tags)
+    d_in, d_out = [db.io_in], [db.io_out]
     h_in = [t.detach().cpu().pin_memory() for t in d_in]
-    h_out = [torch.empty_like(db.out, device="cpu").pin_memory(),
-             torch.empty_like(db.flags, device="cpu").pin_memory()]
+    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in d_out]
+    h2d = sum(t.numel() * t.element_size() for t in
+              [db.q, db.positions, db.seq_lens, db.block_tables]
+              + ([db.k_new, db.v_new] if db.spec.append else [])
+              + ([db.expected_tags] if db.cache.page_tags is not None else []))
+    d2h = db.out.numel() * db.out.element_size() + db.flags.numel()
     total = 0.0
     for i in range(K + 2):
         flush()
@@ -793,15 +807,14 @@ def run_e2e_flushed(args, p, B, stream, step_bytes, world, dev, flush):
             d.copy_(h, non_blocking=True)
         p.append()
         p.stage(B.PFKV_STAGE_ALL)
-        h_out[0].copy_(db.out, non_blocking=True)
-        h_out[1].copy_(db.flags, non_blocking=True)
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
         stream.synchronize()
         if i >= 2:
             total += time.perf_counter() - t0
     total = reduce_max(total, world, dev)
     return {"value": round(aggregate(step_bytes, K, total, world), 2), "unit": UNIT,
-            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_in)),
-            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out)),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": K, "ms_per_step": round(total / K * 1e3, 4)}
 
 

@@ -101,6 +101,40 @@ class DeviceBatch:
             raise RuntimeError(f"fill flagged requests: {self.append_flags.tolist()}")
 
     # ------------------------------------------------------------------
+    def pack_step_io(self):
+        """Move the tensors a decode step takes from the host (q, the new K/V
+        rows, positions, lengths, block table, expected tags) into one device
+        buffer, ``io_in``, and the step's outputs (out, flags) into another,
+        ``io_out``, keeping their contents; a caller then moves each direction
+        with one copy.  Call before taking pointers of these tensors."""
+        spec = self.spec
+        names = ["q", "positions", "seq_lens", "block_tables"]
+        if spec.append:
+            names += ["k_new", "v_new"]
+        if self.pages.expected_tags is not None:
+            names.append("expected_tags")
+        self.io_in = self._pack(names)
+        self.io_out = self._pack(["out", "flags"])
+        sb, sh = self.batch.len_strides
+        tb, th = self.batch.bt_strides
+        self.pages = B.Pages(spec.B, self.batch.max_pages, self.block_tables, tb, th,
+                             self.seq_lens, sb, sh,
+                             self.expected_tags if self.pages.expected_tags is not None else None)
+
+    def _pack(self, names):
+        sizes = [getattr(self, n).numel() * getattr(self, n).element_size() for n in names]
+        offs, off = [], 0
+        for n in sizes:
+            offs.append(off)
+            off += (n + 255) // 256 * 256
+        buf = torch.empty(max(off, 256), dtype=torch.uint8, device=self.device)
+        for n, o, size in zip(names, offs, sizes):
+            old = getattr(self, n)
+            view = buf[o:o + size].view(old.dtype).view(old.shape)
+            view.copy_(old)
+            setattr(self, n, view)
+        return buf
+
     def append_step(self, stream=None):
         if self.spec.append:
             B.pfkv_kv_append(self.cache, self.pages, self.positions, self.k_new, self.v_new,

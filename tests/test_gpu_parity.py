@@ -228,3 +228,24 @@ def test_many_segments_fallback_path(B):
     spec = W.Spec("manyseg", B=3, Hq=32, Hkv=8, D=128, kv_dtype="fp8", num_pages=1024,
                   lens=lens, tags=True, split_tokens=16, seed=404)
     run_and_compare(spec, label="many-segments")
+
+
+def test_packed_step_io_gives_the_same_outputs(B):
+    """DeviceBatch.pack_step_io moves the step's inputs and outputs into two
+    buffers (one copy each way for an end-to-end caller); the step's results
+    are unchanged."""
+    spec = W.spec_llama8b("small")
+    db = _db(W.make_batch(spec))
+    out0 = db.out.clone()
+    db.step()
+    torch.cuda.synchronize()
+    want = db.out.clone()
+    pool_k = db.cache.k_pages.clone()
+    db.pack_step_io()
+    db.out.copy_(out0)
+    db.step()   # the append rewrites the same slots with the same values
+    torch.cuda.synchronize()
+    assert torch.equal(db.out, want)
+    assert torch.equal(db.cache.k_pages, pool_k)
+    assert db.io_in.data_ptr() <= db.q.data_ptr() < db.io_in.data_ptr() + db.io_in.numel()
+    assert db.io_out.data_ptr() <= db.flags.data_ptr() < db.io_out.data_ptr() + db.io_out.numel()
