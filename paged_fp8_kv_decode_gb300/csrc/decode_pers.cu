@@ -149,7 +149,10 @@ __device__ __forceinline__ int seg_of(const int *prefix, int K, int x) {
     return lo;
 }
 
-template <int G>
+// MASS: also store every live token's final scores for the attention-mass
+// pass (a separate instantiation, so that the plain kernel carries no trace of
+// it in its inner loop).
+template <int G, bool MASS>
 __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     decode_split_pers_kernel(DecodeArgs a, int Hkv, int B, int nchunks, int chunk_tokens,
                              int *ws_prefix) {
@@ -555,7 +558,7 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) sc[g] = ok ? sc[g] * ksc : -INFINITY;
-            if (a.mscore && ok) {  // scores for the attention-mass pass
+            if (MASS && ok) {  // scores for the attention-mass pass
                 const int bh = con.k / nchunks, c = con.k - bh * nchunks;
                 const int page = c * (chunk_tokens / kPage) + (con.x + my_u - sm.prefix[con.k]);
                 store_scores<G>(a, bh, page * kPage + my_row, sc);
@@ -892,8 +895,8 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
 // --------------------------------------------------------------------------
 namespace {
 
-template <int G>
-cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+template <int G, bool MASS>
+cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     using C = PersCfg<G>;
     const size_t smem = sizeof(typename C::Smem) + 1024;
     static std::atomic<unsigned long long> configured{0};
@@ -902,13 +905,18 @@ cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(decode_split_pers_kernel<G>,
+        e = cudaFuncSetAttribute(decode_split_pers_kernel<G, MASS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    return launch_pdl(decode_split_pers_kernel<G>, dim3(p.pers_ctas), dim3(C::NT), smem, s, a,
-                      p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
+    return launch_pdl(decode_split_pers_kernel<G, MASS>, dim3(p.pers_ctas), dim3(C::NT), smem, s,
+                      a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
+}
+
+template <int G>
+cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    return a.mscore ? launch_pers_gm<G, true>(a, p, s) : launch_pers_gm<G, false>(a, p, s);
 }
 
 }  // namespace

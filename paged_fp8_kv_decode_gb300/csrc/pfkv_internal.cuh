@@ -128,7 +128,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Tokens of kv head h that virtual request v attends to (see DecodeArgs::kq),
 // or -1 when the request's length is invalid (it is then flagged BAD_LENGTH).
 __device__ __forceinline__ int query_len(const DecodeArgs &a, int v, int h) {
-    const int b = v / a.kq;
+    const int b = a.kq == 1 ? v : v / a.kq;
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
     if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) return -1;
     return max(0, n - a.kq + 1 + (v - b * a.kq));
@@ -136,7 +136,7 @@ __device__ __forceinline__ int query_len(const DecodeArgs &a, int v, int h) {
 
 // First block-table entry of kv head h of virtual request v.
 __device__ __forceinline__ long long table_row(const DecodeArgs &a, int v, int h) {
-    return (long long)(v / a.kq) * a.bt_sb + (long long)h * a.bt_sh;
+    return (long long)(a.kq == 1 ? v : v / a.kq) * a.bt_sb + (long long)h * a.bt_sh;
 }
 
 // Status bits of table entry bt_index naming page `id` of kv head h: BAD_PAGE
