@@ -686,17 +686,17 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
 
 // --------------------------------------------------------------------------
 // combine for the persistent layout: the rows of segment k are k + p for the
-// workers p that touched it.  One CTA of 8 warps per (request b, kv head h):
+// workers p that touched it.  One CTA of 16 warps per (request b, kv head h):
 //  1. the request's flags: lengths and validation bits of every kv head and
 //     the status rows of every segment of the request, in parallel;
 //  2. the rows of (b, h), flattened: chunk c owns rows [cstart[c], cstart[c+1])
 //     of the flat order, the first at workspace row cbase[c];
 //  3. M = max lse per query head, over all rows, in parallel;
-//  4. each warp accumulates exp2(lse - M)-weighted rows j = warp, warp + 8, ...
+//  4. each warp accumulates exp2(lse - M)-weighted rows j = warp, warp + 16, ...
 //     (lane l owns dims [4l, 4l + 4) of every query head of the group);
 //  5. the warps' sums meet in shared memory; out = sum / weight, bf16.
 // --------------------------------------------------------------------------
-constexpr int kCombThreads = 256;
+constexpr int kCombThreads = 512;
 constexpr int kCombWarps = kCombThreads / 32;
 constexpr int kCombMaxChunks = PersCfg<1>::MAXK;  // segments per (b, h) <= all segments
 
@@ -715,6 +715,7 @@ struct CombSmem {
     int part[kCombThreads];
     float mred[kCombWarps][G];
     uint32_t flags;
+    int ndef;  // segments with long row lists, gathered a warp each
 };
 
 template <int G>
@@ -730,7 +731,10 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
     const int K = B * Hkv * nchunks;
     const int U = ws_prefix[K];
     W = min(W, U);  // as in the split kernel
-    if (tid == 0) sm.flags = 0;
+    if (tid == 0) {
+        sm.flags = 0;
+        sm.ndef = 0;
+    }
     __syncthreads();
 
     // ---- 1. request flags (b is a virtual request; the flags belong to the
@@ -741,14 +745,30 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
         if (query_len(a, v0, i) < 0) f |= PFKV_FLAG_BAD_LENGTH;
     if (a.hflags)
         for (int i = tid; i < Hkv * a.htiles; i += NT) f |= a.hflags[(long long)rb * Hkv * a.htiles + i];
-    if (U > 0) {  // rows of the request's segments (rejected requests have none)
+    // rows of the request's segments (rejected requests have none): a thread
+    // per segment; a segment with many rows (few long segments, many workers
+    // each) is deferred to a warp whose lanes take its rows.  The deferred
+    // list borrows the row tables' space, which phase 2 fills later.
+    if (U > 0) {
         for (int it = tid; it < a.kq * Hkv * nchunks; it += NT) {
             const int k = v0 * Hkv * nchunks + it;
             const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
             if (u1 == u0) continue;
             const int p0 = worker_of(u0, U, W), p1 = worker_of(u1 - 1, U, W);
-            for (int p = p0; p <= p1; ++p) f |= a.status[k + p];
+            if (p1 - p0 < 8) {
+                for (int p = p0; p <= p1; ++p) f |= a.status[k + p];
+            } else {
+                sm.u.rows.cbase[atomicAdd(&sm.ndef, 1)] = k;
+            }
         }
+    }
+    if (f) atomicOr(&sm.flags, f);
+    __syncthreads();
+    f = 0;
+    for (int d = warp; d < sm.ndef; d += NW) {
+        const int k = sm.u.rows.cbase[d];
+        const int p0 = worker_of(ws_prefix[k], U, W), p1 = worker_of(ws_prefix[k + 1] - 1, U, W);
+        for (int p = p0 + lane; p <= p1; p += 32) f |= a.status[k + p];
     }
     if (f) atomicOr(&sm.flags, f);
     __syncthreads();
@@ -843,7 +863,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
         acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
         wsum[g] = 0.f;
     }
-#pragma unroll 2
+#pragma unroll 4
     for (int j = warp; j < R; j += NW) {
         const long long row = row_of(j);
 #pragma unroll
@@ -881,8 +901,12 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
             ws += sm.u.red.wsum[w2][g];
         }
         const float inv = ws > 0.f ? 1.f / ws : 0.f;
-        if (a.lse_fin && d4 == 0)
-            a.lse_fin[(long long)(b * Hkv + h) * G + g] = ws > 0.f ? M[g] + plog2(ws) : -INFINITY;
+        if (a.lse_fin && d4 == 0) {
+            float Mg = M[0];  // M[g] without a dynamically indexed register array
+#pragma unroll
+            for (int x = 1; x < G; ++x) Mg = g == x ? M[x] : Mg;
+            a.lse_fin[(long long)(b * Hkv + h) * G + g] = ws > 0.f ? Mg + plog2(ws) : -INFINITY;
+        }
         const __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x * inv, s4.y * inv);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z * inv, s4.w * inv);
         out[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
