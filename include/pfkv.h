@@ -404,6 +404,18 @@ pfkv_status pfkv_step_graph_launch(pfkv_step_graph *graph, void *stream);
 pfkv_status pfkv_step_graph_destroy(pfkv_step_graph *graph);
 
 /*
+ * pfkv_selftest_bounded_wait -- runs the bounded device-side wait that every
+ * kernel of the library uses on its shared-memory barriers, twice, in one
+ * warp: first on a barrier phase that nothing completes, which must give up
+ * after the library's wait limit (100 ms) instead of hanging; then on a phase
+ * that completes, which must succeed.  *result (device, 4-byte aligned)
+ * receives PFKV_FLAG_DEVICE_TIMEOUT if the first wait gave up, | 0x100 if the
+ * second one succeeded: 0x108 on a working device.  The context stays usable.
+ * (A check of the failure path, not part of the method.)
+ */
+pfkv_status pfkv_selftest_bounded_wait(uint32_t *result, void *stream);
+
+/*
  * pfkv_e4m3_encode -- out[i] = e4m3 code of x[i] (fp32), round to nearest
  * even, saturating to +-448, NaN -> 0x7F: the conversion kv_append uses.
  * x: fp32 [n], out: uint8 [n] (device).  n >= 0.

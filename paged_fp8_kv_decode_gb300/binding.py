@@ -46,7 +46,7 @@ EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_a
             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_mass",
             "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
             "pfkv_decode_multi_workspace_size", "pfkv_step_graph_create", "pfkv_step_graph_launch",
-            "pfkv_step_graph_destroy", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string",
+            "pfkv_step_graph_destroy", "pfkv_selftest_bounded_wait", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string",
             "pfkv_abi_version")
 
 
@@ -137,6 +137,8 @@ def lib() -> ctypes.CDLL:
         L.pfkv_step_graph_launch.restype = ctypes.c_int
         L.pfkv_step_graph_destroy.argtypes = [P]
         L.pfkv_step_graph_destroy.restype = ctypes.c_int
+        L.pfkv_selftest_bounded_wait.argtypes = [P, P]
+        L.pfkv_selftest_bounded_wait.restype = ctypes.c_int
         L.pfkv_e4m3_encode.argtypes = [P, I64, P, P]
         L.pfkv_e4m3_encode.restype = ctypes.c_int
         L.pfkv_e4m3_decode.argtypes = [P, I64, P, P]
@@ -432,6 +434,12 @@ def pfkv_step_graph_launch(graph: StepGraph, stream=None) -> None:
 
 def pfkv_step_graph_destroy(graph: StepGraph) -> None:
     graph.close()
+
+
+def pfkv_selftest_bounded_wait(result: torch.Tensor, stream=None) -> None:
+    """result: int32 CUDA tensor of >= 1 element (see include/pfkv.h)."""
+    _check(lib().pfkv_selftest_bounded_wait(_ptr(result), _stream(stream)),
+           "pfkv_selftest_bounded_wait")
 
 
 def pfkv_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:

@@ -35,7 +35,7 @@ def test_header_declares_the_entry_points():
                             "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
                             "pfkv_decode_multi_workspace_size",
                             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
-                            "pfkv_status_string", "pfkv_step_graph_create",
+                            "pfkv_status_string", "pfkv_selftest_bounded_wait", "pfkv_step_graph_create",
                             "pfkv_step_graph_destroy", "pfkv_step_graph_launch"])
 
 
@@ -189,6 +189,11 @@ def test_multi_entry_checks_arguments(B):
     n = ctypes.c_size_t(0)
     assert L.pfkv_decode_multi_workspace_size(ctypes.byref(c), ctypes.byref(p), 4, 0, 0, 64,
                                               ctypes.byref(n)) == 1
+
+
+def test_selftest_checks_its_pointer(B):
+    assert B.lib().pfkv_selftest_bounded_wait(None, None) == 1
+    assert B.lib().pfkv_selftest_bounded_wait(0x1002, None) == 3
 
 
 def test_empty_batch_is_a_no_op(B):
