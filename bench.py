@@ -68,6 +68,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the raw nvidia-smi clock samples at this path (the JSON line "
+                         "carries their summary either way)")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "long", "sweep", "evict"],
                     help="llama8b (default): the Llama-shaped layer; the others are the "
@@ -116,6 +119,18 @@ def aggregate(bytes_per_step_per_rank: float, steps: int, seconds_max: float, wo
 # --------------------------------------------------------------------------
 # clocks
 # --------------------------------------------------------------------------
+def clocks_path(args) -> str:
+    """Where the raw clock samples go: --clocks-csv, else a temporary file."""
+    if args.clocks_csv:
+        d = os.path.dirname(os.path.abspath(args.clocks_csv))
+        os.makedirs(d, exist_ok=True)
+        return args.clocks_csv
+    import tempfile
+    fd, path = tempfile.mkstemp(prefix="pfkv_clocks_", suffix=".csv")
+    os.close(fd)
+    return path
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -321,8 +336,7 @@ def run_gpu(args):
     t1 = torch.cuda.Event(enable_timing=True)
     sampler = None
     if rank == 0 and not args.no_clocks:
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler = ClockSampler(local, clocks_path(args))
         sampler.start()
         time.sleep(0.3)
     if world > 1:
@@ -699,8 +713,7 @@ def run_workload(args):
                     + (spec.B * spec.Hkv * 8 if spec.kv_dtype == "fp8" else 0)) if spec.append else 0
     sampler = None
     if rank == 0 and not args.no_clocks:
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler = ClockSampler(local, clocks_path(args))
         sampler.start()
         time.sleep(0.3)
     if world > 1:
@@ -865,8 +878,7 @@ def run_graph(args):
            for _ in range(K)]
     sampler = None
     if rank == 0 and not args.no_clocks:
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler = ClockSampler(local, clocks_path(args))
         sampler.start()
         time.sleep(0.3)
     if world > 1:
@@ -981,8 +993,7 @@ def run_multi(args):
     K = args.steps
     sampler = None
     if rank == 0 and not args.no_clocks:
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv"))
+        sampler = ClockSampler(local, clocks_path(args))
         sampler.start()
         time.sleep(0.3)
     if world > 1:

@@ -64,3 +64,30 @@ def test_aborted_requests_drop_their_kv_and_scales_but_not_their_tags():
     kv1 = int(lens[1].sum()) * spec.D * 2
     assert full - part == kv1 + 8 * int(pages[1].sum())
     assert db.algorithmic_bytes(tags=False) == full - 8 * int(pages.sum())
+
+
+def test_clock_summary_reads_load_samples_and_throttle_reasons(tmp_path):
+    """nvidia-smi rows (index, sm MHz, max MHz, power W, active mask, hw_slowdown,
+    hw_thermal, sw_thermal, sw_power_cap): the median SM clock is taken over
+    the samples under load (above 200 W), reasons over the same samples."""
+    p = tmp_path / "clocks.csv"
+    p.write_text("\n".join([
+        "0, 2070, 2070, 90.0, 0x0, Not Active, Not Active, Not Active, Not Active",   # idle
+        "0, 2070, 2070, 650.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1995, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2055, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]) + "\n")
+    s = bench.ClockSampler(0, str(p)).summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2055.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1390.0
+
+
+def test_clocks_path_defaults_to_a_temporary_file(tmp_path):
+    a = bench.parse_args([])
+    path = bench.clocks_path(a)
+    assert os.path.exists(path) and "pfkv_clocks_" in os.path.basename(path)
+    os.remove(path)
+    a = bench.parse_args(["--clocks-csv", str(tmp_path / "sub" / "c.csv")])
+    assert bench.clocks_path(a) == str(tmp_path / "sub" / "c.csv")
+    assert os.path.isdir(tmp_path / "sub")
