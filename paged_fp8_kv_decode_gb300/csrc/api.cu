@@ -50,6 +50,8 @@ pfkv_status check_cache(const pfkv_cache *c) {
     if (c->head_dim != 64 && c->head_dim != 128) return PFKV_ERR_UNSUPPORTED;
     if (c->dtype != PFKV_KV_BF16 && c->dtype != PFKV_KV_FP8_E4M3) return PFKV_ERR_INVALID_ARG;
     if (c->num_pages <= 0 || c->num_kv_heads <= 0) return PFKV_ERR_INVALID_ARG;
+    // unit indices page * num_kv_heads + h are 32-bit in the kernels
+    if ((long long)c->num_pages * c->num_kv_heads > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
     if (!c->k_pages || !c->v_pages) return PFKV_ERR_INVALID_ARG;
     if (c->dtype == PFKV_KV_FP8_E4M3 && (!c->k_scale || !c->v_scale)) return PFKV_ERR_INVALID_ARG;
     if (!aligned(c->k_pages, 16) || !aligned(c->v_pages, 16)) return PFKV_ERR_ALIGNMENT;
