@@ -4,7 +4,8 @@
 //
 // What is computed is the attention of decode.cu (single query per head over
 // the tokens its kv head holds, read through the block table from the FP8
-// pool); this file changes how the work is cut and fed:
+// pool); this file changes how the work is cut and fed, and moves both
+// contractions onto the tensor cores:
 //
 // Segments and balanced ranges.  A segment is one (request b, kv head h,
 // chunk c) — c is always 0 unless the caller fixes a split size.  Every CTA
@@ -16,25 +17,30 @@
 // partial row (normalised output and log2-sum-exp per query head) for every
 // segment it touches, at row index segment + worker, which is unique.
 //
-// Workers.  A worker is a pair of warps sharing a 3-stage shared-memory ring
-// (8 KB per stage: K and V slabs of a 2-unit granule, each slab one 2 KB 1-D
-// bulk copy; a quarter-warp reads one 128-byte row, so the linear layout is
-// free of bank conflicts):
-//  * the score warp holds a 16-dim slice of the G query heads in registers
-//    (lane (t, c): slice c, row 4r + t of a unit in pass r), converts K bytes
-//    to fp32 pairs, takes packed fp32x2 dot products, finishes each score with
-//    a select-free reduce-scatter over the 8 lanes of a token group (so lane
-//    (t, c) ends with the G scores of token 4c + t) and hands the value warp
-//    the raw scores;
-//  * the value warp keeps a window of unit metadata (page id, K and V scales,
-//    bad-id bit) for the next 64 units in registers, turns the raw scores into
-//    probabilities (online softmax per granule, lazy rescale), accumulates
-//    its 16-dim slice of the output in registers, writes the partial row at
-//    the end of each segment, and refills the stage it has just finished
-//    with the bulk copies of the granule ST ahead.
-// Splitting scores and values over two warps halves the registers each needs,
-// so 12 warps fit an SM, and the two phases of neighbouring granules overlap.
+// Workers.  A worker is one warp with a 3-stage shared-memory ring of 8 KB
+// granules (K and V slabs of two units).  Each slab arrives by one TMA tensor
+// copy with the 128-byte swizzle (16-byte chunk c of row r lands at chunk
+// c ^ (r & 7)), which makes every fragment load below free of bank conflicts.
+// Per unit of 16 tokens the warp
+//  * takes the scores S = K Q^T as eight m16n8k16 MMAs (f16 operands, fp32
+//    accumulation): the 16 tokens are the M rows, the G query heads the N
+//    columns (zero-padded to 8), the 128 dims the reduction.  e4m3 bytes
+//    become f16 A fragments with one conversion per register (every e4m3
+//    value is exact in f16); Q sits in registers as f16 B fragments, scaled
+//    by a power of two so that its largest element lies in [1, 2);
+//  * runs the online softmax on the accumulator fragment (lane (g, t) holds
+//    tokens g and g + 8 of heads 2t and 2t + 1), with a lazy rescale;
+//  * accumulates O^T = V^T P^T as eight MMAs: the 128 dims are the M rows (in
+//    eight tiles), tokens the reduction, heads the columns.  A byte permute
+//    pairs two tokens of one dim, the conversion makes the A fragment, and the
+//    probabilities, times the unit's V scale over a power-of-two reference,
+//    become f16 B fragments through four shuffles.
+// The dims of the score reduction are taken in a permuted order (lane t owns
+// dims [32t, 32t + 32) of both K and Q), which changes nothing in the sum.
 #include <atomic>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "pfkv_internal.cuh"
 
@@ -54,43 +60,66 @@ __device__ __forceinline__ float plog2(float x) {
     return y;
 }
 
-__device__ __forceinline__ float pwarp_max(float x) {
-    float m;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(x));
-    return m;
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ void named_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-__device__ __forceinline__ void pdequant4(uint32_t w, float2 &lo, float2 &hi) {
-    asm("{\n\t.reg .b16 l, h, a0, a1, b0, b1;\n\t.reg .b32 x, y;\n\t"
-        "mov.b32 {l, h}, %4;\n\t"
-        "cvt.rn.f16x2.e4m3x2 x, l;\n\t"
-        "cvt.rn.f16x2.e4m3x2 y, h;\n\t"
-        "mov.b32 {a0, a1}, x;\n\t"
-        "mov.b32 {b0, b1}, y;\n\t"
-        "cvt.f32.f16 %0, a0;\n\t"
-        "cvt.f32.f16 %1, a1;\n\t"
-        "cvt.f32.f16 %2, b0;\n\t"
-        "cvt.f32.f16 %3, b1;\n\t}"
-        : "=f"(lo.x), "=f"(lo.y), "=f"(hi.x), "=f"(hi.y)
+// four e4m3 codes -> two f16 pairs (bytes 0, 1 -> lo; bytes 2, 3 -> hi; the
+// lower byte of each pair lands in the lower half)
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
         : "r"(w));
 }
 
-__device__ __forceinline__ void pdequant16(const uint4 w, float2 (&f)[8]) {
-    pdequant4(w.x, f[0], f[1]);
-    pdequant4(w.y, f[2], f[3]);
-    pdequant4(w.z, f[4], f[5]);
-    pdequant4(w.w, f[6], f[7]);
+// D += A B for one 16x8x16 tile: f16 A (row-major fragment), f16 B
+// (column-major fragment), fp32 accumulators
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-constexpr float kLazy = 8.0f;  // rescale only when the max grows by > 2^8
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) {
+    return *reinterpret_cast<const uint4 *>(p);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// 2^e as fp32 for e in [-126, 127]
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// smallest e with x < 2^e for finite x > 0 (-126 for zero and subnormals),
+// clamped to 126
+__device__ __forceinline__ int exp_above(float x) {
+    const int eb = (int)((__float_as_uint(x) >> 23) & 0xffu);
+    return min(126, max(eb, 0) - 126);
+}
+
+// TMA: one 16-row x 128-byte box of a pool (rows = units x 16) into shared
+// memory, 128-byte swizzled, completing its bytes on `bar`
+__device__ __forceinline__ void tma_unit(void *dst, const CUtensorMap *map, int row, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+constexpr float kLazy = 8.0f;   // rescale only when the max grows by > 2^8
+constexpr int kNoScale = -1000; // V-scale reference of a worker that has seen no unit yet
 
 // worker of global unit x when U units are shared by W workers (see header)
 __device__ __forceinline__ int worker_of(long long x, long long U, int W) {
@@ -99,37 +128,19 @@ __device__ __forceinline__ int worker_of(long long x, long long U, int W) {
 
 }  // namespace
 
-template <int G>
 struct PersCfg {
     static constexpr int D = 128;
     static constexpr int ROWB = 128;
     static constexpr int UNITB = kPage * ROWB;   // 2 KB
-    static constexpr int GT = 32;                // tokens per granule (2 units)
     static constexpr int STAGEB = 4 * UNITB;     // K u0 | K u1 | V u0 | V u1
-    static constexpr int PAIRS = 6;
+    static constexpr int WORKERS = 8;
     static constexpr int STAGES = 3;
-    static constexpr int NT = PAIRS * 64;
+    static constexpr int NT = WORKERS * 32;
     static constexpr int MAXK = 4096;            // segments (prefix array in smem)
     static constexpr int MAXB = 4096;            // requests
-    // raw scores of one granule, row = the writing lane (lane (t, c) holds
-    // token 4c + t), handed from the score warp to the value warp
-    struct alignas(16) SBuf {
-        float s[GT][G];
-    };
-    struct Pair {
-        alignas(1024) uint8_t ring[STAGES][STAGEB];
-        alignas(16) SBuf sb[STAGES];
-        alignas(16) float p[GT][2 * G];   // value warp: probability x V scale, as pairs
-        alignas(16) __nv_bfloat16 q[2][G][D];
-        alignas(8) uint64_t full[STAGES];
-        alignas(8) uint64_t sready[STAGES];
-        alignas(8) uint64_t qbar[2];
-        int ngran;
-        uint32_t score_status;            // timeouts seen by the score warp
-    };
-    static_assert(sizeof(SBuf) % 16 == 0, "vector stores into every stage buffer");
     struct Smem {
-        Pair pair[PAIRS];
+        alignas(1024) uint8_t ring[WORKERS][STAGES][STAGEB];
+        alignas(8) uint64_t full[WORKERS][STAGES];
         int prefix[MAXK + 1];
         int part[NT];
         uint8_t rflag[MAXB];
@@ -153,11 +164,13 @@ __device__ __forceinline__ int seg_of(const int *prefix, int K, int x) {
 // pass (a separate instantiation, so that the plain kernel carries no trace of
 // it in its inner loop).
 template <int G, bool MASS>
-__global__ void __launch_bounds__(PersCfg<G>::NT, 1)
-    decode_split_pers_kernel(DecodeArgs a, int Hkv, int B, int nchunks, int chunk_tokens,
-                             int *ws_prefix) {
-    using C = PersCfg<G>;
+__global__ void __launch_bounds__(PersCfg::NT, 1)
+    decode_split_pers_kernel(const __grid_constant__ CUtensorMap tmk,
+                             const __grid_constant__ CUtensorMap tmv, DecodeArgs a, int Hkv, int B,
+                             int nchunks, int chunk_tokens, int *ws_prefix) {
+    using C = PersCfg;
     constexpr int ST = C::STAGES;
+    static_assert(G == 1 || G == 2 || G == 4, "query groups of 1, 2 or 4 heads");
     extern __shared__ uint8_t smem_raw[];
     typename C::Smem &sm = *reinterpret_cast<typename C::Smem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -225,26 +238,24 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
     const int U = sm.prefix[K];  // unit counts stay far below 2^31 (rows < 2^31 / 16)
     // never more workers than units: every worker then owns at least one unit,
     // so all workers between a segment's first and last unit write its rows
-    const int W = min((int)gridDim.x * C::PAIRS, U);
+    const int W = min((int)gridDim.x * C::WORKERS, U);
     if (blockIdx.x == 0) {
         for (int k = tid; k <= K; k += C::NT) ws_prefix[k] = sm.prefix[k];
     }
     if (U == 0) return;
 
-    // ---------------- the worker ----------------
-    // Warps map to the SM's four sub-partitions by warp index mod 4; score
-    // warps are 0..PAIRS-1 and value warps PAIRS..2*PAIRS-1 so that the
-    // FMA-heavy score warps spread over all four sub-partitions.
+    // ---------------- the worker: one warp ----------------
     const int warp = tid >> 5, lane = tid & 31;
-    const int pi = warp % C::PAIRS;     // pair index in the CTA
-    const bool is_score = warp < C::PAIRS;
-    typename C::Pair &P = sm.pair[pi];
-    const int w = blockIdx.x * C::PAIRS + pi;
+    const int w = blockIdx.x * C::WORKERS + warp;
     const int x0 = w < W ? (int)(((long long)w * U + W - 1) / W) : U;
     const int x1 = w < W ? (int)(((long long)(w + 1) * U + W - 1) / W) : U;
-    const int vt = lane >> 3, vc = lane & 7;
+    if (x0 >= x1) return;  // no block-wide barrier follows
+    // fragment coordinates: lane (g, t) = (lane / 4, lane % 4)
+    const int fg = lane >> 2, ft = lane & 3;
+    uint8_t(*ring)[C::STAGEB] = sm.ring[warp];
+    uint64_t *full = sm.full[warp];
 
-    // granule cursor (2 units, never across a segment), shared logic of both warps
+    // granule cursor (2 units, never across a segment)
     struct Cursor {
         int x, seg_end, k;
     };
@@ -260,426 +271,392 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
             c.seg_end = min(sm.prefix[c.k + 1], x1);
         }
     };
-
-    if (is_score) {
-        int ngran = 0;
-        if (x0 < x1) {
-            int x = x0;
-            int k = seg_of(sm.prefix, K, x);
-            while (x < x1) {
-                const int e = min(sm.prefix[k + 1], x1);
-                ngran += (e - x + 1) / 2;
-                x = e;
-                ++k;
-                while (k < K && sm.prefix[k + 1] == sm.prefix[k]) ++k;
-            }
-        }
-        if (lane == 0) {
-            P.ngran = ngran;
-            P.score_status = 0;
-            for (int s = 0; s < ST; ++s) {
-                mbar_init(&P.full[s], 1);
-                mbar_init(&P.sready[s], 1);
-            }
-            mbar_init(&P.qbar[0], 1);
-            mbar_init(&P.qbar[1], 1);
-            fence_mbar_init();
+    int ngran = 0;
+    {
+        int x = x0;
+        int k = seg_of(sm.prefix, K, x);
+        while (x < x1) {
+            const int e = min(sm.prefix[k + 1], x1);
+            ngran += (e - x + 1) / 2;
+            x = e;
+            ++k;
+            while (k < K && sm.prefix[k + 1] == sm.prefix[k]) ++k;
         }
     }
-    named_sync(1 + pi, 64);
-    const int ngran = P.ngran;
-    if (ngran == 0) return;
+    if (lane == 0) {
+        for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
+    __syncwarp();
     const uint64_t policy = l2_policy_evict_first();
 
-    if (is_score) {
-        // ===================== score warp =====================
-        // q slice of the current segment in registers; K dot products; the
-        // reduce-scatter; raw scores to the value warp.
-        Cursor con;
-        cursor_init(con);
-        auto q_copy = [&](int slot, int k) {  // lane 0
-            const int bh = k / nchunks;
-            const __nv_bfloat16 *src = a.q + (long long)bh * G * C::D;  // (b*Hkv + h)*G rows
-            mbar_arrive_expect_tx(&P.qbar[slot], G * C::D * 2);
-            bulk_g2s(&P.q[slot][0][0], src, G * C::D * 2, &P.qbar[slot], policy);
-        };
-        int seg_ord = 0;
-        int next_seg_k = -1;
-        if (lane == 0) q_copy(0, con.k);
-        if (con.seg_end < x1) {
-            next_seg_k = seg_of(sm.prefix, K, con.seg_end);
-            if (lane == 0) q_copy(1, next_seg_k);
+    // unit metadata window: lane l holds unit base + l (cur) and base + 32 + l
+    // (nxt): unit index (-1 bad, -2 absent), the two scales and the bad bits
+    int base = x0;
+    int cphys, nphys;
+    float cks, cvs, nks, nvs;
+    uint32_t cbad, nbad;
+    auto load_ids = [&](int bx, int &phys, uint32_t &bad) {
+        const int x = bx + lane;
+        phys = -2;
+        bad = 0;
+        if (x < x1) {
+            const int k = seg_of(sm.prefix, K, x);
+            const int bh = k / nchunks, c = k - bh * nchunks;
+            const int b = bh / Hkv, h = bh - b * Hkv;
+            const int page = c * (chunk_tokens / kPage) + (int)(x - sm.prefix[k]);
+            const long long bi = table_row(a, b, h) + page;
+            const int id = a.block_tables[bi];
+            bad = entry_bits(a, id, h, Hkv, bi);
+            phys = bad ? -1 : id * Hkv + h;  // unit index
         }
-        float2 q2[G][8];
-        uint32_t q_phase = 0, status = 0;
-        uint32_t parity = 0;  // every stage completes one phase per round of ST granules
-        int s = 0;
-        bool seg_start = true;
-        for (int i = 0; i < ngran; ++i) {
-            if (seg_start) {
-                const int slot = seg_ord & 1;
-                if (!mbar_wait_bounded(&P.qbar[slot], (q_phase >> slot) & 1u)) status |= kStatusTimeout;
-                q_phase ^= 1u << slot;
-                const __nv_bfloat16 *qs = &P.q[slot][0][0];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const uint4 w0 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16);
-                    const uint4 w1 = *reinterpret_cast<const uint4 *>(qs + g * C::D + vc * 16 + 8);
-                    const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float2 f = bf16x2_to_float2(ws[e]);
-                        q2[g][e] = make_float2(f.x * a.q_scale, f.y * a.q_scale);
-                    }
+    };
+    auto load_scales = [&](int phys, float &ks, float &vs) {
+        const long long u = phys >= 0 ? phys : 0;
+        ks = a.k_scale[u];
+        vs = a.v_scale[u];
+    };
+    load_ids(base, cphys, cbad);
+    load_ids(base + 32, nphys, nbad);
+    load_scales(cphys, cks, cvs);
+    load_scales(nphys, nks, nvs);
+    // metadata of unit x (in [base, base + 64)).  One uniform branch picks
+    // the window half (a select would wait for the next half's loads even
+    // when only the current one is read).
+    struct UnitMeta {
+        int phys;
+        float ks, vs;
+        uint32_t bad;
+    };
+    auto unit_meta = [&](int x) {
+        UnitMeta m;
+        const int d = x - base;
+        if (d < 32) {
+            m.phys = __shfl_sync(0xffffffffu, cphys, d);
+            m.ks = __shfl_sync(0xffffffffu, cks, d);
+            m.vs = __shfl_sync(0xffffffffu, cvs, d);
+            m.bad = __shfl_sync(0xffffffffu, cbad, d);
+        } else {
+            m.phys = __shfl_sync(0xffffffffu, nphys, d - 32);
+            m.ks = __shfl_sync(0xffffffffu, nks, d - 32);
+            m.vs = __shfl_sync(0xffffffffu, nvs, d - 32);
+            m.bad = __shfl_sync(0xffffffffu, nbad, d - 32);
+        }
+        return m;
+    };
+    auto unit_phys = [&](int x) {
+        const int d = x - base;
+        if (d < 32) return __shfl_sync(0xffffffffu, cphys, d);
+        return __shfl_sync(0xffffffffu, nphys, d - 32);
+    };
+    Cursor iss, con;
+    cursor_init(iss);
+    cursor_init(con);
+    // load (or mark empty) the granule at cursor c into stage s; lane 0 issues
+    auto issue_at = [&](const Cursor &c, int s) {
+        const int n = min(2, c.seg_end - c.x);
+        const int p0 = unit_phys(c.x);
+        const int p1 = n == 2 ? unit_phys(c.x + 1) : -2;
+        if (lane == 0) {
+            if (p0 < 0 && p1 < 0) {
+                mbar_arrive(&full[s]);
+            } else {
+                uint8_t *dst = ring[s];
+                mbar_arrive_expect_tx(&full[s], (p0 >= 0 ? 2 * C::UNITB : 0) + (p1 >= 0 ? 2 * C::UNITB : 0));
+                if (p0 >= 0) {
+                    tma_unit(dst, &tmk, p0 * kPage, &full[s], policy);
+                    tma_unit(dst + 2 * C::UNITB, &tmv, p0 * kPage, &full[s], policy);
                 }
-                __syncwarp();
-                // the slot just read is free: prefetch the segment after next
-                if (next_seg_k >= 0) {
-                    const int e = min(sm.prefix[next_seg_k + 1], x1);
-                    const int k2 = e < x1 ? seg_of(sm.prefix, K, e) : -1;
-                    if (k2 >= 0 && lane == 0) {
-                        fence_proxy_async_smem();
-                        q_copy(slot, k2);
-                    }
-                    next_seg_k = k2;
+                if (p1 >= 0) {
+                    tma_unit(dst + C::UNITB, &tmk, p1 * kPage, &full[s], policy);
+                    tma_unit(dst + 3 * C::UNITB, &tmv, p1 * kPage, &full[s], policy);
                 }
-                seg_start = false;
             }
-            const int n_units = min(2, con.seg_end - con.x);
-            if (!mbar_wait_bounded(&P.full[s], parity)) status |= kStatusTimeout;
-            const uint8_t *stage = P.ring[s];
+        }
+        return n;
+    };
+    for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
 
-            // ---- partial dot products and the reduce-scatter ----
-            // Lane (vt, vc) ends with the scores of token 4 vc + vt, i.e. pass
-            // vc: row 4 (vc & 3) + vt of unit vc >> 2.  The reduce-scatter folds
-            // the 8 passes in three levels (xor 4, 2, 1 between lanes); at each
-            // level a lane keeps the half named by its own bit of vc (bA, bB, bC:
-            // bits 2, 1, 0) and sends the other half.  Computing the passes in a
-            // lane-dependent order puts the kept half and the sent half in fixed
-            // registers, so no level needs a select: level-1 slot j holds row
-            // 4 (j ^ 2 bB ^ bC) + vt, of unit bA (kept) and of unit 1 - bA (sent).
-            // Each pair of passes is folded as soon as it is computed, so at most
-            // 24 partials are live.
-            const int bA = (vc >> 2) & 1, bB = (vc >> 1) & 1, bC = vc & 1;
-            const uint8_t *kkeep = stage + bA * C::UNITB + vt * C::ROWB + (vc << 4);
-            const uint8_t *ksend = stage + (bA ^ 1) * C::UNITB + vt * C::ROWB + (vc << 4);
-            float r1[4][G], r2[2][G], sc[G];
-            auto dot_row = [&](const uint8_t *krow, float (&pr)[G]) {
-                const uint4 wv = *reinterpret_cast<const uint4 *>(krow);
-                float2 kf[8];
-                pdequant16(wv, kf);
+    // query: raw bf16 of head fg, dims [32 ft, 32 ft + 32), fetched one
+    // segment ahead; f16 B fragments of the current segment (qb0/qb1[ks]:
+    // dims 32 ft + 4 ks + {0, 1} / {2, 3}) and the factor that undoes the
+    // power-of-two scaling and applies sm_scale * log2(e)
+    uint4 qraw[4];
+    auto q_fetch = [&](int k) {
+        if (fg < G) {
+            const int bh = k / nchunks;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((long long)bh * G + fg) * C::D + 32 * ft);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float2 acc = __fmul2_rn(q2[g][0], kf[0]);
+            for (int j = 0; j < 4; ++j) qraw[j] = __ldg(src + j);
+        } else {
 #pragma unroll
-                    for (int e = 1; e < 8; ++e) acc = __ffma2_rn(q2[g][e], kf[e], acc);
-                    pr[g] = acc.x + acc.y;
-                }
-            };
+            for (int j = 0; j < 4; ++j) qraw[j] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    uint32_t qb0[8], qb1[8];
+    float qmul = 0.f;
+    q_fetch(con.k);
+
+    // fragment offsets inside a swizzled 2 KB slab
+    // K (A of S = K Q^T): rows fg and fg + 8, logical chunks 2 ft and 2 ft + 1
+    const int offK0 = fg * C::ROWB + (((2 * ft) ^ (fg & 7)) << 4);
+    const int offK1 = fg * C::ROWB + (((2 * ft + 1) ^ (fg & 7)) << 4);
+    // V (A of O^T = V^T P^T): rows 2 ft, 2 ft + 1 (+ 8), logical chunk fg
+    const int offV0 = (2 * ft) * C::ROWB + ((fg ^ (2 * ft)) << 4);
+    const int offV1 = (2 * ft + 1) * C::ROWB + ((fg ^ (2 * ft + 1)) << 4);
+    // shuffle sources of the probability fragment (tokens 2 ft and 2 ft + 1,
+    // head fg) and which of the source's two heads is fg
+    const int src0 = 8 * ft + (fg >> 1), src1 = src0 + 4;
+    const bool odd_head = (fg & 1) != 0;
+
+    // online softmax state of heads 2 ft (A) and 2 ft + 1 (B); O^T fragments:
+    // o[mt][0] = (dim 16 fg + 2 mt, head A), [1] = (same dim, head B),
+    // [2] = (dim + 1, head A), [3] = (dim + 1, head B); O is kept in units of
+    // 2^eO (the V-scale reference)
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    int eO = kNoScale;
+    float vref = 0.f;  // 2^-eO
+
+    uint32_t parity = 0, seg_status = 0;
+    int s = 0;
+    bool pending_scales = false, seg_start = true;
+    for (int i = 0; i < ngran; ++i) {
+        // metadata window upkeep
+        if (pending_scales) {
+            load_scales(nphys, nks, nvs);
+            pending_scales = false;
+        }
+        if (con.x >= base + 32) {
+            base += 32;
+            cphys = nphys; cks = nks; cvs = nvs; cbad = nbad;
+            load_ids(base + 32, nphys, nbad);
+            pending_scales = true;
+        }
+        if (seg_start) {
+            // this segment's query fragments, then fetch the next segment's
+            uint32_t amax = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int roff = 4 * (j ^ (2 * bB) ^ bC) * C::ROWB;
-                float keep[G], send[G];
-                dot_row(kkeep + roff, keep);
-                dot_row(ksend + roff, send);
 #pragma unroll
-                for (int g = 0; g < G; ++g) r1[j][g] = keep[g] + __shfl_xor_sync(0xffffffffu, send[g], 4);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    r2[j][g] = r1[j][g] + __shfl_xor_sync(0xffffffffu, r1[j + 2][g], 2);
-#pragma unroll
-            for (int g = 0; g < G; ++g) sc[g] = r2[0][g] + __shfl_xor_sync(0xffffffffu, r2[1][g], 1);
-            // lane (vt, vc) now holds the G raw scores of token 4 vc + vt
-            if constexpr (G == 4) {
-                *reinterpret_cast<float4 *>(P.sb[s].s[lane]) = make_float4(sc[0], sc[1], sc[2], sc[3]);
-            } else if constexpr (G == 2) {
-                *reinterpret_cast<float2 *>(P.sb[s].s[lane]) = make_float2(sc[0], sc[1]);
-            } else {
-                P.sb[s].s[lane][0] = sc[0];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&P.sready[s]);
-            const bool seg_end = con.x + n_units >= con.seg_end;
-            cursor_next(con, n_units);
-            if (seg_end) {
-                seg_start = true;
-                ++seg_ord;
-            }
-            if (++s == ST) {
-                s = 0;
-                parity ^= 1u;
-            }
-        }
-        if (status && lane == 0) atomicOr(&P.score_status, status);
-    } else {
-        // ===================== value warp =====================
-        // unit metadata window: lane l holds unit base + l (cur) and
-        // base + 32 + l (nxt): page id (-1 bad, -2 absent) and the two scales
-        int base = x0;
-        int cphys, nphys;
-        float cks, cvs, nks, nvs;
-        uint32_t cbad, nbad;
-        auto load_ids = [&](int bx, int &phys, uint32_t &bad) {
-            const int x = bx + lane;
-            phys = -2;
-            bad = 0;
-            if (x < x1) {
-                const int k = seg_of(sm.prefix, K, x);
-                const int bh = k / nchunks, c = k - bh * nchunks;
-                const int b = bh / Hkv, h = bh - b * Hkv;
-                const int page = c * (chunk_tokens / kPage) + (int)(x - sm.prefix[k]);
-                const long long bi = table_row(a, b, h) + page;
-                const int id = a.block_tables[bi];
-                bad = entry_bits(a, id, h, Hkv, bi);
-                phys = bad ? -1 : id * Hkv + h;  // unit index
-            }
-        };
-        auto load_scales = [&](int phys, float &ks, float &vs) {
-            const long long u = phys >= 0 ? phys : 0;
-            ks = a.k_scale[u];
-            vs = a.v_scale[u];
-        };
-        load_ids(base, cphys, cbad);
-        load_ids(base + 32, nphys, nbad);
-        load_scales(cphys, cks, cvs);
-        load_scales(nphys, nks, nvs);
-        // metadata of unit x (in [base, base + 64)).  One uniform branch picks
-        // the window half (a select would wait for the next half's loads even
-        // when only the current one is read).
-        struct UnitMeta {
-            int phys;
-            float ks, vs;
-            uint32_t bad;
-        };
-        auto unit_meta = [&](int x) {
-            UnitMeta m;
-            const int d = x - base;
-            if (d < 32) {
-                m.phys = __shfl_sync(0xffffffffu, cphys, d);
-                m.ks = __shfl_sync(0xffffffffu, cks, d);
-                m.vs = __shfl_sync(0xffffffffu, cvs, d);
-                m.bad = __shfl_sync(0xffffffffu, cbad, d);
-            } else {
-                m.phys = __shfl_sync(0xffffffffu, nphys, d - 32);
-                m.ks = __shfl_sync(0xffffffffu, nks, d - 32);
-                m.vs = __shfl_sync(0xffffffffu, nvs, d - 32);
-                m.bad = __shfl_sync(0xffffffffu, nbad, d - 32);
-            }
-            return m;
-        };
-        auto unit_phys = [&](int x) {
-            const int d = x - base;
-            if (d < 32) return __shfl_sync(0xffffffffu, cphys, d);
-            return __shfl_sync(0xffffffffu, nphys, d - 32);
-        };
-        Cursor iss, con;
-        cursor_init(iss);
-        cursor_init(con);
-        // load (or mark empty) the granule at cursor c into stage s; lane 0 issues
-        auto issue_at = [&](const Cursor &c, int s) {
-            const int n = min(2, c.seg_end - c.x);
-            const int p0 = unit_phys(c.x);
-            const int p1 = n == 2 ? unit_phys(c.x + 1) : -2;
-            if (lane == 0) {
-                if (p0 < 0 && p1 < 0) {
-                    mbar_arrive(&P.full[s]);
-                } else {
-                    uint8_t *dst = P.ring[s];
-                    const uint8_t *kp = static_cast<const uint8_t *>(a.k_pages);
-                    const uint8_t *vp = static_cast<const uint8_t *>(a.v_pages);
-                    mbar_arrive_expect_tx(&P.full[s], (p0 >= 0 ? 2 * C::UNITB : 0) + (p1 >= 0 ? 2 * C::UNITB : 0));
-                    if (p0 >= 0) {
-                        bulk_g2s(dst, kp + (long long)p0 * C::UNITB, C::UNITB, &P.full[s], policy);
-                        bulk_g2s(dst + 2 * C::UNITB, vp + (long long)p0 * C::UNITB, C::UNITB, &P.full[s], policy);
-                    }
-                    if (p1 >= 0) {
-                        bulk_g2s(dst + C::UNITB, kp + (long long)p1 * C::UNITB, C::UNITB, &P.full[s], policy);
-                        bulk_g2s(dst + 3 * C::UNITB, vp + (long long)p1 * C::UNITB, C::UNITB, &P.full[s], policy);
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t wq = word_of(qraw[j], c);
+                    amax = max(amax, max((wq << 16) & 0x7fff0000u, wq & 0x7fff0000u));
                 }
             }
-            return n;
-        };
-        for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
-
-        float m[G], l[G];
-        float2 o[G][8];
+            asm volatile("redux.sync.max.u32 %0, %0, 0xffffffff;" : "+r"(amax));
+            const int eq = min(126, max(-126, (int)(amax >> 23) - 127));
+            const float down = pow2i(-eq);
+            qmul = a.q_scale * pow2i(eq);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            m[g] = -INFINITY;
-            l[g] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
+            for (int ks = 0; ks < 8; ++ks) {
+                const float2 f0 = bf16x2_to_float2(word_of(qraw[ks >> 1], 2 * (ks & 1)));
+                const float2 f1 = bf16x2_to_float2(word_of(qraw[ks >> 1], 2 * (ks & 1) + 1));
+                qb0[ks] = pack_half2(f0.x * down, f0.y * down);
+                qb1[ks] = pack_half2(f1.x * down, f1.y * down);
+            }
+            if (con.seg_end < x1) q_fetch(seg_of(sm.prefix, K, con.seg_end));
+            seg_start = false;
         }
-        uint32_t parity = 0, seg_status = 0;
-        int s = 0;
-        bool pending_scales = false;
-        for (int i = 0; i < ngran; ++i) {
-            // metadata window upkeep
-            if (pending_scales) {
-                load_scales(nphys, nks, nvs);
-                pending_scales = false;
-            }
-            if (con.x >= base + 32) {
-                base += 32;
-                cphys = nphys; cks = nks; cvs = nvs; cbad = nbad;
-                load_ids(base + 32, nphys, nbad);
-                pending_scales = true;
-            }
-            const int n_units = min(2, con.seg_end - con.x);
-            const UnitMeta u0m = unit_meta(con.x);
-            UnitMeta u1m = {-2, 0.f, 0.f, 0u};
-            if (n_units == 2) u1m = unit_meta(con.x + 1);
-            seg_status |= u0m.bad | u1m.bad;
-            const int seg_last = sm.prefix[con.k + 1] - 1;
-            const int lnv = sm.last_nv[con.k];
-            const int nv0 = u0m.phys >= 0 ? (con.x == seg_last ? lnv : kPage) : 0;
-            const int nv1 = u1m.phys >= 0 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
-            const float ks0 = u0m.ks, ks1 = u1m.ks, vs0 = u0m.vs, vs1 = u1m.vs;
+        const int n_units = min(2, con.seg_end - con.x);
+        const UnitMeta u0m = unit_meta(con.x);
+        UnitMeta u1m = {-2, 0.f, 0.f, 0u};
+        if (n_units == 2) u1m = unit_meta(con.x + 1);
+        seg_status |= u0m.bad | u1m.bad;
+        const int seg_last = sm.prefix[con.k + 1] - 1;
+        const int lnv = sm.last_nv[con.k];
+        int nv[2];
+        nv[0] = u0m.phys >= 0 ? (con.x == seg_last ? lnv : kPage) : 0;
+        nv[1] = u1m.phys >= 0 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
+        const float ksc[2] = {u0m.ks, u1m.ks};
 
-            if (!mbar_wait_bounded(&P.sready[s], parity)) seg_status |= kStatusTimeout;
+        if (!mbar_wait_bounded(&full[s], parity)) seg_status |= kStatusTimeout;
+        const uint8_t *stage = ring[s];
 
-            // ---- online softmax over the granule (lane: token 4 vc + vt) ----
-            const int my_u = vc >> 2, my_row = (4 * vc + vt) & 15;
-            const bool ok = my_row < (my_u ? nv1 : nv0);
-            const float ksc = my_u ? ks1 : ks0;
-            float sc[G];
-            if constexpr (G == 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(P.sb[s].s[lane]);
-                sc[0] = v4.x; sc[1] = v4.y; sc[2] = v4.z; sc[3] = v4.w;
-            } else if constexpr (G == 2) {
-                const float2 v2 = *reinterpret_cast<const float2 *>(P.sb[s].s[lane]);
-                sc[0] = v2.x; sc[1] = v2.y;
-            } else {
-                sc[0] = P.sb[s].s[lane][0];
-            }
+        // ---- scores: S = K Q^T per unit; sc[u][j]: token fg (+8 for j >= 2),
+        //      head 2 ft (+1 for odd j); -inf outside the unit's live rows ----
+        float sc[2][4];
 #pragma unroll
-            for (int g = 0; g < G; ++g) sc[g] = ok ? sc[g] * ksc : -INFINITY;
-            if (MASS && ok) {  // scores for the attention-mass pass
+        for (int u = 0; u < 2; ++u) {
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            if (nv[u] > 0) {
+                const uint8_t *kb = stage + u * C::UNITB;
+                const uint4 ra0 = lds128(kb + offK0), ra1 = lds128(kb + offK1);
+                const uint4 rb0 = lds128(kb + 8 * C::ROWB + offK0), rb1 = lds128(kb + 8 * C::ROWB + offK1);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t wa = word_of(ks < 4 ? ra0 : ra1, ks & 3);
+                    const uint32_t wb = word_of(ks < 4 ? rb0 : rb1, ks & 3);
+                    uint32_t a0, a2, a1, a3;
+                    e4m3x4_to_f16x2(wa, a0, a2);
+                    e4m3x4_to_f16x2(wb, a1, a3);
+                    if (ks & 1) mma_16816(c1, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+                    else mma_16816(c0, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+                }
+            }
+            const float f = qmul * ksc[u];
+            const bool lo_ok = fg < nv[u], hi_ok = fg + 8 < nv[u];
+            sc[u][0] = lo_ok ? (c0[0] + c1[0]) * f : -INFINITY;
+            sc[u][1] = lo_ok ? (c0[1] + c1[1]) * f : -INFINITY;
+            sc[u][2] = hi_ok ? (c0[2] + c1[2]) * f : -INFINITY;
+            sc[u][3] = hi_ok ? (c0[3] + c1[3]) * f : -INFINITY;
+            if (MASS) {  // scores for the attention-mass pass
                 const int bh = con.k / nchunks, c = con.k - bh * nchunks;
-                const int page = c * (chunk_tokens / kPage) + (con.x + my_u - sm.prefix[con.k]);
-                store_scores<G>(a, bh, page * kPage + my_row, sc);
-            }
-            float mb[G];
-            bool grow = false;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                mb[g] = pwarp_max(sc[g]);
-                grow |= mb[g] > m[g] + kLazy;
-            }
-            if (grow) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float mn = fmaxf(m[g], mb[g]);
-                    const float alpha = m[g] == -INFINITY ? 0.f : pexp2(m[g] - mn);
-                    const float2 a2 = make_float2(alpha, alpha);
-                    m[g] = mn;
-                    l[g] *= alpha;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[g][e] = __fmul2_rn(o[g][e], a2);
+                const int tok0 = (c * (chunk_tokens / kPage) + (con.x + u - sm.prefix[con.k])) * kPage + fg;
+                float *dst = a.mscore + ((long long)bh * a.mlen + tok0) * G;
+                if (2 * ft < G) {
+                    if (lo_ok) dst[2 * ft] = sc[u][0];
+                    if (hi_ok) dst[8 * G + 2 * ft] = sc[u][2];
+                }
+                if (2 * ft + 1 < G) {
+                    if (lo_ok) dst[2 * ft + 1] = sc[u][1];
+                    if (hi_ok) dst[8 * G + 2 * ft + 1] = sc[u][3];
                 }
             }
-            {
-                const float vsc = my_u ? vs1 : vs0;
-                float pp[2 * G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float pr = ok ? pexp2(sc[g] - m[g]) : 0.f;
-                    l[g] += pr;
-                    pp[2 * g] = pp[2 * g + 1] = pr * vsc;
-                }
-                // rows transposed (t, c) -> 8 t + c: a quarter-warp's stores land
-                // in consecutive rows
-                float *dstp = P.p[8 * vt + vc];
-                if constexpr (G >= 2) {
-#pragma unroll
-                    for (int x = 0; x < G / 2; ++x)
-                        reinterpret_cast<float4 *>(dstp)[x] =
-                            make_float4(pp[4 * x], pp[4 * x + 1], pp[4 * x + 2], pp[4 * x + 3]);
-                } else {
-                    *reinterpret_cast<float2 *>(dstp) = make_float2(pp[0], pp[1]);
-                }
-            }
-            __syncwarp();
+        }
 
-            // ---- values: lane (vt, vc) accumulates slice vc over tokens 4r + vt ----
-            const uint8_t *stage = P.ring[s];
-            auto value_pass = [&](int r) {
-                const int row = 4 * (r & 3) + vt;
-                const uint8_t *vrow = stage + 2 * C::UNITB + (r >> 2) * C::UNITB + row * C::ROWB;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(vrow + (vc << 4));
-                float2 vf[8];
-                pdequant16(wv, vf);
-                // token 4r + vt was scored by lane (t = vt, c = r): row 8 vt + r
-                const float2 *ps = reinterpret_cast<const float2 *>(P.p[8 * vt + r]);
-                float2 pg[G];
+        // ---- online softmax: granule max per head over the 8 token rows ----
+        float mbA = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+        float mbB = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
 #pragma unroll
-                for (int g = 0; g < G; ++g) pg[g] = ps[g];
+        for (int off = 4; off < 32; off <<= 1) {
+            mbA = fmaxf(mbA, __shfl_xor_sync(0xffffffffu, mbA, off));
+            mbB = fmaxf(mbB, __shfl_xor_sync(0xffffffffu, mbB, off));
+        }
+        const bool grow = mbA > mA + kLazy || mbB > mB + kLazy;
+        // V-scale reference: 2^eO bounds every live unit's V scale seen so far
+        int eneed = kNoScale;
+        if (nv[0] > 0) eneed = exp_above(u0m.vs);
+        if (nv[1] > 0) eneed = max(eneed, exp_above(u1m.vs));
+        const bool scale_up = eneed > eO;
+        float fA = 1.f, fB = 1.f;
+        if (scale_up) {
+            const int d = eO - eneed;  // < 0
+            const float r = (eO == kNoScale || d < -126) ? 0.f : pow2i(d);
+            fA = fB = r;
+            eO = eneed;
+            vref = pow2i(-eO);
+        }
+        if (grow) {
+            const float nA = fmaxf(mA, mbA), nB = fmaxf(mB, mbB);
+            const float aA = mA == -INFINITY ? 0.f : pexp2(mA - nA);
+            const float aB = mB == -INFINITY ? 0.f : pexp2(mB - nB);
+            mA = nA;
+            mB = nB;
+            lA *= aA;
+            lB *= aB;
+            fA *= aA;
+            fB *= aB;
+        }
+        if (grow || scale_up) {
 #pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[g][e] = __ffma2_rn(pg[g], vf[e], o[g][e]);
-            };
-            if (nv0 == kPage && nv1 == kPage) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) value_pass(r);
-            } else {
-                // tokens past the sequence end or in a missing unit are skipped:
-                // their rows may hold stale bytes (even NaN codes)
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = 4 * (r & 3) + vt;
-                    if (row < ((r >> 2) ? nv1 : nv0)) value_pass(r);
-                }
+            for (int mt = 0; mt < 8; ++mt) {
+                o[mt][0] *= fA;
+                o[mt][2] *= fA;
+                o[mt][1] *= fB;
+                o[mt][3] *= fB;
             }
-            const bool seg_end = con.x + n_units >= con.seg_end;
-            if (seg_end) {
-                // finish the segment: sum the lanes, normalise, write the row
-                const int row = con.k + w;
+        }
+
+        // ---- probabilities -> B fragments of the V product; V product ----
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float lt = l[g];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-                    const float inv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-#pragma unroll
-                        for (int off = 8; off < 32; off <<= 1) {
-                            o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, off);
-                            o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, off);
-                        }
-                    }
-                    if (vt == 0) {
-                        float4 *dst = reinterpret_cast<float4 *>(a.o + ((long long)row * G + g) * C::D + vc * 16);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_float4(o[g][2 * e].x * inv, o[g][2 * e].y * inv,
-                                                 o[g][2 * e + 1].x * inv, o[g][2 * e + 1].y * inv);
-                    }
-                    if (lane == 0) a.lse[(long long)row * G + g] = lt > 0.f ? m[g] + plog2(lt) : -INFINITY;
-                    m[g] = -INFINITY;
-                    l[g] = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[g][e] = make_float2(0.f, 0.f);
-                }
-                if (lane == 0) a.status[row] = seg_status | P.score_status;
-                seg_status = 0;
+        for (int u = 0; u < 2; ++u) {
+            const bool lo_ok = fg < nv[u], hi_ok = fg + 8 < nv[u];
+            const float pA0 = lo_ok ? pexp2(sc[u][0] - mA) : 0.f;
+            const float pB0 = lo_ok ? pexp2(sc[u][1] - mB) : 0.f;
+            const float pA1 = hi_ok ? pexp2(sc[u][2] - mA) : 0.f;
+            const float pB1 = hi_ok ? pexp2(sc[u][3] - mB) : 0.f;
+            lA += pA0 + pA1;
+            lB += pB0 + pB1;
+            if (nv[u] == 0) continue;  // uniform: nothing of this unit is live
+            const float vs = (u ? u1m.vs : u0m.vs) * vref;
+            // X0: head A at tokens (fg, fg + 8); X1: head B
+            const uint32_t X0 = pack_half2(pA0 * vs, pA1 * vs);
+            const uint32_t X1 = pack_half2(pB0 * vs, pB1 * vs);
+            const uint32_t s00 = __shfl_sync(0xffffffffu, X0, src0), s01 = __shfl_sync(0xffffffffu, X1, src0);
+            const uint32_t s10 = __shfl_sync(0xffffffffu, X0, src1), s11 = __shfl_sync(0xffffffffu, X1, src1);
+            const uint32_t Y0 = odd_head ? s01 : s00;  // head fg, tokens (2 ft, 2 ft + 8)
+            const uint32_t Y1 = odd_head ? s11 : s10;  // head fg, tokens (2 ft + 1, 2 ft + 9)
+            const uint32_t pb0 = __byte_perm(Y0, Y1, 0x5410);  // tokens 2 ft, 2 ft + 1
+            const uint32_t pb1 = __byte_perm(Y0, Y1, 0x7632);  // tokens 2 ft + 8, 2 ft + 9
+
+            const uint8_t *vb = stage + (2 + u) * C::UNITB;
+            uint4 r0 = lds128(vb + offV0), r1 = lds128(vb + offV1);
+            uint4 r2 = lds128(vb + 8 * C::ROWB + offV0), r3 = lds128(vb + 8 * C::ROWB + offV1);
+            if (nv[u] < kPage) {
+                // rows past the live tokens may hold stale bytes (even NaN
+                // codes): zero them so that 0 x row stays 0
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                if (2 * ft >= nv[u]) r0 = z;
+                if (2 * ft + 1 >= nv[u]) r1 = z;
+                if (2 * ft + 8 >= nv[u]) r2 = z;
+                if (2 * ft + 9 >= nv[u]) r3 = z;
             }
-            // refill this stage with the granule ST ahead
-            __syncwarp();
-            if (i + ST < ngran) {
-                if (lane == 0) fence_proxy_async_smem();
-                cursor_next(iss, issue_at(iss, s));
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) {
+                const uint32_t w0 = word_of(r0, wd), w1 = word_of(r1, wd);
+                const uint32_t w2 = word_of(r2, wd), w3 = word_of(r3, wd);
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x5140), a0, a1);  // dims 4wd, 4wd+1
+                e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x5140), a2, a3);
+                mma_16816(o[2 * wd], a0, a1, a2, a3, pb0, pb1);
+                e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x7362), a0, a1);  // dims 4wd+2, 4wd+3
+                e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x7362), a2, a3);
+                mma_16816(o[2 * wd + 1], a0, a1, a2, a3, pb0, pb1);
             }
-            cursor_next(con, n_units);
-            if (++s == ST) {
-                s = 0;
-                parity ^= 1u;
+        }
+
+        const bool seg_end = con.x + n_units >= con.seg_end;
+        if (seg_end) {
+            // finish the segment: sum l over the token rows, normalise, write
+            float tA = lA, tB = lB;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                tA += __shfl_xor_sync(0xffffffffu, tA, off);
+                tB += __shfl_xor_sync(0xffffffffu, tB, off);
             }
+            const float up = eO == kNoScale ? 0.f : pow2i(eO);
+            const float iA = tA > 0.f ? up / tA : 0.f, iB = tB > 0.f ? up / tB : 0.f;
+            const long long row = con.k + w;
+            float *orow = a.o + row * G * C::D + 16 * fg;
+            if (2 * ft < G) {
+                float4 *dst = reinterpret_cast<float4 *>(orow + (2 * ft) * C::D);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(o[2 * e][0] * iA, o[2 * e][2] * iA, o[2 * e + 1][0] * iA, o[2 * e + 1][2] * iA);
+                if (fg == 0) a.lse[row * G + 2 * ft] = tA > 0.f ? mA + plog2(tA) : -INFINITY;
+            }
+            if (2 * ft + 1 < G) {
+                float4 *dst = reinterpret_cast<float4 *>(orow + (2 * ft + 1) * C::D);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(o[2 * e][1] * iB, o[2 * e][3] * iB, o[2 * e + 1][1] * iB, o[2 * e + 1][3] * iB);
+                if (fg == 0) a.lse[row * G + 2 * ft + 1] = tB > 0.f ? mB + plog2(tB) : -INFINITY;
+            }
+            if (lane == 0) a.status[row] = seg_status;
+            seg_status = 0;
+            mA = mB = -INFINITY;
+            lA = lB = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+            eO = kNoScale;
+            vref = 0.f;
+            seg_start = true;
+        }
+        // refill this stage with the granule ST ahead
+        __syncwarp();
+        if (i + ST < ngran) {
+            if (lane == 0) fence_proxy_async_smem();
+            cursor_next(iss, issue_at(iss, s));
+        }
+        cursor_next(con, n_units);
+        if (++s == ST) {
+            s = 0;
+            parity ^= 1u;
         }
     }
 }
@@ -698,7 +675,7 @@ __global__ void __launch_bounds__(PersCfg<G>::NT, 1)
 // --------------------------------------------------------------------------
 constexpr int kCombThreads = 512;
 constexpr int kCombWarps = kCombThreads / 32;
-constexpr int kCombMaxChunks = PersCfg<1>::MAXK;  // segments per (b, h) <= all segments
+constexpr int kCombMaxChunks = PersCfg::MAXK;  // segments per (b, h) <= all segments
 
 template <int G>
 struct CombSmem {
@@ -919,9 +896,39 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
 // --------------------------------------------------------------------------
 namespace {
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// A pool [units][16][128] bytes as a 2-D tensor (128-byte rows) read in
+// 16-row boxes with the 128-byte swizzle.
+cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long rows) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)PersCfg::ROWB, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)PersCfg::ROWB};
+    const cuuint32_t box[2] = {(cuuint32_t)PersCfg::ROWB, (cuuint32_t)kPage};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pages), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int G, bool MASS>
 cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    using C = PersCfg<G>;
+    using C = PersCfg;
     const size_t smem = sizeof(typename C::Smem) + 1024;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
@@ -934,7 +941,11 @@ cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    return launch_pdl(decode_split_pers_kernel<G, MASS>, dim3(p.pers_ctas), dim3(C::NT), smem, s,
+    const long long rows = (long long)a.num_pages * p.Hkv * kPage;
+    alignas(64) CUtensorMap tmk, tmv;
+    if ((e = pool_tensor_map(&tmk, a.k_pages, rows)) != cudaSuccess) return e;
+    if ((e = pool_tensor_map(&tmv, a.v_pages, rows)) != cudaSuccess) return e;
+    return launch_pdl(decode_split_pers_kernel<G, MASS>, dim3(p.pers_ctas), dim3(C::NT), smem, s, tmk, tmv,
                       a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
 }
 
@@ -945,13 +956,13 @@ cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t
 
 }  // namespace
 
-int pers_workers_per_cta() { return PersCfg<4>::PAIRS; }
+int pers_workers_per_cta() { return PersCfg::WORKERS; }
 
 bool pers_supported(const DecodePlan &p, int num_pages) {
     const long long rows = (long long)num_pages * p.Hkv * kPage;
     const long long K = (long long)p.B * p.Hkv * p.nchunks;
     return p.dtype == PFKV_KV_FP8_E4M3 && p.D == 128 && p.G <= 4 && rows < (1LL << 31) &&
-           K <= PersCfg<4>::MAXK && p.Breq <= PersCfg<4>::MAXB;
+           K <= PersCfg::MAXK && p.Breq <= PersCfg::MAXB;
 }
 
 cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
@@ -964,7 +975,7 @@ cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStre
 }
 
 cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    const int W = p.pers_ctas * PersCfg<4>::PAIRS;
+    const int W = p.pers_ctas * PersCfg::WORKERS;
     const dim3 grid((unsigned)(p.B * p.Hkv));
     switch (p.G) {
         case 1: return launch_pdl(decode_combine_pers_kernel<1>, grid, dim3(kCombThreads), 0, s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
