@@ -335,8 +335,9 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
     }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((stages & PFKV_STAGE_VALIDATE) && plan.tags && !fused && launch_validate(a, plan, s) != cudaSuccess)
-        return PFKV_ERR_CUDA;
+    const bool validate = (stages & PFKV_STAGE_VALIDATE) && plan.tags && !fused;
+    a.early = validate ? 1 : 0;
+    if (validate && launch_validate(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     if ((stages & PFKV_STAGE_SPLIT) && launch_split(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     if ((stages & PFKV_STAGE_COMBINE) && launch_combine(a, plan, s) != cudaSuccess)
         return PFKV_ERR_CUDA;

@@ -139,6 +139,8 @@ cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
 // of their tags and expected tags, so a tile costs two memory round trips.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(kValThreads) validate_kernel(DecodeArgs a, int Hkv) {
+    // wait first, then let the next kernel start: the split kernel relies on
+    // it (DecodeArgs::early)
     pdl_enter();
     const int bh = blockIdx.x, tile = blockIdx.y;
     const int b = bh / Hkv, h = bh - b * Hkv;

@@ -10,7 +10,8 @@
 // Segments and balanced ranges.  A segment is one (request b, kv head h,
 // chunk c) — c is always 0 unless the caller fixes a split size.  Every CTA
 // computes the same exclusive prefix sum of the segments' 16-token units
-// (units of a request the validation kernel rejected count as zero).  With U
+// (units of a request the validation kernel rejected are counted, then
+// skipped).  With U
 // units in all and W workers, worker w takes the units
 // [ceil(wU/W), ceil((w+1)U/W)): equal shares, crossing segment boundaries, so
 // no worker idles while another finishes a long sequence.  A worker writes one
@@ -38,6 +39,7 @@
 // The dims of the score reduction are taken in a permuted order (lane t owns
 // dims [32t, 32t + 32) of both K and Q), which changes nothing in the sum.
 #include <atomic>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -128,12 +130,17 @@ __device__ __forceinline__ int worker_of(long long x, long long U, int W) {
 
 }  // namespace
 
+// Kernel shape: units per granule (one ring stage) and worker warps per CTA.
+constexpr int kGranUnits = 2;
+constexpr int kWorkers = 8;
+
 struct PersCfg {
     static constexpr int D = 128;
     static constexpr int ROWB = 128;
     static constexpr int UNITB = kPage * ROWB;   // 2 KB
-    static constexpr int STAGEB = 4 * UNITB;     // K u0 | K u1 | V u0 | V u1
-    static constexpr int WORKERS = 8;
+    static constexpr int GU = kGranUnits;
+    static constexpr int STAGEB = 2 * GU * UNITB;  // K u0 .. K u(GU-1) | V u0 .. V u(GU-1)
+    static constexpr int WORKERS = kWorkers;
     static constexpr int STAGES = 3;
     static constexpr int NT = WORKERS * 32;
     static constexpr int MAXK = 4096;            // segments (prefix array in smem)
@@ -176,19 +183,17 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int K = B * Hkv * nchunks;
-    pdl_enter();
+    const int Breq = B / a.kq;  // B counts virtual requests (see DecodeArgs::kq)
+    // Without a.early, wait for the previous kernels right away.  With it, the
+    // part up to the second pdl_enter() below runs while the validation kernel
+    // finishes: everything before that kernel is complete, so this part may
+    // read the call's inputs, the scales and the pool, but not the validation
+    // bits, and it writes only shared memory.
+    if (!a.early) pdl_enter();
 
-    // ---------------- prologue: request flags, unit prefix sums ----------------
-    // B counts virtual requests (see DecodeArgs::kq); rflag is per request
-    const int Breq = B / a.kq;
-    for (int b = tid; b < Breq; b += C::NT) sm.rflag[b] = 0;
-    __syncthreads();
-    if (a.hflags) {  // [Breq][Hkv][htiles], read in parallel
-        const int per_req = Hkv * a.htiles;
-        for (int i = tid; i < Breq * per_req; i += C::NT)
-            if (a.hflags[i]) sm.rflag[i / per_req] = 1;
-    }
-    __syncthreads();
+    // ---------------- prologue: unit prefix sums ----------------
+    // They do not depend on the validation bits: units of rejected requests
+    // stay in the sums, and the workers skip them.
     const int per = (K + C::NT - 1) / C::NT;
     const int k0 = min(K, tid * per), k1 = min(K, k0 + per);
     int local = 0;
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
         const int b = bh / Hkv, h = bh - b * Hkv;  // b: virtual request
         const int n = query_len(a, b, h);
         int units = 0, lastnv = 0;
-        if (!sm.rflag[b / a.kq] && n >= 0) {
+        if (n >= 0) {
             const int pages = (n + kPage - 1) / kPage;
             const int cp = chunk_tokens / kPage;
             units = max(0, min(pages, (c + 1) * cp) - c * cp);
@@ -239,23 +244,19 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     // never more workers than units: every worker then owns at least one unit,
     // so all workers between a segment's first and last unit write its rows
     const int W = min((int)gridDim.x * C::WORKERS, U);
-    if (blockIdx.x == 0) {
-        for (int k = tid; k <= K; k += C::NT) ws_prefix[k] = sm.prefix[k];
-    }
-    if (U == 0) return;
 
     // ---------------- the worker: one warp ----------------
     const int warp = tid >> 5, lane = tid & 31;
     const int w = blockIdx.x * C::WORKERS + warp;
     const int x0 = w < W ? (int)(((long long)w * U + W - 1) / W) : U;
     const int x1 = w < W ? (int)(((long long)(w + 1) * U + W - 1) / W) : U;
-    if (x0 >= x1) return;  // no block-wide barrier follows
+    const bool idle = x0 >= x1;
     // fragment coordinates: lane (g, t) = (lane / 4, lane % 4)
     const int fg = lane >> 2, ft = lane & 3;
     uint8_t(*ring)[C::STAGEB] = sm.ring[warp];
     uint64_t *full = sm.full[warp];
 
-    // granule cursor (2 units, never across a segment)
+    // granule cursor (GU units, never across a segment)
     struct Cursor {
         int x, seg_end, k;
     };
@@ -272,18 +273,18 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
         }
     };
     int ngran = 0;
-    {
+    if (!idle) {
         int x = x0;
         int k = seg_of(sm.prefix, K, x);
         while (x < x1) {
             const int e = min(sm.prefix[k + 1], x1);
-            ngran += (e - x + 1) / 2;
+            ngran += (e - x + C::GU - 1) / C::GU;
             x = e;
             ++k;
             while (k < K && sm.prefix[k + 1] == sm.prefix[k]) ++k;
         }
     }
-    if (lane == 0) {
+    if (!idle && lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
@@ -298,10 +299,12 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     int cphys, nphys;
     float cks, cvs, nks, nvs;
     uint32_t cbad, nbad;
-    auto load_ids = [&](int bx, int &phys, uint32_t &bad) {
+    // req: the unit's request (-1 for no unit), for skip_rejected()
+    auto load_ids = [&](int bx, int &phys, uint32_t &bad, int &req) {
         const int x = bx + lane;
         phys = -2;
         bad = 0;
+        req = -1;
         if (x < x1) {
             const int k = seg_of(sm.prefix, K, x);
             const int bh = k / nchunks, c = k - bh * nchunks;
@@ -311,6 +314,14 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
             const int id = a.block_tables[bi];
             bad = entry_bits(a, id, h, Hkv, bi);
             phys = bad ? -1 : id * Hkv + h;  // unit index
+            req = b / a.kq;
+        }
+    };
+    // units of a request the validation kernel rejected are absent
+    auto skip_rejected = [&](int req, int &phys, uint32_t &bad) {
+        if (req >= 0 && sm.rflag[req]) {
+            phys = -2;
+            bad = 0;
         }
     };
     auto load_scales = [&](int phys, float &ks, float &vs) {
@@ -318,10 +329,11 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
         ks = a.k_scale[u];
         vs = a.v_scale[u];
     };
-    load_ids(base, cphys, cbad);
-    load_ids(base + 32, nphys, nbad);
-    load_scales(cphys, cks, cvs);
-    load_scales(nphys, nks, nvs);
+    int creq = -1, nreq = -1;
+    if (!idle) {
+        load_ids(base, cphys, cbad, creq);
+        load_ids(base + 32, nphys, nbad, nreq);
+    }
     // metadata of unit x (in [base, base + 64)).  One uniform branch picks
     // the window half (a select would wait for the next half's loads even
     // when only the current one is read).
@@ -356,28 +368,31 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     cursor_init(con);
     // load (or mark empty) the granule at cursor c into stage s; lane 0 issues
     auto issue_at = [&](const Cursor &c, int s) {
-        const int n = min(2, c.seg_end - c.x);
-        const int p0 = unit_phys(c.x);
-        const int p1 = n == 2 ? unit_phys(c.x + 1) : -2;
+        const int n = min(C::GU, c.seg_end - c.x);
+        int pu[C::GU];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int u = 0; u < C::GU; ++u) {
+            pu[u] = u < n ? unit_phys(c.x + u) : -2;
+            bytes += pu[u] >= 0 ? 2 * C::UNITB : 0;
+        }
         if (lane == 0) {
-            if (p0 < 0 && p1 < 0) {
+            if (bytes == 0) {
                 mbar_arrive(&full[s]);
             } else {
                 uint8_t *dst = ring[s];
-                mbar_arrive_expect_tx(&full[s], (p0 >= 0 ? 2 * C::UNITB : 0) + (p1 >= 0 ? 2 * C::UNITB : 0));
-                if (p0 >= 0) {
-                    tma_unit(dst, &tmk, p0 * kPage, &full[s], policy);
-                    tma_unit(dst + 2 * C::UNITB, &tmv, p0 * kPage, &full[s], policy);
-                }
-                if (p1 >= 0) {
-                    tma_unit(dst + C::UNITB, &tmk, p1 * kPage, &full[s], policy);
-                    tma_unit(dst + 3 * C::UNITB, &tmv, p1 * kPage, &full[s], policy);
+                mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+                for (int u = 0; u < C::GU; ++u) {
+                    if (pu[u] >= 0) {
+                        tma_unit(dst + u * C::UNITB, &tmk, pu[u] * kPage, &full[s], policy);
+                        tma_unit(dst + (C::GU + u) * C::UNITB, &tmv, pu[u] * kPage, &full[s], policy);
+                    }
                 }
             }
         }
         return n;
     };
-    for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
 
     // query: raw bf16 of head fg, dims [32 ft, 32 ft + 32), fetched one
     // segment ahead; f16 B fragments of the current segment (qb0/qb1[ks]:
@@ -397,7 +412,41 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     };
     uint32_t qb0[8], qb1[8];
     float qmul = 0.f;
-    q_fetch(con.k);
+    if (!idle) {
+        q_fetch(con.k);
+        if (a.early) {
+            // everything before the validation kernel is complete (see
+            // DecodeArgs::early): the scales and the pool are final, so the
+            // first granules load now; units of requests that turn out to be
+            // rejected are dropped below, before anything reads them
+            load_scales(cphys, cks, cvs);
+            load_scales(nphys, nks, nvs);
+            for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
+        }
+    }
+
+    // ---------------- after the previous kernels: validation bits ----------------
+    if (a.early) pdl_enter();
+    if (blockIdx.x == 0) {
+        for (int k = tid; k <= K; k += C::NT) ws_prefix[k] = sm.prefix[k];
+    }
+    for (int b = tid; b < Breq; b += C::NT) sm.rflag[b] = 0;
+    __syncthreads();
+    if (a.hflags) {  // [Breq][Hkv][htiles], read in parallel
+        const int per_req = Hkv * a.htiles;
+        for (int i = tid; i < Breq * per_req; i += C::NT)
+            if (a.hflags[i]) sm.rflag[i / per_req] = 1;
+    }
+    __syncthreads();
+    if (idle) return;  // no block-wide barrier follows
+    skip_rejected(creq, cphys, cbad);
+    skip_rejected(nreq, nphys, nbad);
+    if (!a.early) {
+        load_scales(cphys, cks, cvs);
+        load_scales(nphys, nks, nvs);
+        for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
+    }
+
 
     // fragment offsets inside a swizzled 2 KB slab
     // K (A of S = K Q^T): rows fg and fg + 8, logical chunks 2 ft and 2 ft + 1
@@ -434,7 +483,9 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
         if (con.x >= base + 32) {
             base += 32;
             cphys = nphys; cks = nks; cvs = nvs; cbad = nbad;
-            load_ids(base + 32, nphys, nbad);
+            int req;
+            load_ids(base + 32, nphys, nbad, req);
+            skip_rejected(req, nphys, nbad);
             pending_scales = true;
         }
         if (seg_start) {
@@ -462,153 +513,176 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
             if (con.seg_end < x1) q_fetch(seg_of(sm.prefix, K, con.seg_end));
             seg_start = false;
         }
-        const int n_units = min(2, con.seg_end - con.x);
-        const UnitMeta u0m = unit_meta(con.x);
-        UnitMeta u1m = {-2, 0.f, 0.f, 0u};
-        if (n_units == 2) u1m = unit_meta(con.x + 1);
-        seg_status |= u0m.bad | u1m.bad;
+        const int n_units = min(C::GU, con.seg_end - con.x);
+        UnitMeta um[C::GU];
+        int nv[C::GU];
         const int seg_last = sm.prefix[con.k + 1] - 1;
         const int lnv = sm.last_nv[con.k];
-        int nv[2];
-        nv[0] = u0m.phys >= 0 ? (con.x == seg_last ? lnv : kPage) : 0;
-        nv[1] = u1m.phys >= 0 ? (con.x + 1 == seg_last ? lnv : kPage) : 0;
-        const float ksc[2] = {u0m.ks, u1m.ks};
+        bool full_gran = n_units == C::GU;
+#pragma unroll
+        for (int u = 0; u < C::GU; ++u) {
+            um[u] = UnitMeta{-2, 0.f, 0.f, 0u};
+            if (u < n_units) um[u] = unit_meta(con.x + u);
+            seg_status |= um[u].bad;
+            nv[u] = um[u].phys >= 0 ? (con.x + u == seg_last ? lnv : kPage) : 0;
+            full_gran = full_gran && nv[u] == kPage;
+        }
 
         if (!mbar_wait_bounded(&full[s], parity)) seg_status |= kStatusTimeout;
         const uint8_t *stage = ring[s];
 
-        // ---- scores: S = K Q^T per unit; sc[u][j]: token fg (+8 for j >= 2),
-        //      head 2 ft (+1 for odd j); -inf outside the unit's live rows ----
-        float sc[2][4];
+        // One granule.  FULL: every unit holds 16 live tokens, so no unit needs
+        // a check and the units' MMA chains interleave.
+        auto granule = [&](auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
+            // ---- scores: S = K Q^T per unit; sc[u][j]: token fg (+8 for j >= 2),
+            //      head 2 ft (+1 for odd j); -inf outside the unit's live rows ----
+            float sc[C::GU][4];
+            float c0[C::GU][4], c1[C::GU][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-            if (nv[u] > 0) {
-                const uint8_t *kb = stage + u * C::UNITB;
-                const uint4 ra0 = lds128(kb + offK0), ra1 = lds128(kb + offK1);
-                const uint4 rb0 = lds128(kb + 8 * C::ROWB + offK0), rb1 = lds128(kb + 8 * C::ROWB + offK1);
+            for (int u = 0; u < C::GU; ++u) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t wa = word_of(ks < 4 ? ra0 : ra1, ks & 3);
-                    const uint32_t wb = word_of(ks < 4 ? rb0 : rb1, ks & 3);
-                    uint32_t a0, a2, a1, a3;
-                    e4m3x4_to_f16x2(wa, a0, a2);
-                    e4m3x4_to_f16x2(wb, a1, a3);
-                    if (ks & 1) mma_16816(c1, a0, a1, a2, a3, qb0[ks], qb1[ks]);
-                    else mma_16816(c0, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+                for (int j = 0; j < 4; ++j) c0[u][j] = c1[u][j] = 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < C::GU; ++u) {
+                if (FULL || nv[u] > 0) {
+                    const uint8_t *kb = stage + u * C::UNITB;
+                    const uint4 ra0 = lds128(kb + offK0), ra1 = lds128(kb + offK1);
+                    const uint4 rb0 = lds128(kb + 8 * C::ROWB + offK0), rb1 = lds128(kb + 8 * C::ROWB + offK1);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t wa = word_of(ks < 4 ? ra0 : ra1, ks & 3);
+                        const uint32_t wb = word_of(ks < 4 ? rb0 : rb1, ks & 3);
+                        uint32_t a0, a2, a1, a3;
+                        e4m3x4_to_f16x2(wa, a0, a2);
+                        e4m3x4_to_f16x2(wb, a1, a3);
+                        if (ks & 1) mma_16816(c1[u], a0, a1, a2, a3, qb0[ks], qb1[ks]);
+                        else mma_16816(c0[u], a0, a1, a2, a3, qb0[ks], qb1[ks]);
+                    }
                 }
             }
-            const float f = qmul * ksc[u];
-            const bool lo_ok = fg < nv[u], hi_ok = fg + 8 < nv[u];
-            sc[u][0] = lo_ok ? (c0[0] + c1[0]) * f : -INFINITY;
-            sc[u][1] = lo_ok ? (c0[1] + c1[1]) * f : -INFINITY;
-            sc[u][2] = hi_ok ? (c0[2] + c1[2]) * f : -INFINITY;
-            sc[u][3] = hi_ok ? (c0[3] + c1[3]) * f : -INFINITY;
-            if (MASS) {  // scores for the attention-mass pass
-                const int bh = con.k / nchunks, c = con.k - bh * nchunks;
-                const int tok0 = (c * (chunk_tokens / kPage) + (con.x + u - sm.prefix[con.k])) * kPage + fg;
-                float *dst = a.mscore + ((long long)bh * a.mlen + tok0) * G;
-                if (2 * ft < G) {
-                    if (lo_ok) dst[2 * ft] = sc[u][0];
-                    if (hi_ok) dst[8 * G + 2 * ft] = sc[u][2];
+#pragma unroll
+            for (int u = 0; u < C::GU; ++u) {
+                const float f = qmul * um[u].ks;
+                const bool lo_ok = FULL || fg < nv[u], hi_ok = FULL || fg + 8 < nv[u];
+                sc[u][0] = lo_ok ? (c0[u][0] + c1[u][0]) * f : -INFINITY;
+                sc[u][1] = lo_ok ? (c0[u][1] + c1[u][1]) * f : -INFINITY;
+                sc[u][2] = hi_ok ? (c0[u][2] + c1[u][2]) * f : -INFINITY;
+                sc[u][3] = hi_ok ? (c0[u][3] + c1[u][3]) * f : -INFINITY;
+                if (MASS) {  // scores for the attention-mass pass
+                    const int bh = con.k / nchunks, c = con.k - bh * nchunks;
+                    const int tok0 = (c * (chunk_tokens / kPage) + (con.x + u - sm.prefix[con.k])) * kPage + fg;
+                    float *dst = a.mscore + ((long long)bh * a.mlen + tok0) * G;
+                    if (2 * ft < G) {
+                        if (lo_ok) dst[2 * ft] = sc[u][0];
+                        if (hi_ok) dst[8 * G + 2 * ft] = sc[u][2];
+                    }
+                    if (2 * ft + 1 < G) {
+                        if (lo_ok) dst[2 * ft + 1] = sc[u][1];
+                        if (hi_ok) dst[8 * G + 2 * ft + 1] = sc[u][3];
+                    }
                 }
-                if (2 * ft + 1 < G) {
-                    if (lo_ok) dst[2 * ft + 1] = sc[u][1];
-                    if (hi_ok) dst[8 * G + 2 * ft + 1] = sc[u][3];
+            }
+
+            // ---- online softmax: granule max per head over the token rows ----
+            float mbA = fmaxf(sc[0][0], sc[0][2]), mbB = fmaxf(sc[0][1], sc[0][3]);
+#pragma unroll
+            for (int u = 1; u < C::GU; ++u) {
+                mbA = fmaxf(mbA, fmaxf(sc[u][0], sc[u][2]));
+                mbB = fmaxf(mbB, fmaxf(sc[u][1], sc[u][3]));
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mbA = fmaxf(mbA, __shfl_xor_sync(0xffffffffu, mbA, off));
+                mbB = fmaxf(mbB, __shfl_xor_sync(0xffffffffu, mbB, off));
+            }
+            const bool grow = mbA > mA + kLazy || mbB > mB + kLazy;
+            // V-scale reference: 2^eO bounds every live unit's V scale seen so far
+            int eneed = kNoScale;
+#pragma unroll
+            for (int u = 0; u < C::GU; ++u)
+                if (FULL || nv[u] > 0) eneed = max(eneed, exp_above(um[u].vs));
+            const bool scale_up = eneed > eO;
+            float fA = 1.f, fB = 1.f;
+            if (scale_up) {
+                const int d = eO - eneed;  // < 0
+                const float r = (eO == kNoScale || d < -126) ? 0.f : pow2i(d);
+                fA = fB = r;
+                eO = eneed;
+                vref = pow2i(-eO);
+            }
+            if (grow) {
+                const float nA = fmaxf(mA, mbA), nB = fmaxf(mB, mbB);
+                const float aA = mA == -INFINITY ? 0.f : pexp2(mA - nA);
+                const float aB = mB == -INFINITY ? 0.f : pexp2(mB - nB);
+                mA = nA;
+                mB = nB;
+                lA *= aA;
+                lB *= aB;
+                fA *= aA;
+                fB *= aB;
+            }
+            if (grow || scale_up) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    o[mt][0] *= fA;
+                    o[mt][2] *= fA;
+                    o[mt][1] *= fB;
+                    o[mt][3] *= fB;
                 }
             }
-        }
 
-        // ---- online softmax: granule max per head over the 8 token rows ----
-        float mbA = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
-        float mbB = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+            // ---- probabilities -> B fragments of the V product; V product ----
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mbA = fmaxf(mbA, __shfl_xor_sync(0xffffffffu, mbA, off));
-            mbB = fmaxf(mbB, __shfl_xor_sync(0xffffffffu, mbB, off));
-        }
-        const bool grow = mbA > mA + kLazy || mbB > mB + kLazy;
-        // V-scale reference: 2^eO bounds every live unit's V scale seen so far
-        int eneed = kNoScale;
-        if (nv[0] > 0) eneed = exp_above(u0m.vs);
-        if (nv[1] > 0) eneed = max(eneed, exp_above(u1m.vs));
-        const bool scale_up = eneed > eO;
-        float fA = 1.f, fB = 1.f;
-        if (scale_up) {
-            const int d = eO - eneed;  // < 0
-            const float r = (eO == kNoScale || d < -126) ? 0.f : pow2i(d);
-            fA = fB = r;
-            eO = eneed;
-            vref = pow2i(-eO);
-        }
-        if (grow) {
-            const float nA = fmaxf(mA, mbA), nB = fmaxf(mB, mbB);
-            const float aA = mA == -INFINITY ? 0.f : pexp2(mA - nA);
-            const float aB = mB == -INFINITY ? 0.f : pexp2(mB - nB);
-            mA = nA;
-            mB = nB;
-            lA *= aA;
-            lB *= aB;
-            fA *= aA;
-            fB *= aB;
-        }
-        if (grow || scale_up) {
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= fA;
-                o[mt][2] *= fA;
-                o[mt][1] *= fB;
-                o[mt][3] *= fB;
-            }
-        }
+            for (int u = 0; u < C::GU; ++u) {
+                const bool lo_ok = FULL || fg < nv[u], hi_ok = FULL || fg + 8 < nv[u];
+                const float pA0 = lo_ok ? pexp2(sc[u][0] - mA) : 0.f;
+                const float pB0 = lo_ok ? pexp2(sc[u][1] - mB) : 0.f;
+                const float pA1 = hi_ok ? pexp2(sc[u][2] - mA) : 0.f;
+                const float pB1 = hi_ok ? pexp2(sc[u][3] - mB) : 0.f;
+                lA += pA0 + pA1;
+                lB += pB0 + pB1;
+                if (!FULL && nv[u] == 0) continue;  // uniform: nothing of this unit is live
+                const float vs = um[u].vs * vref;
+                // X0: head A at tokens (fg, fg + 8); X1: head B
+                const uint32_t X0 = pack_half2(pA0 * vs, pA1 * vs);
+                const uint32_t X1 = pack_half2(pB0 * vs, pB1 * vs);
+                const uint32_t s00 = __shfl_sync(0xffffffffu, X0, src0), s01 = __shfl_sync(0xffffffffu, X1, src0);
+                const uint32_t s10 = __shfl_sync(0xffffffffu, X0, src1), s11 = __shfl_sync(0xffffffffu, X1, src1);
+                const uint32_t Y0 = odd_head ? s01 : s00;  // head fg, tokens (2 ft, 2 ft + 8)
+                const uint32_t Y1 = odd_head ? s11 : s10;  // head fg, tokens (2 ft + 1, 2 ft + 9)
+                const uint32_t pb0 = __byte_perm(Y0, Y1, 0x5410);  // tokens 2 ft, 2 ft + 1
+                const uint32_t pb1 = __byte_perm(Y0, Y1, 0x7632);  // tokens 2 ft + 8, 2 ft + 9
 
-        // ---- probabilities -> B fragments of the V product; V product ----
+                const uint8_t *vb = stage + (C::GU + u) * C::UNITB;
+                uint4 r0 = lds128(vb + offV0), r1 = lds128(vb + offV1);
+                uint4 r2 = lds128(vb + 8 * C::ROWB + offV0), r3 = lds128(vb + 8 * C::ROWB + offV1);
+                if (!FULL && nv[u] < kPage) {
+                    // rows past the live tokens may hold stale bytes (even NaN
+                    // codes): zero them so that 0 x row stays 0
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    if (2 * ft >= nv[u]) r0 = z;
+                    if (2 * ft + 1 >= nv[u]) r1 = z;
+                    if (2 * ft + 8 >= nv[u]) r2 = z;
+                    if (2 * ft + 9 >= nv[u]) r3 = z;
+                }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const bool lo_ok = fg < nv[u], hi_ok = fg + 8 < nv[u];
-            const float pA0 = lo_ok ? pexp2(sc[u][0] - mA) : 0.f;
-            const float pB0 = lo_ok ? pexp2(sc[u][1] - mB) : 0.f;
-            const float pA1 = hi_ok ? pexp2(sc[u][2] - mA) : 0.f;
-            const float pB1 = hi_ok ? pexp2(sc[u][3] - mB) : 0.f;
-            lA += pA0 + pA1;
-            lB += pB0 + pB1;
-            if (nv[u] == 0) continue;  // uniform: nothing of this unit is live
-            const float vs = (u ? u1m.vs : u0m.vs) * vref;
-            // X0: head A at tokens (fg, fg + 8); X1: head B
-            const uint32_t X0 = pack_half2(pA0 * vs, pA1 * vs);
-            const uint32_t X1 = pack_half2(pB0 * vs, pB1 * vs);
-            const uint32_t s00 = __shfl_sync(0xffffffffu, X0, src0), s01 = __shfl_sync(0xffffffffu, X1, src0);
-            const uint32_t s10 = __shfl_sync(0xffffffffu, X0, src1), s11 = __shfl_sync(0xffffffffu, X1, src1);
-            const uint32_t Y0 = odd_head ? s01 : s00;  // head fg, tokens (2 ft, 2 ft + 8)
-            const uint32_t Y1 = odd_head ? s11 : s10;  // head fg, tokens (2 ft + 1, 2 ft + 9)
-            const uint32_t pb0 = __byte_perm(Y0, Y1, 0x5410);  // tokens 2 ft, 2 ft + 1
-            const uint32_t pb1 = __byte_perm(Y0, Y1, 0x7632);  // tokens 2 ft + 8, 2 ft + 9
-
-            const uint8_t *vb = stage + (2 + u) * C::UNITB;
-            uint4 r0 = lds128(vb + offV0), r1 = lds128(vb + offV1);
-            uint4 r2 = lds128(vb + 8 * C::ROWB + offV0), r3 = lds128(vb + 8 * C::ROWB + offV1);
-            if (nv[u] < kPage) {
-                // rows past the live tokens may hold stale bytes (even NaN
-                // codes): zero them so that 0 x row stays 0
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                if (2 * ft >= nv[u]) r0 = z;
-                if (2 * ft + 1 >= nv[u]) r1 = z;
-                if (2 * ft + 8 >= nv[u]) r2 = z;
-                if (2 * ft + 9 >= nv[u]) r3 = z;
+                for (int wd = 0; wd < 4; ++wd) {
+                    const uint32_t w0 = word_of(r0, wd), w1 = word_of(r1, wd);
+                    const uint32_t w2 = word_of(r2, wd), w3 = word_of(r3, wd);
+                    uint32_t a0, a1, a2, a3;
+                    e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x5140), a0, a1);  // dims 4wd, 4wd+1
+                    e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x5140), a2, a3);
+                    mma_16816(o[2 * wd], a0, a1, a2, a3, pb0, pb1);
+                    e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x7362), a0, a1);  // dims 4wd+2, 4wd+3
+                    e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x7362), a2, a3);
+                    mma_16816(o[2 * wd + 1], a0, a1, a2, a3, pb0, pb1);
+                }
             }
-#pragma unroll
-            for (int wd = 0; wd < 4; ++wd) {
-                const uint32_t w0 = word_of(r0, wd), w1 = word_of(r1, wd);
-                const uint32_t w2 = word_of(r2, wd), w3 = word_of(r3, wd);
-                uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x5140), a0, a1);  // dims 4wd, 4wd+1
-                e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x5140), a2, a3);
-                mma_16816(o[2 * wd], a0, a1, a2, a3, pb0, pb1);
-                e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x7362), a0, a1);  // dims 4wd+2, 4wd+3
-                e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x7362), a2, a3);
-                mma_16816(o[2 * wd + 1], a0, a1, a2, a3, pb0, pb1);
-            }
-        }
+        };
+        if (full_gran) granule(std::true_type{});
+        else granule(std::false_type{});
 
         const bool seg_end = con.x + n_units >= con.seg_end;
         if (seg_end) {
