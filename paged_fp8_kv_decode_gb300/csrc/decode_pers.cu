@@ -186,21 +186,40 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     const int Breq = B / a.kq;  // B counts virtual requests (see DecodeArgs::kq)
     // Without a.early, wait for the previous kernels right away.  With it, the
     // part up to the second pdl_enter() below runs while the validation kernel
-    // finishes: everything before that kernel is complete, so this part may
-    // read the call's inputs, the scales and the pool, but not the validation
-    // bits, and it writes only shared memory.
+    // finishes: it reads only inputs of the call (lengths, block tables, tags,
+    // queries), never the pool, the scales or the validation bits, and it
+    // writes only shared memory.
     if (!a.early) pdl_enter();
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
+    {
+        // pull the block-table rows into L2 while the prefix sums are built
+        const int nrows = Breq * (a.bt_sh != 0 ? Hkv : 1);
+        const int lines = (a.max_pages * 4 + 127) / 128 + 1;
+        for (int i = blockIdx.x * C::NT + tid; i < nrows * lines; i += gridDim.x * C::NT) {
+            const int r = i / lines, l = i - r * lines;
+            const int b = a.bt_sh != 0 ? r / Hkv : r, h = a.bt_sh != 0 ? r - b * Hkv : 0;
+            const long long e = min((long long)l * 32, (long long)a.max_pages - 1);
+            const int32_t *ptr = a.block_tables + (long long)b * a.bt_sb + (long long)h * a.bt_sh + e;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+        }
+    }
 
     // ---------------- prologue: unit prefix sums ----------------
     // They do not depend on the validation bits: units of rejected requests
-    // stay in the sums, and the workers skip them.
+    // stay in the sums (see skip_rejected below).
     const int per = (K + C::NT - 1) / C::NT;
     const int k0 = min(K, tid * per), k1 = min(K, k0 + per);
-    int local = 0;
+    int local = 0, nbh = -1, n = 0;
     for (int k = k0; k < k1; ++k) {
         const int bh = k / nchunks, c = k - bh * nchunks;
-        const int b = bh / Hkv, h = bh - b * Hkv;  // b: virtual request
-        const int n = query_len(a, b, h);
+        if (bh != nbh) {  // one length load per (request, head) of the range
+            const int b = bh / Hkv, h = bh - b * Hkv;  // b: virtual request
+            n = query_len(a, b, h);
+            nbh = bh;
+        }
         int units = 0, lastnv = 0;
         if (n >= 0) {
             const int pages = (n + kPage - 1) / kPage;
@@ -287,8 +306,6 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     if (!idle && lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
     __syncwarp();
     const uint64_t policy = l2_policy_evict_first();
@@ -412,18 +429,7 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     };
     uint32_t qb0[8], qb1[8];
     float qmul = 0.f;
-    if (!idle) {
-        q_fetch(con.k);
-        if (a.early) {
-            // everything before the validation kernel is complete (see
-            // DecodeArgs::early): the scales and the pool are final, so the
-            // first granules load now; units of requests that turn out to be
-            // rejected are dropped below, before anything reads them
-            load_scales(cphys, cks, cvs);
-            load_scales(nphys, nks, nvs);
-            for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
-        }
-    }
+    if (!idle) q_fetch(con.k);
 
     // ---------------- after the previous kernels: validation bits ----------------
     if (a.early) pdl_enter();
@@ -439,13 +445,12 @@ __global__ void __launch_bounds__(PersCfg::NT, 1)
     }
     __syncthreads();
     if (idle) return;  // no block-wide barrier follows
+    // no page is read before its request has passed validation
     skip_rejected(creq, cphys, cbad);
     skip_rejected(nreq, nphys, nbad);
-    if (!a.early) {
-        load_scales(cphys, cks, cvs);
-        load_scales(nphys, nks, nvs);
-        for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
-    }
+    load_scales(cphys, cks, cvs);
+    load_scales(nphys, nks, nvs);
+    for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
 
 
     // fragment offsets inside a swizzled 2 KB slab

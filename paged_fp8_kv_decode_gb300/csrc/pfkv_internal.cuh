@@ -88,9 +88,8 @@ struct DecodeArgs {
     int *ws_prefix;     // persistent kind: exclusive unit prefix per segment
     // The kernel just before the split kernel in the stream is this library's
     // validation kernel, launched by the same call.  That kernel waits for its
-    // own predecessors before it lets the split kernel start, so when the
-    // split kernel starts everything before the validation kernel is complete:
-    // inputs, pool and scales are final; only the validation bits are not.
+    // own predecessors before it lets the split kernel start, so the call's
+    // inputs are final when the split kernel starts.
     int early;
 };
 
