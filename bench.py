@@ -241,6 +241,11 @@ class PreparedMassStep(PreparedStep):
             raise RuntimeError(f"pfkv_paged_decode_attn_mass: status {st}")
 
 
+# the arithmetic of the FP8 path (head_dim 128, query groups of up to 4 heads):
+# e4m3 bytes converted exactly to f16, products on the tensor cores, fp32 sums
+FP8_DTYPE = "fp8_e4m3 KV, f16 x f16 tensor-core MMA with fp32 accumulation, bf16 q/out"
+
+
 def profiled_traffic(bytes_per_launch: float):
     """DRAM bytes per launch of the split kernel from the committed ncu summary,
     scaled to this run's algorithmic bytes; None if the kernel source changed
@@ -381,7 +386,7 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp8_e4m3 KV, fp32 accumulate, bf16 q/out", "data": "synthetic",
+            "dtype": FP8_DTYPE, "data": "synthetic",
             "config": {"workload": WORKLOAD, "batch": spec0.B, "num_q_heads": spec0.Hq,
                        "num_kv_heads": spec0.Hkv, "head_dim": spec0.D, "page_size": 16,
                        "seq_lens": "U[512,8192]+1 appended", "num_pages": spec0.num_pages,
@@ -763,7 +768,7 @@ def run_workload(args):
         "warmup": args.warmup, "ms_per_step": r0["ms_per_step"], "p10_ms": r0["p10_ms"],
         "p90_ms": r0["p90_ms"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": f"{'fp8_e4m3' if spec.kv_dtype == 'fp8' else 'bf16'} KV, fp32 accumulate, bf16 q/out",
+        "dtype": FP8_DTYPE if spec.kv_dtype == "fp8" else "bf16 KV, fp32 accumulate, bf16 q/out",
         "data": "synthetic", "config": cfg,
         "tokens_per_s": round(world * spec.B / (N_LAYERS * med_s), 1),
         "tokens_per_s_per_layer": round(world * spec.B / med_s, 1),
@@ -912,7 +917,7 @@ def run_graph(args):
             "ms_per_step": round(total / K * 1e3, 4), "median_ms": round(med, 4),
             "p10_ms": round(p10, 4), "p90_ms": round(p90, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp8_e4m3 KV, fp32 accumulate, bf16 q/out", "data": "synthetic",
+            "dtype": FP8_DTYPE, "data": "synthetic",
             "config": {"workload": "llama8b-fp8-decode-stack", "layers": n, "batch": spec.B,
                        "num_q_heads": spec.Hq, "num_kv_heads": spec.Hkv, "head_dim": spec.D,
                        "page_size": 16, "num_pages_per_layer": spec.num_pages,
@@ -1024,7 +1029,7 @@ def run_multi(args):
             "value": round(aggregate(step_bytes, K, el, world), 2), "unit": "GB/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(el / K * 1e3, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8_e4m3 KV, fp32 accumulate, bf16 q/out",
+            "vs_baseline": None, "dtype": FP8_DTYPE,
             "data": "synthetic",
             "config": {"workload": "llama8b-fp8-verify", "batch": spec0.B,
                        "query_tokens_per_request": kq, "num_q_heads": spec0.Hq,

@@ -22,6 +22,13 @@ constexpr int kValThreads = 256;
 constexpr int kValPer = 8;
 constexpr int kValTile = kValThreads * kValPer;
 
+// persistent split kernel: worker warps per CTA, and the largest segment and
+// request counts its shared-memory tables hold (the combine kernels size
+// their own tables from the same numbers)
+constexpr int kPersWorkers = 8;
+constexpr int kPersMaxSegments = 4096;
+constexpr int kPersMaxRequests = 4096;
+
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 100ull * 1000ull * 1000ull;
 
@@ -153,6 +160,12 @@ __device__ __forceinline__ uint32_t entry_bits(const DecodeArgs &a, int id, int 
     if (a.fuse_tags && a.page_tags[(long long)id * Hkv + h] != a.expected_tags[bt_index])
         return PFKV_FLAG_TAG_MISMATCH;
     return 0u;
+}
+
+// Persistent layout: the worker of global unit x when U units are shared by W
+// workers (worker w takes units [ceil(wU/W), ceil((w+1)U/W))).
+__device__ __forceinline__ int pers_worker_of(long long x, long long U, int W) {
+    return (int)((x * W) / U);
 }
 
 // Final scores of one token for the attention-mass pass (a.mscore set).
