@@ -30,22 +30,25 @@ __device__ __forceinline__ float plog2(float x) {
 }  // namespace
 
 // --------------------------------------------------------------------------
-// combine for the persistent layout: the rows of segment k are k + p for the
-// workers p that touched it.  One CTA of 16 warps per (request b, kv head h):
-//  1. the request's flags: lengths and validation bits of every kv head and
-//     the status rows of every segment of the request, in parallel;
-//  2. the rows of (b, h), flattened: chunk c owns rows [cstart[c], cstart[c+1])
-//     of the flat order, the first at workspace row cbase[c];
-//  3. M = max lse per query head, over all rows, in parallel;
-//  4. each warp accumulates exp2(lse - M)-weighted rows j = warp, warp + 16, ...
-//     (lane l owns dims [4l, 4l + 4) of every query head of the group);
-//  5. the warps' sums meet in shared memory; out = sum / weight, bf16.
+// One CTA of NW warps per (request b, kv head h), two rounds of loads (8
+// warps when a head has one chunk and few rows, 16 when it has many chunks):
+//  1. the unit prefix of every segment of the request and of every chunk of
+//     (b, h), the request's lengths and validation words; the chunks' row
+//     counts are scanned into a flat row order (chunk c owns flat rows
+//     [cstart[c], cstart[c+1]), the first at workspace row cbase[c]);
+//  2. the status rows of the request's segments (a thread per segment; lists
+//     of 8 or more rows go to a warp each) and the rows of (b, h): warp w
+//     merges flat rows w, w + NW, ..., four at a time with their loads issued
+//     together, with a running max per query head (lane l owns dims
+//     [4l, 4l + 4) of every head);
+//  the warps' (max, weight, sum) meet in shared memory; out = sum / weight,
+//  bf16, or zeros if the request carries a flag.
 // --------------------------------------------------------------------------
-constexpr int kCombThreads = 512;
-constexpr int kCombWarps = kCombThreads / 32;
 constexpr int kCombMaxChunks = kPersMaxSegments;  // segments per (b, h) <= all segments
+constexpr int kCombShortList = 8;                  // status rows a thread gathers itself
+constexpr int kCombMaxDeferred = 256;              // longer lists handed to warps
 
-template <int G>
+template <int G, int NW>
 struct CombSmem {
     union {
         struct {
@@ -53,22 +56,23 @@ struct CombSmem {
             int cbase[kCombMaxChunks];
         } rows;
         struct {
-            float acc[kCombWarps][G][128];
-            float wsum[kCombWarps][G];
+            float acc[NW][G][128];
+            float wsum[NW][G];
+            float wmax[NW][G];
         } red;
     } u;
-    int part[kCombThreads];
-    float mred[kCombWarps][G];
+    int part[NW * 32];
+    int defk[kCombMaxDeferred];
     uint32_t flags;
-    int ndef;  // segments with long row lists, gathered a warp each
+    int ndef;
 };
 
-template <int G>
-__global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
+template <int G, int NW>
+__global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
                                                                           int nchunks, int W,
                                                                           const int *ws_prefix) {
-    constexpr int D = 128, NT = kCombThreads, NW = kCombWarps;
-    __shared__ CombSmem<G> sm;
+    constexpr int D = 128, NT = NW * 32;
+    __shared__ CombSmem<G, NW> sm;
     pdl_enter();
     const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -80,54 +84,29 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
         sm.flags = 0;
         sm.ndef = 0;
     }
-    __syncthreads();
 
     // ---- 1. request flags (b is a virtual request; the flags belong to the
-    //      request rb and cover all of its query tokens) ----
+    //      request rb and cover all of its query tokens), segment row lists,
+    //      the chunks of (b, h) ----
     const int rb = b / a.kq, v0 = rb * a.kq;
     uint32_t f = 0;
     for (int i = tid; i < Hkv; i += NT)
         if (query_len(a, v0, i) < 0) f |= PFKV_FLAG_BAD_LENGTH;
     if (a.hflags)
         for (int i = tid; i < Hkv * a.htiles; i += NT) f |= a.hflags[(long long)rb * Hkv * a.htiles + i];
-    // rows of the request's segments: a thread
-    // per segment; a segment with many rows (few long segments, many workers
-    // each) is deferred to a warp whose lanes take its rows.  The deferred
-    // list borrows the row tables' space, which phase 2 fills later.
-    if (U > 0) {
-        for (int it = tid; it < a.kq * Hkv * nchunks; it += NT) {
-            const int k = v0 * Hkv * nchunks + it;
-            const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
-            if (u1 == u0) continue;
-            const int p0 = pers_worker_of(u0, U, W), p1 = pers_worker_of(u1 - 1, U, W);
-            if (p1 - p0 < 8) {
-                for (int p = p0; p <= p1; ++p) f |= a.status[k + p];
-            } else {
-                sm.u.rows.cbase[atomicAdd(&sm.ndef, 1)] = k;
-            }
+    // status rows of this thread's segment (one segment per thread covers
+    // every request of up to NT segments; more go round the loop below)
+    const int nseg = a.kq * Hkv * nchunks, kseg0 = v0 * Hkv * nchunks;
+    int sk = -1, sp0 = 0, scnt = 0;
+    if (U > 0 && tid < nseg) {
+        const int k = kseg0 + tid;
+        const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+        if (u1 > u0) {
+            sk = k;
+            sp0 = pers_worker_of(u0, U, W);
+            scnt = pers_worker_of(u1 - 1, U, W) - sp0 + 1;
         }
     }
-    if (f) atomicOr(&sm.flags, f);
-    __syncthreads();
-    f = 0;
-    for (int d = warp; d < sm.ndef; d += NW) {
-        const int k = sm.u.rows.cbase[d];
-        const int p0 = pers_worker_of(ws_prefix[k], U, W), p1 = pers_worker_of(ws_prefix[k + 1] - 1, U, W);
-        for (int p = p0 + lane; p <= p1; p += 32) f |= a.status[k + p];
-    }
-    if (f) atomicOr(&sm.flags, f);
-    __syncthreads();
-    const uint32_t flags = sm.flags;
-    if (b == v0 && h == 0 && tid == 0 && a.flags) a.flags[rb] = (uint8_t)flags;
-    if (b == v0 && h == 0 && tid == 0 && a.rflags) a.rflags[rb] = (uint8_t)flags;
-    const int n = max(0, query_len(a, b, h));
-    uint2 *out = reinterpret_cast<uint2 *>(a.out + (long long)(b * Hkv + h) * G * D);
-    if (flags != 0 || n == 0 || U == 0) {
-        for (int i = tid; i < G * D / 4; i += NT) out[i] = make_uint2(0u, 0u);
-        return;
-    }
-
-    // ---- 2. flat row order: per-thread chunk ranges, scanned by one warp ----
     const int kbase = (b * Hkv + h) * nchunks;
     const int per = (nchunks + NT - 1) / NT;
     const int c0 = min(nchunks, tid * per), c1 = min(nchunks, c0 + per);
@@ -136,7 +115,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
         const int k = kbase + c;
         const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
         int cnt = 0, base = 0;
-        if (u1 > u0) {
+        if (U > 0 && u1 > u0) {
             const int p0 = pers_worker_of(u0, U, W), p1 = pers_worker_of(u1 - 1, U, W);
             cnt = p1 - p0 + 1;
             base = k + p0;
@@ -181,85 +160,140 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_pers_kernel(Decod
             if (sm.u.rows.cstart[mid] <= j) lo = mid;
             else hi = mid;
         }
-        return sm.u.rows.cbase[lo] + (j - sm.u.rows.cstart[lo]);
+        return (long long)sm.u.rows.cbase[lo] + (j - sm.u.rows.cstart[lo]);
     };
 
-    // ---- 3. M per query head (thread tid always sees head tid % G) ----
-    const int gm = tid % G;
-    float mx = -INFINITY;
-    for (int idx = tid; idx < R * G; idx += NT) mx = fmaxf(mx, a.lse[(long long)row_of(idx / G) * G + gm]);
+    // ---- 2. status rows (loaded now, used after the merge) and the rows ----
+    uint32_t st[kCombShortList];
 #pragma unroll
-    for (int off = 16; off >= G; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane < G) sm.mred[warp][lane] = mx;
-    __syncthreads();
-    float M[G];
+    for (int i = 0; i < kCombShortList; ++i) st[i] = 0u;
+    if (scnt > 0 && scnt <= kCombShortList) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        M[g] = sm.mred[0][g];
-#pragma unroll
-        for (int w2 = 1; w2 < NW; ++w2) M[g] = fmaxf(M[g], sm.mred[w2][g]);
+        for (int i = 0; i < kCombShortList; ++i)
+            if (i < scnt) st[i] = a.status[sk + sp0 + i];
     }
-
-    // ---- 4. weighted sums, rows spread over the warps ----
+    float M[G], S[G];
     float4 acc[G];
-    float wsum[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
+        M[g] = -INFINITY;
+        S[g] = 0.f;
         acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-        wsum[g] = 0.f;
     }
-#pragma unroll 4
-    for (int j = warp; j < R; j += NW) {
-        const long long row = row_of(j);
+    constexpr int RB = 4;  // rows in flight per warp
+    for (int j0 = warp; j0 < R; j0 += RB * NW) {
+        float lc[RB][G];
+        float4 ov[RB][G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float lc = a.lse[row * G + g];
-            const float wt = lc == -INFINITY ? 0.f : pexp2(lc - M[g]);
-            const float4 ov = *reinterpret_cast<const float4 *>(a.o + (row * G + g) * D + lane * 4);
-            wsum[g] += wt;
-            acc[g].x = fmaf(wt, ov.x, acc[g].x);
-            acc[g].y = fmaf(wt, ov.y, acc[g].y);
-            acc[g].z = fmaf(wt, ov.z, acc[g].z);
-            acc[g].w = fmaf(wt, ov.w, acc[g].w);
+        for (int r = 0; r < RB; ++r) {
+            const int j = j0 + r * NW;
+            const long long row = j < R ? row_of(j) : 0;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                lc[r][g] = j < R ? a.lse[row * G + g] : -INFINITY;
+                ov[r][g] = j < R ? *reinterpret_cast<const float4 *>(a.o + (row * G + g) * D + lane * 4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                if (lc[r][g] == -INFINITY) continue;  // uniform: no token of this head in the row
+                if (lc[r][g] > M[g]) {
+                    const float sc = M[g] == -INFINITY ? 0.f : pexp2(M[g] - lc[r][g]);
+                    S[g] *= sc;
+                    acc[g].x *= sc;
+                    acc[g].y *= sc;
+                    acc[g].z *= sc;
+                    acc[g].w *= sc;
+                    M[g] = lc[r][g];
+                }
+                const float wt = pexp2(lc[r][g] - M[g]);
+                S[g] += wt;
+                acc[g].x = fmaf(wt, ov[r][g].x, acc[g].x);
+                acc[g].y = fmaf(wt, ov[r][g].y, acc[g].y);
+                acc[g].z = fmaf(wt, ov[r][g].z, acc[g].z);
+                acc[g].w = fmaf(wt, ov[r][g].w, acc[g].w);
+            }
         }
     }
-    __syncthreads();  // the row tables are dead: their space takes the sums
+#pragma unroll
+    for (int i = 0; i < kCombShortList; ++i) f |= st[i];
+    if (scnt > kCombShortList) {  // a long list: a warp takes it below
+        const int d = atomicAdd(&sm.ndef, 1);
+        if (d < kCombMaxDeferred) sm.defk[d] = tid;
+        else
+            for (int p = 0; p < scnt; ++p) f |= a.status[sk + sp0 + p];
+    }
+    // segments beyond the first NT of the request (long requests with many
+    // chunks): the same gathering, a thread per segment
+    for (int it = tid + NT; U > 0 && it < nseg; it += NT) {
+        const int k = kseg0 + it;
+        const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+        if (u1 == u0) continue;
+        const int p0 = pers_worker_of(u0, U, W), p1 = pers_worker_of(u1 - 1, U, W);
+        for (int p = p0; p <= p1; ++p) f |= a.status[k + p];
+    }
+    __syncthreads();  // deferred list complete; the row tables are dead
+    {
+        const int ndef = min(sm.ndef, kCombMaxDeferred);
+        for (int d = warp; d < ndef; d += NW) {
+            const int t = sm.defk[d];  // the thread that found the list
+            const int k = kseg0 + t;
+            const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+            const int p0 = pers_worker_of(u0, U, W), p1 = pers_worker_of(u1 - 1, U, W);
+            for (int p = p0 + lane; p <= p1; p += 32) f |= a.status[k + p];
+        }
+    }
+    if (f) atomicOr(&sm.flags, f);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         *reinterpret_cast<float4 *>(&sm.u.red.acc[warp][g][lane * 4]) = acc[g];
-        if (lane == 0) sm.u.red.wsum[warp][g] = wsum[g];
+        if (lane == 0) {
+            sm.u.red.wsum[warp][g] = S[g];
+            sm.u.red.wmax[warp][g] = M[g];
+        }
     }
     __syncthreads();
+    const uint32_t flags = sm.flags;
+    if (b == v0 && h == 0 && tid == 0 && a.flags) a.flags[rb] = (uint8_t)flags;
+    if (b == v0 && h == 0 && tid == 0 && a.rflags) a.rflags[rb] = (uint8_t)flags;
+    const int n = max(0, query_len(a, b, h));
+    uint2 *out = reinterpret_cast<uint2 *>(a.out + (long long)(b * Hkv + h) * G * D);
+    if (flags != 0 || n == 0 || U == 0) {
+        for (int i = tid; i < G * D / 4; i += NT) out[i] = make_uint2(0u, 0u);
+        return;
+    }
 
-    // ---- 5. out = sum over warps / weight over warps ----
+    // ---- out = merged sum / merged weight ----
     for (int i = tid; i < G * D / 4; i += NT) {
         const int g = i / (D / 4), d4 = i - g * (D / 4);
+        float Mg = -INFINITY;
+#pragma unroll
+        for (int w2 = 0; w2 < NW; ++w2) Mg = fmaxf(Mg, sm.u.red.wmax[w2][g]);
         float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
         float ws = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < NW; ++w2) {
+            const float mw = sm.u.red.wmax[w2][g];
+            const float sc = mw == -INFINITY ? 0.f : pexp2(mw - Mg);
             const float4 v = *reinterpret_cast<const float4 *>(&sm.u.red.acc[w2][g][d4 * 4]);
-            s4.x += v.x;
-            s4.y += v.y;
-            s4.z += v.z;
-            s4.w += v.w;
-            ws += sm.u.red.wsum[w2][g];
+            s4.x = fmaf(sc, v.x, s4.x);
+            s4.y = fmaf(sc, v.y, s4.y);
+            s4.z = fmaf(sc, v.z, s4.z);
+            s4.w = fmaf(sc, v.w, s4.w);
+            ws = fmaf(sc, sm.u.red.wsum[w2][g], ws);
         }
         const float inv = ws > 0.f ? 1.f / ws : 0.f;
-        if (a.lse_fin && d4 == 0) {
-            float Mg = M[0];  // M[g] without a dynamically indexed register array
-#pragma unroll
-            for (int x = 1; x < G; ++x) Mg = g == x ? M[x] : Mg;
+        if (a.lse_fin && d4 == 0)
             a.lse_fin[(long long)(b * Hkv + h) * G + g] = ws > 0.f ? Mg + plog2(ws) : -INFINITY;
-        }
         const __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x * inv, s4.y * inv);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z * inv, s4.w * inv);
         out[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
                             *reinterpret_cast<const uint32_t *>(&hi));
     }
 }
-
-
 
 // --------------------------------------------------------------------------
 // host side
@@ -269,8 +303,12 @@ namespace {
 template <int G>
 cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     const int W = p.pers_ctas * kPersWorkers;
-    return launch_pdl(decode_combine_pers_kernel<G>, dim3((unsigned)(p.B * p.Hkv)), dim3(kCombThreads), 0, s, a,
-                      p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+    const dim3 grid((unsigned)(p.B * p.Hkv));
+    if (p.nchunks == 1)
+        return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks, W,
+                          (const int *)a.ws_prefix);
+    return launch_pdl(decode_combine_pers_kernel<G, 16>, grid, dim3(16 * 32), 0, s, a, p.Hkv, p.nchunks, W,
+                      (const int *)a.ws_prefix);
 }
 
 }  // namespace
