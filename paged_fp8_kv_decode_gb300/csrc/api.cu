@@ -126,7 +126,10 @@ pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_he
                                                          : kPage);
     q.nchunks = max_seq_len > 0 ? (max_seq_len + q.chunk_tokens - 1) / q.chunk_tokens : 1;
     q.pers_ctas = num_sms;
-    q.workers = num_sms * pers_workers_per_cta();
+    // every (virtual request, kv head) at max_seq_len: an upper bound on the units
+    const long long units_bound =
+        (long long)q.B * q.Hkv * (max_seq_len > 0 ? (max_seq_len + kPage - 1) / kPage : 1);
+    q.workers = num_sms * pers_workers_for(units_bound, num_sms);
     if (!pers_supported(q, c->num_pages)) {
         q.kind = 0;
         q.chunk_tokens = split_tokens > 0 ? split_tokens

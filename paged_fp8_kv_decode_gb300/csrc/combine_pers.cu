@@ -302,7 +302,7 @@ namespace {
 
 template <int G>
 cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    const int W = p.pers_ctas * kPersWorkers;
+    const int W = p.workers;  // as the plan sized the split kernel
     const dim3 grid((unsigned)(p.B * p.Hkv));
     if (p.nchunks == 1)
         return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks, W,

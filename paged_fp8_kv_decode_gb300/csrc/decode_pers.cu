@@ -125,18 +125,22 @@ constexpr int kNoScale = -1000; // V-scale reference of a worker that has seen n
 
 }  // namespace
 
-// Kernel shape: units per granule (one ring stage) and worker warps per CTA.
+// Kernel shape: units per granule (one ring stage), worker warps per CTA and
+// ring stages per worker.  Two shapes are built, both with 192 KB of rings:
+// 8 workers x 3 stages, and 12 workers x 2 stages, which hides more latency
+// when every worker streams long runs (see pers_workers_for).
 constexpr int kGranUnits = 2;
-constexpr int kWorkers = kPersWorkers;
 
+template <int WK>
 struct PersCfg {
+    static_assert(WK == 8 || WK == 12, "8 or 12 workers per CTA");
     static constexpr int D = 128;
     static constexpr int ROWB = 128;
     static constexpr int UNITB = kPage * ROWB;   // 2 KB
     static constexpr int GU = kGranUnits;
     static constexpr int STAGEB = 2 * GU * UNITB;  // K u0 .. K u(GU-1) | V u0 .. V u(GU-1)
-    static constexpr int WORKERS = kWorkers;
-    static constexpr int STAGES = 3;
+    static constexpr int WORKERS = WK;
+    static constexpr int STAGES = WK == 8 ? 3 : 2;
     static constexpr int NT = WORKERS * 32;
     static constexpr int MAXK = kPersMaxSegments;  // segments (prefix array in smem)
     static constexpr int MAXB = kPersMaxRequests;  // requests
@@ -165,12 +169,12 @@ __device__ __forceinline__ int seg_of(const int *prefix, int K, int x) {
 // MASS: also store every live token's final scores for the attention-mass
 // pass (a separate instantiation, so that the plain kernel carries no trace of
 // it in its inner loop).
-template <int G, bool MASS>
-__global__ void __launch_bounds__(PersCfg::NT, 1)
+template <int G, bool MASS, int WK>
+__global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
     decode_split_pers_kernel(const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, DecodeArgs a, int Hkv, int B,
                              int nchunks, int chunk_tokens, int *ws_prefix) {
-    using C = PersCfg;
+    using C = PersCfg<WK>;
     constexpr int ST = C::STAGES;
     static_assert(G == 1 || G == 2 || G == 4, "query groups of 1, 2 or 4 heads");
     extern __shared__ uint8_t smem_raw[];
@@ -760,9 +764,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long rows) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)PersCfg::ROWB, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)PersCfg::ROWB};
-    const cuuint32_t box[2] = {(cuuint32_t)PersCfg::ROWB, (cuuint32_t)kPage};
+    const cuuint64_t dims[2] = {(cuuint64_t)PersCfg<8>::ROWB, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)PersCfg<8>::ROWB};
+    const cuuint32_t box[2] = {(cuuint32_t)PersCfg<8>::ROWB, (cuuint32_t)kPage};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pages), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -770,9 +774,9 @@ cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int G, bool MASS>
+template <int G, bool MASS, int WK>
 cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    using C = PersCfg;
+    using C = PersCfg<WK>;
     const size_t smem = sizeof(typename C::Smem) + 1024;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
@@ -780,7 +784,7 @@ cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(decode_split_pers_kernel<G, MASS>,
+        e = cudaFuncSetAttribute(decode_split_pers_kernel<G, MASS, WK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
@@ -789,24 +793,40 @@ cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_
     alignas(64) CUtensorMap tmk, tmv;
     if ((e = pool_tensor_map(&tmk, a.k_pages, rows)) != cudaSuccess) return e;
     if ((e = pool_tensor_map(&tmv, a.v_pages, rows)) != cudaSuccess) return e;
-    return launch_pdl(decode_split_pers_kernel<G, MASS>, dim3(p.pers_ctas), dim3(C::NT), smem, s, tmk, tmv,
-                      a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
+    return launch_pdl(decode_split_pers_kernel<G, MASS, WK>, dim3(p.pers_ctas), dim3(C::NT), smem, s, tmk,
+                      tmv, a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
+}
+
+template <int G, int WK>
+cudaError_t launch_pers_gw(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    return a.mscore ? launch_pers_gm<G, true, WK>(a, p, s) : launch_pers_gm<G, false, WK>(a, p, s);
 }
 
 template <int G>
 cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    return a.mscore ? launch_pers_gm<G, true>(a, p, s) : launch_pers_gm<G, false>(a, p, s);
+    switch (p.pers_ctas > 0 ? p.workers / p.pers_ctas : 0) {
+        case 8: return launch_pers_gw<G, 8>(a, p, s);
+        case 12: return launch_pers_gw<G, 12>(a, p, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int pers_workers_per_cta() { return PersCfg::WORKERS; }
+// 12 workers when each SM has more than 8 x 192 units to stream (by the
+// host-known bound: every head at max_seq_len); 8 otherwise.  Measured on the
+// GB300: 12 x 2 stages was 6% faster on 128K-512K contexts and 4% faster on a
+// 64 x 32K batch, but 4% slower on a batch of 32 lengths up to 8K, where the
+// per-worker startup and the partial rows weigh more.
+int pers_workers_for(long long units_bound, int num_sms) {
+    return units_bound > (long long)num_sms * 8 * 192 ? 12 : 8;
+}
 
 bool pers_supported(const DecodePlan &p, int num_pages) {
     const long long rows = (long long)num_pages * p.Hkv * kPage;
     const long long K = (long long)p.B * p.Hkv * p.nchunks;
     return p.dtype == PFKV_KV_FP8_E4M3 && p.D == 128 && p.G <= 4 && rows < (1LL << 31) &&
-           K <= PersCfg::MAXK && p.Breq <= PersCfg::MAXB;
+           K <= kPersMaxSegments && p.Breq <= kPersMaxRequests;
 }
 
 cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {

@@ -22,10 +22,9 @@ constexpr int kValThreads = 256;
 constexpr int kValPer = 8;
 constexpr int kValTile = kValThreads * kValPer;
 
-// persistent split kernel: worker warps per CTA, and the largest segment and
-// request counts its shared-memory tables hold (the combine kernels size
-// their own tables from the same numbers)
-constexpr int kPersWorkers = 8;
+// persistent split kernel: the largest segment and request counts its
+// shared-memory tables hold (the combine kernels size their own tables from
+// the same numbers)
 constexpr int kPersMaxSegments = 4096;
 constexpr int kPersMaxRequests = 4096;
 
@@ -204,7 +203,7 @@ cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t 
 cudaError_t launch_mass(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 bool swz_supported(const DecodePlan &p, int num_pages);
 bool pers_supported(const DecodePlan &p, int num_pages);
-int pers_workers_per_cta();
+int pers_workers_for(long long units_bound, int num_sms);
 cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_split_swz(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);

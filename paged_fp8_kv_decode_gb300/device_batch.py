@@ -24,7 +24,8 @@ def _i32(a: np.ndarray, device) -> torch.Tensor:
 class DeviceBatch:
     def __init__(self, batch: W.Batch, device="cuda", keep_rows: bool = False,
                  tags: Optional[bool] = None, fill_chunk_tokens: int = 8192, rows=None,
-                 q: Optional[torch.Tensor] = None, fused_tags: bool = False):
+                 q: Optional[torch.Tensor] = None, fused_tags: bool = False,
+                 max_seq_len: Optional[int] = None):
         spec = batch.spec
         self.spec, self.batch, self.device = spec, batch, device
         self.fused_tags = fused_tags  # tag check inside the attention kernel
@@ -55,6 +56,8 @@ class DeviceBatch:
         self.pages_untracked = B.Pages(spec.B, batch.max_pages, self.block_tables, tb, th,
                                        self.fill_lens, sb, sh, None)
         self.max_seq_len = int(batch.seq_lens.max()) if batch.seq_lens.size else 0
+        if max_seq_len is not None:  # a looser host-known bound, as a caller may pass
+            self.max_seq_len = max(self.max_seq_len, int(max_seq_len))
         self.q = W.draw_q(spec, device=device) if q is None else q.to(device).contiguous()
         self.out = torch.empty((spec.B, spec.Hq, D), dtype=torch.bfloat16, device=device)
         nflag = max(4, (spec.B + 3) // 4 * 4)

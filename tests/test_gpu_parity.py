@@ -35,11 +35,12 @@ def _db(batch, **kw):
     return DeviceBatch(batch, keep_rows=True, **kw)
 
 
-def run_and_compare(spec, tags=None, rows=None, q=None, label="", fused_tags=False):
+def run_and_compare(spec, tags=None, rows=None, q=None, label="", fused_tags=False,
+                    max_seq_len=None):
     """Fill, append, attend on the GPU and on the oracle; compare everything."""
     batch = W.make_batch(spec)
     use_tags = spec.tags if tags is None else tags
-    db = _db(batch, tags=use_tags, rows=rows, q=q, fused_tags=fused_tags)
+    db = _db(batch, tags=use_tags, rows=rows, q=q, fused_tags=fused_tags, max_seq_len=max_seq_len)
     ref = oracle_reference(spec, batch, db.k_rows.cpu(), db.v_rows.cpu(), db.q.cpu(),
                            None if db.k_new is None else db.k_new.cpu(),
                            None if db.v_new is None else db.v_new.cpu(), tags=use_tags)
@@ -79,6 +80,15 @@ def test_tiny_bf16(B):
 def test_llama8b_small_fp8_append(B, split):
     spec = dataclasses.replace(W.spec_llama8b("small"), split_tokens=split)
     run_and_compare(spec, label=f"llama8b-small split={split}")
+
+
+@pytest.mark.parametrize("split", [0, 1024])
+def test_twelve_worker_shape(B, split):
+    """A large host-known length bound (4 requests x 8 kv heads x 8,192 units,
+    above 8 x 192 units per SM) selects the split kernel's 12-worker shape,
+    while the actual lengths stay small enough for the oracle."""
+    spec = dataclasses.replace(W.spec_llama8b("small"), split_tokens=split)
+    run_and_compare(spec, label=f"llama8b-small 12 workers split={split}", max_seq_len=131072)
 
 
 def test_long_small_split(B):
