@@ -204,6 +204,19 @@ class PreparedStep:
                                 None, 1, db.k_new.data_ptr(), db.v_new.data_ptr(),
                                 db.append_flags.data_ptr(), stream_handle)
 
+    def full_step(self):
+        """The whole step through the public API: pfkv_decode_step (append and
+        attention in one call) where the workload appends, else the attention
+        call with every stage."""
+        if self.append_args is None:
+            self.stage(self.B.PFKV_STAGE_ALL)
+            return
+        a = self.append_args
+        st = self.L.pfkv_decode_step(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], *self.args[2:],
+                                     self.opt, self.s)
+        if st:
+            raise RuntimeError(f"pfkv_decode_step: status {st}")
+
     def append(self):
         if self.append_args is not None:
             st = self.L.pfkv_kv_append(*self.append_args)
@@ -316,10 +329,10 @@ def run_gpu(args):
     S_V, S_S, S_C = B.PFKV_STAGE_VALIDATE, B.PFKV_STAGE_SPLIT, B.PFKV_STAGE_COMBINE
 
     def one_step(p, ev=None):
-        p.append()
         if ev is None:
-            p.stage(S_ALL)
-        else:
+            p.full_step()
+        else:  # the split kernel timed alone: the same work as separate calls
+            p.append()
             p.stage(S_V)
             ev[0].record(stream)
             p.stage(S_S)
@@ -394,6 +407,9 @@ def run_gpu(args):
                        "tag_check": ("none" if args.no_tags else
                                      "fused into attention" if args.fused_tags else "separate pass"),
                        "split_tokens": args.split, "replicas": args.replicas,
+                       "step_call": "pfkv_decode_step (kv_append and validation share a launch); "
+                                    "every 4th step runs the stages as separate calls, with "
+                                    "events around the split kernel",
                        "l2": "inputs larger than L2: %d rotating replicas, %.0f MB live KV each"
                              % (args.replicas, kv_bytes / 1e6),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -253,6 +253,29 @@ pfkv_status pfkv_paged_decode_attn_fused_tags(const pfkv_cache *cache, const pfk
                                               uint8_t *flags, void *stream);
 
 /*
+ * pfkv_decode_step -- one decode step of a layer: pfkv_kv_append of the new
+ * tokens, then pfkv_paged_decode_attn over the same pages, in one call.
+ *
+ * Arguments are those of the two calls: positions .. append_flags as for
+ * pfkv_kv_append (append_flags receives its bits), q .. flags as for
+ * pfkv_paged_decode_attn (same workspace size).  options: 0, or
+ * PFKV_STAGE_FUSED_TAGS for the check inside attention.
+ *
+ * The result is exactly that of the two calls in stream order: same pool
+ * bytes, scales, outputs and flags.  The validation reads only tables, tags
+ * and lengths, never the pool, so here it runs in the same launch as the
+ * append, which saves one kernel's latency per step.  Every argument of both
+ * parts is checked before anything is launched; on any error nothing runs.
+ */
+pfkv_status pfkv_decode_step(const pfkv_cache *cache, const pfkv_pages *pages,
+                             const int32_t *positions, const int32_t *new_lens,
+                             int32_t num_new_tokens, const void *k_new, const void *v_new,
+                             uint8_t *append_flags, const void *q, int32_t num_q_heads,
+                             float sm_scale, int32_t split_tokens, int32_t max_seq_len,
+                             void *workspace, size_t workspace_bytes, void *out, uint8_t *flags,
+                             uint32_t options, void *stream);
+
+/*
  * pfkv_paged_decode_attn_noalloc -- pfkv_paged_decode_attn without a
  * caller-provided workspace.  (The source pages have no counterpart to this
  * call; it exists for callers, not for the method.)

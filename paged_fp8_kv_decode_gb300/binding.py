@@ -42,6 +42,7 @@ PFKV_STAGE_FUSED_TAGS = 0x8
 
 # every symbol include/pfkv.h declares
 EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",
+            "pfkv_decode_step",
             "pfkv_paged_decode_attn_stages", "pfkv_paged_decode_attn_fused_tags",
             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_mass",
             "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
@@ -106,6 +107,10 @@ def lib() -> ctypes.CDLL:
                                                     ctypes.c_float, I32, I32, P, ctypes.c_size_t,
                                                     P, P, ctypes.c_uint32, P]
         L.pfkv_paged_decode_attn_stages.restype = ctypes.c_int
+        L.pfkv_decode_step.argtypes = [ctypes.POINTER(_CCache), ctypes.POINTER(_CPages), P, P, I32,
+                                       P, P, P, P, I32, ctypes.c_float, I32, I32, P,
+                                       ctypes.c_size_t, P, P, ctypes.c_uint32, P]
+        L.pfkv_decode_step.restype = ctypes.c_int
         L.pfkv_paged_decode_attn_fused_tags.argtypes = L.pfkv_paged_decode_attn.argtypes
         L.pfkv_paged_decode_attn_fused_tags.restype = ctypes.c_int
         L.pfkv_paged_decode_attn_noalloc.argtypes = [ctypes.POINTER(_CCache),
@@ -282,6 +287,25 @@ def pfkv_paged_decode_attn_stages(cache: Cache, pages: Pages, q: torch.Tensor, s
         ctypes.byref(c), ctypes.byref(p), _ptr(q), Hq, float(sm_scale), int(split_tokens),
         int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), _ptr(flags), int(stages), _stream(stream)), "pfkv_paged_decode_attn_stages")
+
+
+def pfkv_decode_step(cache: Cache, pages: Pages, positions: torch.Tensor, k_new: torch.Tensor,
+                     v_new: torch.Tensor, q: torch.Tensor, sm_scale: float, split_tokens: int,
+                     max_seq_len: int, workspace: torch.Tensor, out: torch.Tensor,
+                     flags: Optional[torch.Tensor] = None,
+                     append_flags: Optional[torch.Tensor] = None,
+                     new_lens: Optional[torch.Tensor] = None, options: int = 0,
+                     stream=None) -> None:
+    """pfkv_kv_append then pfkv_paged_decode_attn in one call (the append and
+    the validation share a launch); arguments as for the two calls."""
+    c, p = cache.c_struct(), pages.c_struct()
+    T = int(k_new.shape[2])
+    Hq = int(q.shape[1])
+    _check(lib().pfkv_decode_step(
+        ctypes.byref(c), ctypes.byref(p), _ptr(positions), _ptr(new_lens), T, _ptr(k_new),
+        _ptr(v_new), _ptr(append_flags), _ptr(q), Hq, float(sm_scale), int(split_tokens),
+        int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(flags), int(options), _stream(stream)), "pfkv_decode_step")
 
 
 def pfkv_paged_decode_attn_fused_tags(cache: Cache, pages: Pages, q: torch.Tensor,

@@ -101,6 +101,51 @@ pfkv_status check_decode_args(const pfkv_cache *c, int32_t num_q_heads, int32_t 
     return PFKV_OK;
 }
 
+// Arguments of a kv_append call, checked (no launch).  PFKV_OK with an empty
+// batch means there is nothing to do.
+pfkv_status append_args(const pfkv_cache *cache, const pfkv_pages *pages, const int32_t *positions,
+                        const int32_t *new_lens, int32_t num_new_tokens, const void *k_new,
+                        const void *v_new, uint8_t *flags, AppendArgs *out) {
+    pfkv_status st = check_cache(cache);
+    if (st != PFKV_OK) return st;
+    st = check_pages(cache, pages);
+    if (st != PFKV_OK) return st;
+    if (num_new_tokens <= 0) return PFKV_ERR_INVALID_ARG;
+    if (pages->batch == 0) return PFKV_OK;
+    if (!positions || !k_new || !v_new) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(positions, 4) || (new_lens && !aligned(new_lens, 4))) return PFKV_ERR_ALIGNMENT;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PFKV_ERR_ALIGNMENT;
+    if (flags && !aligned(flags, 4)) return PFKV_ERR_ALIGNMENT;
+    const long long units = ((long long)num_new_tokens + 30) / kPage;
+    if ((units + 3) / 4 > 65535) return PFKV_ERR_UNSUPPORTED;
+    if ((long long)pages->batch * cache->num_kv_heads > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
+    AppendArgs a{};
+    a.k_pages = cache->k_pages;
+    a.v_pages = cache->v_pages;
+    a.k_scale = cache->k_scale;
+    a.v_scale = cache->v_scale;
+    a.page_tags = cache->page_tags;
+    a.num_pages = cache->num_pages;
+    a.Hkv = cache->num_kv_heads;
+    a.D = cache->head_dim;
+    a.dtype = cache->dtype;
+    a.block_tables = pages->block_tables;
+    a.bt_sb = pages->bt_stride_b;
+    a.bt_sh = pages->bt_stride_h;
+    a.expected_tags = pages->expected_tags;
+    a.max_pages = pages->max_pages;
+    a.positions = positions;
+    a.new_lens = new_lens;
+    a.len_sb = pages->len_stride_b;
+    a.len_sh = pages->len_stride_h;
+    a.T = num_new_tokens;
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.flags = flags;
+    *out = a;
+    return PFKV_OK;
+}
+
 pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_heads,
                       int32_t split_tokens, int32_t max_seq_len, int num_sms, DecodePlan *plan,
                       bool mass = false, int32_t kq = 1) {
@@ -192,45 +237,12 @@ pfkv_status pfkv_kv_append(const pfkv_cache *cache, const pfkv_pages *pages,
                            const int32_t *positions, const int32_t *new_lens,
                            int32_t num_new_tokens, const void *k_new, const void *v_new,
                            uint8_t *flags, void *stream) {
-    pfkv_status st = check_cache(cache);
-    if (st != PFKV_OK) return st;
-    st = check_pages(cache, pages);
-    if (st != PFKV_OK) return st;
-    if (num_new_tokens <= 0) return PFKV_ERR_INVALID_ARG;
-    if (pages->batch == 0) return PFKV_OK;
-    if (!positions || !k_new || !v_new) return PFKV_ERR_INVALID_ARG;
-    if (!aligned(positions, 4) || (new_lens && !aligned(new_lens, 4))) return PFKV_ERR_ALIGNMENT;
-    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PFKV_ERR_ALIGNMENT;
-    if (flags && !aligned(flags, 4)) return PFKV_ERR_ALIGNMENT;
-    const long long units = ((long long)num_new_tokens + 30) / kPage;
-    if ((units + 3) / 4 > 65535) return PFKV_ERR_UNSUPPORTED;
-    if ((long long)pages->batch * cache->num_kv_heads > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
+    AppendArgs a{};
+    pfkv_status st = append_args(cache, pages, positions, new_lens, num_new_tokens, k_new, v_new,
+                                       flags, &a);
+    if (st != PFKV_OK || pages->batch == 0) return st;
     st = device_check(nullptr);
     if (st != PFKV_OK) return st;
-
-    AppendArgs a{};
-    a.k_pages = cache->k_pages;
-    a.v_pages = cache->v_pages;
-    a.k_scale = cache->k_scale;
-    a.v_scale = cache->v_scale;
-    a.page_tags = cache->page_tags;
-    a.num_pages = cache->num_pages;
-    a.Hkv = cache->num_kv_heads;
-    a.D = cache->head_dim;
-    a.dtype = cache->dtype;
-    a.block_tables = pages->block_tables;
-    a.bt_sb = pages->bt_stride_b;
-    a.bt_sh = pages->bt_stride_h;
-    a.expected_tags = pages->expected_tags;
-    a.max_pages = pages->max_pages;
-    a.positions = positions;
-    a.new_lens = new_lens;
-    a.len_sb = pages->len_stride_b;
-    a.len_sh = pages->len_stride_h;
-    a.T = num_new_tokens;
-    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
-    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-    a.flags = flags;
     if (launch_kv_append(a, pages->batch, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PFKV_ERR_CUDA;
     return PFKV_OK;
@@ -266,12 +278,14 @@ struct MassOut {
 };
 
 // The attention call: the stages named in `stages`, plus the attention-mass
-// pass when `mass` is given.
+// pass when `mass` is given.  With `app` (checked arguments of a kv_append
+// for the same pages), the append runs first, in the same launch as the
+// validation when that stage runs.
 pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const void *q,
                       int32_t num_q_heads, float sm_scale, int32_t split_tokens,
                       int32_t max_seq_len, void *workspace, size_t workspace_bytes, void *out,
                       uint8_t *flags, uint32_t stages, const MassOut *mass, void *stream,
-                      int32_t kq = 1) {
+                      int32_t kq = 1, const AppendArgs *app = nullptr) {
     if (kq < 1 || (mass && kq != 1)) return kq < 1 ? PFKV_ERR_INVALID_ARG : PFKV_ERR_UNSUPPORTED;
     if ((stages & PFKV_STAGE_ALL) == 0 || (stages & ~(PFKV_STAGE_ALL | PFKV_STAGE_FUSED_TAGS)))
         return PFKV_ERR_INVALID_ARG;
@@ -340,7 +354,12 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool validate = (stages & PFKV_STAGE_VALIDATE) && plan.tags && !fused;
     a.early = validate ? 1 : 0;
-    if (validate && launch_validate(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
+    if (app && validate) {
+        if (launch_append_validate(*app, pages->batch, a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
+    } else {
+        if (app && launch_kv_append(*app, pages->batch, s) != cudaSuccess) return PFKV_ERR_CUDA;
+        if (validate && launch_validate(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
+    }
     if ((stages & PFKV_STAGE_SPLIT) && launch_split(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     if ((stages & PFKV_STAGE_COMBINE) && launch_combine(a, plan, s) != cudaSuccess)
         return PFKV_ERR_CUDA;
@@ -351,6 +370,21 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
 }  // namespace
 
 extern "C" {
+
+pfkv_status pfkv_decode_step(const pfkv_cache *cache, const pfkv_pages *pages,
+                             const int32_t *positions, const int32_t *new_lens, int32_t num_new_tokens,
+                             const void *k_new, const void *v_new, uint8_t *append_flags,
+                             const void *q, int32_t num_q_heads, float sm_scale, int32_t split_tokens,
+                             int32_t max_seq_len, void *workspace, size_t workspace_bytes, void *out,
+                             uint8_t *flags, uint32_t options, void *stream) {
+    if (options & ~PFKV_STAGE_FUSED_TAGS) return PFKV_ERR_INVALID_ARG;
+    AppendArgs ap{};
+    const pfkv_status st = append_args(cache, pages, positions, new_lens, num_new_tokens, k_new, v_new,
+                                       append_flags, &ap);
+    if (st != PFKV_OK || pages->batch == 0) return st;
+    return attn_impl(cache, pages, q, num_q_heads, sm_scale, split_tokens, max_seq_len, workspace,
+                     workspace_bytes, out, flags, PFKV_STAGE_ALL | options, nullptr, stream, 1, &ap);
+}
 
 pfkv_status pfkv_paged_decode_attn_stages(const pfkv_cache *cache, const pfkv_pages *pages,
                                           const void *q, int32_t num_q_heads, float sm_scale,

@@ -17,14 +17,11 @@ namespace pfkv {
 // --------------------------------------------------------------------------
 constexpr int kAppendWarps = 4;
 
+// The k-th unit touched by the call for (request, kv head) bh, by one warp.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(AppendArgs a) {
+__device__ __forceinline__ void append_unit(const AppendArgs &a, int bh, int k, int lane) {
     constexpr int EPL = D / 32;  // elements per lane per row (4 or 2)
-    pdl_enter();
-    const int bh = blockIdx.x;
     const int b = bh / a.Hkv, h = bh - b * a.Hkv;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int k = blockIdx.y * kAppendWarps + warp;
 
     const long long li = (long long)b * a.len_sb + (long long)h * a.len_sh;
     const int p0 = a.positions[li];
@@ -118,6 +115,12 @@ __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(AppendArgs
     }
 }
 
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(AppendArgs a) {
+    pdl_enter();
+    append_unit<D, FP8>(a, blockIdx.x, blockIdx.y * kAppendWarps + (threadIdx.x >> 5), threadIdx.x & 31);
+}
+
 cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
     const long long units = ((long long)a.T + 30) / kPage;  // ceil((T + 15) / 16)
     dim3 grid((unsigned)(B * a.Hkv), (unsigned)((units + kAppendWarps - 1) / kAppendWarps));
@@ -138,11 +141,8 @@ cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
 // after this kernel completes.  A thread loads all of its page ids, then all
 // of their tags and expected tags, so a tile costs two memory round trips.
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(kValThreads) validate_kernel(DecodeArgs a, int Hkv) {
-    // wait first, then let the next kernel start: the split kernel relies on
-    // it (DecodeArgs::early)
-    pdl_enter();
-    const int bh = blockIdx.x, tile = blockIdx.y;
+// One tile by a CTA of kValThreads threads (every thread must call it).
+__device__ __forceinline__ void validate_tile(const DecodeArgs &a, int Hkv, int bh, int tile) {
     const int b = bh / Hkv, h = bh - b * Hkv;
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
     uint32_t bits = 0;
@@ -181,13 +181,59 @@ __global__ void __launch_bounds__(kValThreads) validate_kernel(DecodeArgs a, int
         if (any_len) f |= PFKV_FLAG_BAD_LENGTH;
         if (any_page) f |= PFKV_FLAG_BAD_PAGE;
         if (any_tag) f |= PFKV_FLAG_TAG_MISMATCH;
-        a.hflags[(long long)bh * gridDim.y + tile] = f;
+        a.hflags[(long long)bh * a.htiles + tile] = f;
     }
+}
+
+__global__ void __launch_bounds__(kValThreads) validate_kernel(DecodeArgs a, int Hkv) {
+    // wait first, then let the next kernel start: the split kernel relies on
+    // it (DecodeArgs::early)
+    pdl_enter();
+    validate_tile(a, Hkv, blockIdx.x, blockIdx.y);
 }
 
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     return launch_pdl(validate_kernel, dim3(p.Breq * p.Hkv, p.htiles), dim3(kValThreads), 0, s, a,
                       p.Hkv);
+}
+
+// --------------------------------------------------------------------------
+// kv_append and validation of one decode step in one launch.  Validation
+// reads only the block tables, tags and lengths, never the pool, so the two
+// jobs are independent; the first nA CTAs append (kValThreads / 32 warps
+// each, one unit per warp) and the others validate one tile each.  Like both
+// kernels it waits for its predecessor first, then lets the next kernel
+// start (DecodeArgs::early holds as after the validation kernel).
+// --------------------------------------------------------------------------
+constexpr int kStepAppendWarps = kValThreads / 32;
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kValThreads) append_validate_kernel(AppendArgs ap, DecodeArgs a, int Hkv,
+                                                                      int nA, int ay) {
+    pdl_enter();
+    if ((int)blockIdx.x < nA) {
+        const int bh = blockIdx.x / ay, yy = blockIdx.x - bh * ay;
+        append_unit<D, FP8>(ap, bh, yy * kStepAppendWarps + (threadIdx.x >> 5), threadIdx.x & 31);
+        return;  // uniform per CTA: no barrier in this branch
+    }
+    const int i = blockIdx.x - nA;
+    validate_tile(a, Hkv, i / a.htiles, i - i / a.htiles * a.htiles);
+}
+
+cudaError_t launch_append_validate(const AppendArgs &ap, int B, const DecodeArgs &a, const DecodePlan &p,
+                                   cudaStream_t s) {
+    const long long units = ((long long)ap.T + 30) / kPage;  // as launch_kv_append
+    const int ay = (int)((units + kStepAppendWarps - 1) / kStepAppendWarps);
+    const long long nA = (long long)B * ap.Hkv * ay;
+    const long long nV = (long long)p.Breq * p.Hkv * p.htiles;
+    if (nA + nV > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)(nA + nV)), block(kValThreads);
+    if (ap.dtype == PFKV_KV_FP8_E4M3) {
+        if (ap.D == 128) return launch_pdl(append_validate_kernel<128, true>, grid, block, 0, s, ap, a, p.Hkv, (int)nA, ay);
+        return launch_pdl(append_validate_kernel<64, true>, grid, block, 0, s, ap, a, p.Hkv, (int)nA, ay);
+    }
+    if (ap.D == 128) return launch_pdl(append_validate_kernel<128, false>, grid, block, 0, s, ap, a, p.Hkv, (int)nA, ay);
+    return launch_pdl(append_validate_kernel<64, false>, grid, block, 0, s, ap, a, p.Hkv, (int)nA, ay);
 }
 
 // --------------------------------------------------------------------------

@@ -49,14 +49,14 @@ pfkv_status pfkv_step_graph_create(const pfkv_layer *layers, int32_t num_layers,
     pfkv_status st = PFKV_OK;
     for (int l = 0; l < num_layers && st == PFKV_OK; ++l) {
         const pfkv_layer &L = layers[l];
-        if (L.k_new) {
-            st = pfkv_kv_append(&L.cache, pages, positions, new_lens, num_new_tokens, L.k_new,
-                                L.v_new, append_flags, s);
-            if (st != PFKV_OK) break;
-        }
-        st = pfkv_paged_decode_attn_stages(&L.cache, pages, L.q, num_q_heads, sm_scale,
-                                           split_tokens, max_seq_len, workspace, workspace_bytes,
-                                           L.out, L.flags, PFKV_STAGE_ALL | options, s);
+        if (L.k_new)  // append + attention as one step (append and validation share a launch)
+            st = pfkv_decode_step(&L.cache, pages, positions, new_lens, num_new_tokens, L.k_new, L.v_new,
+                                  append_flags, L.q, num_q_heads, sm_scale, split_tokens, max_seq_len,
+                                  workspace, workspace_bytes, L.out, L.flags, options, s);
+        else
+            st = pfkv_paged_decode_attn_stages(&L.cache, pages, L.q, num_q_heads, sm_scale,
+                                               split_tokens, max_seq_len, workspace, workspace_bytes,
+                                               L.out, L.flags, PFKV_STAGE_ALL | options, s);
     }
     cudaGraph_t g = nullptr;
     const cudaError_t ce = cudaStreamEndCapture(s, &g);

@@ -199,6 +199,8 @@ __device__ __forceinline__ bool request_rejected_cta(const DecodeArgs &a, int b,
 // launchers (defined in the .cu files)
 cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s);
 cudaError_t launch_validate(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_append_validate(const AppendArgs &ap, int B, const DecodeArgs &a, const DecodePlan &p,
+                                   cudaStream_t s);
 cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_mass(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 bool swz_supported(const DecodePlan &p, int num_pages);

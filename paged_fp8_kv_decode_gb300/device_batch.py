@@ -149,10 +149,17 @@ class DeviceBatch:
            self.split_tokens if split_tokens is None else split_tokens,
            self.max_seq_len, self.workspace, self.out, self.flags, stream=stream)
 
-    def step(self, stream=None):
-        """One decode step: append the new token (if any), then attention."""
-        self.append_step(stream)
-        self.attend(stream)
+    def step(self, stream=None, one_call: bool = True):
+        """One decode step: append the new token (if any), then attention;
+        with ``one_call`` through pfkv_decode_step, else as the two calls."""
+        if not (one_call and self.spec.append):
+            self.append_step(stream)
+            self.attend(stream)
+            return
+        B.pfkv_decode_step(self.cache, self.pages, self.positions, self.k_new, self.v_new, self.q,
+                           self.spec.sm_scale, self.split_tokens, self.max_seq_len, self.workspace,
+                           self.out, self.flags, append_flags=self.append_flags,
+                           options=B.PFKV_STAGE_FUSED_TAGS if self.fused_tags else 0, stream=stream)
 
     # ------------------------------------------------------------------
     def _lens(self, skip=None) -> np.ndarray:

@@ -30,7 +30,7 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert names == sorted(["pfkv_abi_version", "pfkv_decode_workspace_size", "pfkv_e4m3_decode",
-                            "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_paged_decode_attn",
+                            "pfkv_e4m3_encode", "pfkv_kv_append", "pfkv_decode_step", "pfkv_paged_decode_attn",
                             "pfkv_paged_decode_attn_fused_tags", "pfkv_paged_decode_attn_mass",
                             "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
                             "pfkv_decode_multi_workspace_size",
@@ -137,6 +137,33 @@ def test_fused_tag_entry_checks_arguments_like_the_plain_one(B):
     assert fused(max_len=-1) == 1
     assert fused(ws=None) == 4
     assert fused(ws=0xB0010) == 3
+
+
+def test_decode_step_checks_both_parts_before_any_launch(B):
+    """pfkv_decode_step = kv_append + attention: the append's argument errors
+    and the attention's come back with the same codes as from the two calls,
+    and an unknown option bit is rejected (all before any device access)."""
+    c, p = _structs(B)
+    L = B.lib()
+    def step(T=1, k=0x80000, positions=0x70000, Hq=4, split=0, ws=0xB0000, out=0xC0000, options=0):
+        return L.pfkv_decode_step(ctypes.byref(c), ctypes.byref(p), positions, None, T, k, 0x90000,
+                                  None, 0xA0000, Hq, 0.125, split, 64, ws, 1 << 30, out, None,
+                                  options, None)
+    assert step(options=0x1) == 1
+    assert step(options=0x10) == 1
+    assert step(T=0) == 1
+    assert step(k=None) == 1
+    assert step(k=0x80008) == 3
+    assert step(positions=0x70002) == 3
+    assert step(Hq=6) == 2
+    assert step(split=24) == 1
+    assert step(ws=None) == 4
+    assert step(out=0xC0004) == 3
+    for over, code in [(dict(page_size=32), 2), (dict(block_tables=None), 1)]:
+        c2, p2 = _structs(B, **over)
+        assert L.pfkv_decode_step(ctypes.byref(c2), ctypes.byref(p2), 0x70000, None, 1, 0x80000,
+                                  0x90000, None, 0xA0000, 4, 0.125, 0, 64, 0xB0000, 1 << 30,
+                                  0xC0000, None, 0, None) == code
 
 
 def test_step_graph_argument_checks(B):
