@@ -86,6 +86,21 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// the same with bf16 operands
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
     return *reinterpret_cast<const uint4 *>(p);
 }
@@ -120,24 +135,33 @@ __device__ __forceinline__ void tma_unit(void *dst, const CUtensorMap *map, int 
         : "memory");
 }
 
+// the same for the 3-D BF16 map: both lines of each of the 16 rows
+__device__ __forceinline__ void tma_unit3(void *dst, const CUtensorMap *map, int row, uint64_t *bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 constexpr float kLazy = 8.0f;   // rescale only when the max grows by > 2^8
 constexpr int kNoScale = -1000; // V-scale reference of a worker that has seen no unit yet
 
 }  // namespace
 
-// Kernel shape: units per granule (one ring stage), worker warps per CTA and
-// ring stages per worker.  Two shapes are built, both with 192 KB of rings:
-// 8 workers x 3 stages, and 12 workers x 2 stages, which hides more latency
-// when every worker streams long runs (see pers_workers_for).
-constexpr int kGranUnits = 2;
-
-template <int WK>
+// Kernel shape: worker warps per CTA, ring stages per worker, and units per
+// granule (one ring stage of 8 KB: two FP8 units or one BF16 unit).  Two
+// worker counts are built, both with 192 KB of rings: 8 workers x 3 stages,
+// and 12 workers x 2 stages, which hides more latency when every worker
+// streams long runs (see pers_workers_for).
+template <int WK, bool BF>
 struct PersCfg {
     static_assert(WK == 8 || WK == 12, "8 or 12 workers per CTA");
     static constexpr int D = 128;
-    static constexpr int ROWB = 128;
-    static constexpr int UNITB = kPage * ROWB;   // 2 KB
-    static constexpr int GU = kGranUnits;
+    static constexpr int ROWB = D * (BF ? 2 : 1);  // one token row of a slab
+    static constexpr int UNITB = kPage * ROWB;     // 2 KB (FP8) or 4 KB (BF16)
+    static constexpr int GU = BF ? 1 : 2;
     static constexpr int STAGEB = 2 * GU * UNITB;  // K u0 .. K u(GU-1) | V u0 .. V u(GU-1)
     static constexpr int WORKERS = WK;
     static constexpr int STAGES = WK == 8 ? 3 : 2;
@@ -169,12 +193,12 @@ __device__ __forceinline__ int seg_of(const int *prefix, int K, int x) {
 // MASS: also store every live token's final scores for the attention-mass
 // pass (a separate instantiation, so that the plain kernel carries no trace of
 // it in its inner loop).
-template <int G, bool MASS, int WK>
-__global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
+template <int G, bool MASS, int WK, bool BF>
+__global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
     decode_split_pers_kernel(const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, DecodeArgs a, int Hkv, int B,
                              int nchunks, int chunk_tokens, int *ws_prefix) {
-    using C = PersCfg<WK>;
+    using C = PersCfg<WK, BF>;
     constexpr int ST = C::STAGES;
     static_assert(G == 1 || G == 2 || G == 4, "query groups of 1, 2 or 4 heads");
     extern __shared__ uint8_t smem_raw[];
@@ -341,9 +365,13 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
         }
     };
     auto load_scales = [&](int phys, float &ks, float &vs) {
-        const long long u = phys >= 0 ? phys : 0;
-        ks = a.k_scale[u];
-        vs = a.v_scale[u];
+        if constexpr (BF) {  // a BF16 pool has no scales
+            ks = vs = 1.f;
+        } else {
+            const long long u = phys >= 0 ? phys : 0;
+            ks = a.k_scale[u];
+            vs = a.v_scale[u];
+        }
     };
     int creq = -1, nreq = -1;
     if (!idle) {
@@ -400,9 +428,13 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
                 mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
                 for (int u = 0; u < C::GU; ++u) {
-                    if (pu[u] >= 0) {
+                    if (pu[u] >= 0 && !BF) {
                         tma_unit(dst + u * C::UNITB, &tmk, pu[u] * kPage, &full[s], policy);
                         tma_unit(dst + (C::GU + u) * C::UNITB, &tmv, pu[u] * kPage, &full[s], policy);
+                    }
+                    if (pu[u] >= 0 && BF) {
+                        tma_unit3(dst + u * C::UNITB, &tmk, pu[u] * kPage, &full[s], policy);
+                        tma_unit3(dst + (C::GU + u) * C::UNITB, &tmv, pu[u] * kPage, &full[s], policy);
                     }
                 }
             }
@@ -452,16 +484,38 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
     for (int j = 0; j < ST && j < ngran; ++j) cursor_next(iss, issue_at(iss, j));
 
 
-    // fragment offsets inside a swizzled 2 KB slab
-    // K (A of S = K Q^T): rows fg and fg + 8, logical chunks 2 ft and 2 ft + 1
-    const int offK0 = fg * C::ROWB + (((2 * ft) ^ (fg & 7)) << 4);
-    const int offK1 = fg * C::ROWB + (((2 * ft + 1) ^ (fg & 7)) << 4);
-    // V (A of O^T = V^T P^T): rows 2 ft, 2 ft + 1 (+ 8), logical chunk fg
-    const int offV0 = (2 * ft) * C::ROWB + ((fg ^ (2 * ft)) << 4);
-    const int offV1 = (2 * ft + 1) * C::ROWB + ((fg ^ (2 * ft + 1)) << 4);
-    // shuffle sources of the probability fragment (tokens 2 ft and 2 ft + 1,
-    // head fg) and which of the source's two heads is fg
-    const int src0 = 8 * ft + (fg >> 1), src1 = src0 + 4;
+    // Fragment offsets inside a swizzled slab.  Its 128-byte lines are
+    // numbered L (FP8: L = row; BF16: L = 2 row + half, a row being two
+    // lines), and 16-byte chunk c of line L sits at chunk c ^ (L & 7).
+    auto swz = [](int line, int chunk) { return line * 128 + ((chunk ^ (line & 7)) << 4); };
+    int offK[4], offV[4];
+    if constexpr (!BF) {
+        // K (A of S = K Q^T): row fg (+8: +1 KB), chunks 2 ft, 2 ft + 1 (dims 32 ft ..)
+        offK[0] = swz(fg, 2 * ft);
+        offK[1] = swz(fg, 2 * ft + 1);
+        // V (A of O^T = V^T P^T): rows 2 ft, 2 ft + 1 (+8: +1 KB), chunk fg
+        offV[0] = swz(2 * ft, fg);
+        offV[1] = swz(2 * ft + 1, fg);
+        offK[2] = offK[3] = offV[2] = offV[3] = 0;
+    } else {
+        // K: row fg (+8: +2 KB), dims 32 ft .. 32 ft + 31: half ft / 2, chunks
+        // 4 (ft & 1) + j
+        const int hk = ft >> 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) offK[j] = swz(2 * fg + hk, 4 * (ft & 1) + j);
+        // V: rows ft and ft + 4 (+8: +2 KB), in half fg / 4 the chunks
+        // fg & 3 and (fg & 3) + 4, i.e. dims 64 h + 8 (fg & 3) + 0..7 and the
+        // same + 32
+        const int hv = fg >> 2, gg = fg & 3;
+        offV[0] = swz(2 * ft + hv, gg);
+        offV[1] = swz(2 * ft + hv, gg + 4);
+        offV[2] = swz(2 * (ft + 4) + hv, gg);
+        offV[3] = swz(2 * (ft + 4) + hv, gg + 4);
+    }
+    // shuffle sources of the probability fragment of head fg: FP8 pairs the
+    // tokens (2 ft, 2 ft + 1) and (2 ft + 8, 2 ft + 9), BF16 pairs (ft, ft + 4)
+    // and (ft + 8, ft + 12); and which of the source's two heads is fg
+    const int src0 = (BF ? 4 : 8) * ft + (fg >> 1), src1 = src0 + (BF ? 16 : 4);
     const bool odd_head = (fg & 1) != 0;
 
     // online softmax state of heads 2 ft (A) and 2 ft + 1 (B); O^T fragments:
@@ -491,6 +545,17 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
             load_ids(base + 32, nphys, nbad, req);
             skip_rejected(req, nphys, nbad);
             pending_scales = true;
+        }
+        if (seg_start && BF) {
+            // BF16: the query's bf16 pairs are the B fragments as they are
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qb0[ks] = word_of(qraw[ks >> 1], 2 * (ks & 1));
+                qb1[ks] = word_of(qraw[ks >> 1], 2 * (ks & 1) + 1);
+            }
+            qmul = a.q_scale;
+            if (con.seg_end < x1) q_fetch(seg_of(sm.prefix, K, con.seg_end));
+            seg_start = false;
         }
         if (seg_start) {
             // this segment's query fragments, then fetch the next segment's
@@ -550,10 +615,10 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
             }
 #pragma unroll
             for (int u = 0; u < C::GU; ++u) {
-                if (FULL || nv[u] > 0) {
+                if ((FULL || nv[u] > 0) && !BF) {
                     const uint8_t *kb = stage + u * C::UNITB;
-                    const uint4 ra0 = lds128(kb + offK0), ra1 = lds128(kb + offK1);
-                    const uint4 rb0 = lds128(kb + 8 * C::ROWB + offK0), rb1 = lds128(kb + 8 * C::ROWB + offK1);
+                    const uint4 ra0 = lds128(kb + offK[0]), ra1 = lds128(kb + offK[1]);
+                    const uint4 rb0 = lds128(kb + 8 * C::ROWB + offK[0]), rb1 = lds128(kb + 8 * C::ROWB + offK[1]);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t wa = word_of(ks < 4 ? ra0 : ra1, ks & 3);
@@ -563,6 +628,25 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
                         e4m3x4_to_f16x2(wb, a1, a3);
                         if (ks & 1) mma_16816(c1[u], a0, a1, a2, a3, qb0[ks], qb1[ks]);
                         else mma_16816(c0[u], a0, a1, a2, a3, qb0[ks], qb1[ks]);
+                    }
+                }
+                if ((FULL || nv[u] > 0) && BF) {
+                    // BF16: the bf16 pairs of K are the A fragments as they are
+                    const uint8_t *kb = stage + u * C::UNITB;
+                    uint4 ra[4], rb[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        ra[j] = lds128(kb + offK[j]);
+                        rb[j] = lds128(kb + 8 * C::ROWB + offK[j]);
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t a0 = word_of(ra[ks >> 1], 2 * (ks & 1));
+                        const uint32_t a2 = word_of(ra[ks >> 1], 2 * (ks & 1) + 1);
+                        const uint32_t a1 = word_of(rb[ks >> 1], 2 * (ks & 1));
+                        const uint32_t a3 = word_of(rb[ks >> 1], 2 * (ks & 1) + 1);
+                        if (ks & 1) mma_16816_bf16(c1[u], a0, a1, a2, a3, qb0[ks], qb1[ks]);
+                        else mma_16816_bf16(c0[u], a0, a1, a2, a3, qb0[ks], qb1[ks]);
                     }
                 }
             }
@@ -603,10 +687,10 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
             }
             const bool grow = mbA > mA + kLazy || mbB > mB + kLazy;
             // V-scale reference: 2^eO bounds every live unit's V scale seen so far
-            int eneed = kNoScale;
+            int eneed = kNoScale;  // (a BF16 pool has no V scale: eO stays 0)
 #pragma unroll
             for (int u = 0; u < C::GU; ++u)
-                if (FULL || nv[u] > 0) eneed = max(eneed, exp_above(um[u].vs));
+                if (!BF && (FULL || nv[u] > 0)) eneed = max(eneed, exp_above(um[u].vs));
             const bool scale_up = eneed > eO;
             float fA = 1.f, fB = 1.f;
             if (scale_up) {
@@ -649,19 +733,52 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
                 lB += pB0 + pB1;
                 if (!FULL && nv[u] == 0) continue;  // uniform: nothing of this unit is live
                 const float vs = um[u].vs * vref;
-                // X0: head A at tokens (fg, fg + 8); X1: head B
-                const uint32_t X0 = pack_half2(pA0 * vs, pA1 * vs);
-                const uint32_t X1 = pack_half2(pB0 * vs, pB1 * vs);
+                // X0: head A at tokens (fg, fg + 8); X1: head B (BF16: bf16
+                // probabilities, no V scale)
+                const uint32_t X0 = BF ? pack_bf162(pA0, pA1) : pack_half2(pA0 * vs, pA1 * vs);
+                const uint32_t X1 = BF ? pack_bf162(pB0, pB1) : pack_half2(pB0 * vs, pB1 * vs);
                 const uint32_t s00 = __shfl_sync(0xffffffffu, X0, src0), s01 = __shfl_sync(0xffffffffu, X1, src0);
                 const uint32_t s10 = __shfl_sync(0xffffffffu, X0, src1), s11 = __shfl_sync(0xffffffffu, X1, src1);
-                const uint32_t Y0 = odd_head ? s01 : s00;  // head fg, tokens (2 ft, 2 ft + 8)
-                const uint32_t Y1 = odd_head ? s11 : s10;  // head fg, tokens (2 ft + 1, 2 ft + 9)
-                const uint32_t pb0 = __byte_perm(Y0, Y1, 0x5410);  // tokens 2 ft, 2 ft + 1
-                const uint32_t pb1 = __byte_perm(Y0, Y1, 0x7632);  // tokens 2 ft + 8, 2 ft + 9
+                // head fg: Y0 = tokens (a, a + 8), Y1 = (b, b + 8) with (a, b) =
+                // (2 ft, 2 ft + 1) for FP8 and (ft, ft + 4) for BF16
+                const uint32_t Y0 = odd_head ? s01 : s00;
+                const uint32_t Y1 = odd_head ? s11 : s10;
+                const uint32_t pb0 = __byte_perm(Y0, Y1, 0x5410);  // tokens a, b
+                const uint32_t pb1 = __byte_perm(Y0, Y1, 0x7632);  // tokens a + 8, b + 8
 
                 const uint8_t *vb = stage + (C::GU + u) * C::UNITB;
-                uint4 r0 = lds128(vb + offV0), r1 = lds128(vb + offV1);
-                uint4 r2 = lds128(vb + 8 * C::ROWB + offV0), r3 = lds128(vb + 8 * C::ROWB + offV1);
+                if constexpr (BF) {
+                    // rows ft, ft + 4, ft + 8, ft + 12; chunks A and B of each
+                    uint4 ra[4], rb[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        ra[r] = lds128(vb + (r & 2 ? 8 * C::ROWB : 0) + offV[(r & 1) * 2]);
+                        rb[r] = lds128(vb + (r & 2 ? 8 * C::ROWB : 0) + offV[(r & 1) * 2 + 1]);
+                    }
+                    if (!FULL && nv[u] < kPage) {
+                        // rows past the live tokens may hold stale bytes (even
+                        // NaN codes): zero them so that 0 x row stays 0
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            if (ft + 4 * r >= nv[u]) ra[r] = rb[r] = z;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        // dims (2q, 2q + 1) of chunk A -> tile q; of chunk B -> tile 4 + q
+                        uint32_t w0 = word_of(ra[0], q), w1 = word_of(ra[1], q);
+                        uint32_t w2 = word_of(ra[2], q), w3 = word_of(ra[3], q);
+                        mma_16816_bf16(o[q], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
+                                       __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+                        w0 = word_of(rb[0], q), w1 = word_of(rb[1], q);
+                        w2 = word_of(rb[2], q), w3 = word_of(rb[3], q);
+                        mma_16816_bf16(o[4 + q], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
+                                       __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+                    }
+                    continue;
+                }
+                uint4 r0 = lds128(vb + offV[0]), r1 = lds128(vb + offV[1]);
+                uint4 r2 = lds128(vb + 8 * C::ROWB + offV[0]), r3 = lds128(vb + 8 * C::ROWB + offV[1]);
                 if (!FULL && nv[u] < kPage) {
                     // rows past the live tokens may hold stale bytes (even NaN
                     // codes): zero them so that 0 x row stays 0
@@ -697,22 +814,29 @@ __global__ void __launch_bounds__(PersCfg<WK>::NT, 1)
                 tA += __shfl_xor_sync(0xffffffffu, tA, off);
                 tB += __shfl_xor_sync(0xffffffffu, tB, off);
             }
-            const float up = eO == kNoScale ? 0.f : pow2i(eO);
+            const float up = BF ? 1.f : (eO == kNoScale ? 0.f : pow2i(eO));
             const float iA = tA > 0.f ? up / tA : 0.f, iB = tB > 0.f ? up / tB : 0.f;
             const long long row = con.k + w;
-            float *orow = a.o + row * G * C::D + 16 * fg;
-            if (2 * ft < G) {
-                float4 *dst = reinterpret_cast<float4 *>(orow + (2 * ft) * C::D);
+            // tile mt holds dims (base, base + 1) in components (0, 2) for head
+            // A and (1, 3) for head B; FP8: base = 16 fg + 2 mt; BF16: base =
+            // 64 (fg / 4) + 8 (fg & 3) + 2 mt, plus 24 for mt >= 4
+            auto store_head = [&](int head, int c0, int c1, float inv) {
+                float *orow = a.o + (row * G + head) * C::D;
+                float4 *dst = reinterpret_cast<float4 *>(orow + (BF ? 64 * (fg >> 2) + 8 * (fg & 3) : 16 * fg));
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_float4(o[2 * e][0] * iA, o[2 * e][2] * iA, o[2 * e + 1][0] * iA, o[2 * e + 1][2] * iA);
+                for (int e = 0; e < 4; ++e) {
+                    const float4 v = make_float4(o[2 * e][c0] * inv, o[2 * e][c1] * inv,
+                                                 o[2 * e + 1][c0] * inv, o[2 * e + 1][c1] * inv);
+                    if (BF && e >= 2) dst[e + 6] = v;  // dims + 32
+                    else dst[e] = v;
+                }
+            };
+            if (2 * ft < G) {
+                store_head(2 * ft, 0, 2, iA);
                 if (fg == 0) a.lse[row * G + 2 * ft] = tA > 0.f ? mA + plog2(tA) : -INFINITY;
             }
             if (2 * ft + 1 < G) {
-                float4 *dst = reinterpret_cast<float4 *>(orow + (2 * ft + 1) * C::D);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_float4(o[2 * e][1] * iB, o[2 * e][3] * iB, o[2 * e + 1][1] * iB, o[2 * e + 1][3] * iB);
+                store_head(2 * ft + 1, 1, 3, iB);
                 if (fg == 0) a.lse[row * G + 2 * ft + 1] = tB > 0.f ? mB + plog2(tB) : -INFINITY;
             }
             if (lane == 0) a.status[row] = seg_status;
@@ -759,24 +883,37 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A pool [units][16][128] bytes as a 2-D tensor (128-byte rows) read in
-// 16-row boxes with the 128-byte swizzle.
-cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long rows) {
+// A pool as a tensor read in one box per unit, with the 128-byte swizzle.
+// FP8 [units x 16][128 B]: 2-D, 16-row boxes.  BF16 [units x 16][2][64]: a
+// 256-byte row is two 128-byte lines (the swizzle spans at most 128 bytes),
+// so the tensor is 3-D and a box is 16 rows x 2 lines.
+cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long rows, bool bf16) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)PersCfg<8>::ROWB, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)PersCfg<8>::ROWB};
-    const cuuint32_t box[2] = {(cuuint32_t)PersCfg<8>::ROWB, (cuuint32_t)kPage};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pages), dims, strides,
-                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (!bf16) {
+        const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {128};
+        const cuuint32_t box[2] = {128, (cuuint32_t)kPage};
+        const cuuint32_t estr[2] = {1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pages), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[3] = {64, 2, (cuuint64_t)rows};
+        const cuuint64_t strides[2] = {128, 256};
+        const cuuint32_t box[3] = {64, 2, (cuuint32_t)kPage};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pages), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int G, bool MASS, int WK>
+template <int G, bool MASS, int WK, bool BF>
 cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    using C = PersCfg<WK>;
+    using C = PersCfg<WK, BF>;
     const size_t smem = sizeof(typename C::Smem) + 1024;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
@@ -784,31 +921,36 @@ cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(decode_split_pers_kernel<G, MASS, WK>,
+        e = cudaFuncSetAttribute(decode_split_pers_kernel<G, MASS, WK, BF>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const long long rows = (long long)a.num_pages * p.Hkv * kPage;
     alignas(64) CUtensorMap tmk, tmv;
-    if ((e = pool_tensor_map(&tmk, a.k_pages, rows)) != cudaSuccess) return e;
-    if ((e = pool_tensor_map(&tmv, a.v_pages, rows)) != cudaSuccess) return e;
-    return launch_pdl(decode_split_pers_kernel<G, MASS, WK>, dim3(p.pers_ctas), dim3(C::NT), smem, s, tmk,
-                      tmv, a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
+    if ((e = pool_tensor_map(&tmk, a.k_pages, rows, BF)) != cudaSuccess) return e;
+    if ((e = pool_tensor_map(&tmv, a.v_pages, rows, BF)) != cudaSuccess) return e;
+    return launch_pdl(decode_split_pers_kernel<G, MASS, WK, BF>, dim3(p.pers_ctas), dim3(C::NT), smem, s,
+                      tmk, tmv, a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
 }
 
-template <int G, int WK>
+template <int G, int WK, bool BF>
 cudaError_t launch_pers_gw(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    return a.mscore ? launch_pers_gm<G, true, WK>(a, p, s) : launch_pers_gm<G, false, WK>(a, p, s);
+    return a.mscore ? launch_pers_gm<G, true, WK, BF>(a, p, s) : launch_pers_gm<G, false, WK, BF>(a, p, s);
+}
+
+template <int G, bool BF>
+cudaError_t launch_pers_gb(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    switch (p.pers_ctas > 0 ? p.workers / p.pers_ctas : 0) {
+        case 8: return launch_pers_gw<G, 8, BF>(a, p, s);
+        case 12: return launch_pers_gw<G, 12, BF>(a, p, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <int G>
 cudaError_t launch_pers_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    switch (p.pers_ctas > 0 ? p.workers / p.pers_ctas : 0) {
-        case 8: return launch_pers_gw<G, 8>(a, p, s);
-        case 12: return launch_pers_gw<G, 12>(a, p, s);
-    }
-    return cudaErrorInvalidValue;
+    return p.dtype == PFKV_KV_BF16 ? launch_pers_gb<G, true>(a, p, s) : launch_pers_gb<G, false>(a, p, s);
 }
 
 }  // namespace
@@ -825,7 +967,8 @@ int pers_workers_for(long long units_bound, int num_sms) {
 bool pers_supported(const DecodePlan &p, int num_pages) {
     const long long rows = (long long)num_pages * p.Hkv * kPage;
     const long long K = (long long)p.B * p.Hkv * p.nchunks;
-    return p.dtype == PFKV_KV_FP8_E4M3 && p.D == 128 && p.G <= 4 && rows < (1LL << 31) &&
+    return (p.dtype == PFKV_KV_FP8_E4M3 || p.dtype == PFKV_KV_BF16) && p.D == 128 && p.G <= 4 &&
+           rows < (1LL << 31) &&
            K <= kPersMaxSegments && p.Breq <= kPersMaxRequests;
 }
 
