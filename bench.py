@@ -257,6 +257,8 @@ class PreparedMassStep(PreparedStep):
 # the arithmetic of the FP8 path (head_dim 128, query groups of up to 4 heads):
 # e4m3 bytes converted exactly to f16, products on the tensor cores, fp32 sums
 FP8_DTYPE = "fp8_e4m3 KV, f16 x f16 tensor-core MMA with fp32 accumulation, bf16 q/out"
+# BF16 pools with head_dim 128 and groups of up to 4 heads: the same kernel
+BF16_MMA_DTYPE = "bf16 KV, bf16 x bf16 tensor-core MMA with fp32 accumulation, bf16 q/out"
 
 
 def profiled_traffic(bytes_per_launch: float):
@@ -784,7 +786,9 @@ def run_workload(args):
         "warmup": args.warmup, "ms_per_step": r0["ms_per_step"], "p10_ms": r0["p10_ms"],
         "p90_ms": r0["p90_ms"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": FP8_DTYPE if spec.kv_dtype == "fp8" else "bf16 KV, fp32 accumulate, bf16 q/out",
+        "dtype": (FP8_DTYPE if spec.kv_dtype == "fp8" else
+                  BF16_MMA_DTYPE if spec.D == 128 and spec.Hq // spec.Hkv <= 4 else
+                  "bf16 KV, fp32 FMA, bf16 q/out"),
         "data": "synthetic", "config": cfg,
         "tokens_per_s": round(world * spec.B / (N_LAYERS * med_s), 1),
         "tokens_per_s_per_layer": round(world * spec.B / med_s, 1),
