@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
         S[g] = 0.f;
         acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    constexpr int RB = 4;  // rows in flight per warp
+    constexpr int RB = G == 8 ? 1 : 4;  // rows in flight per warp (registers)
     for (int j0 = warp; j0 < R; j0 += RB * NW) {
         float lc[RB][G];
         float4 ov[RB][G];
@@ -304,11 +304,18 @@ template <int G>
 cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     const int W = p.workers;  // as the plan sized the split kernel
     const dim3 grid((unsigned)(p.B * p.Hkv));
-    if (p.nchunks == 1)
+    // 8 warps for one chunk per head, 16 for many (8 for groups of 8 heads:
+    // 16 warps x 8 heads would not fit static shared memory)
+    if constexpr (G == 8) {
         return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks, W,
                           (const int *)a.ws_prefix);
-    return launch_pdl(decode_combine_pers_kernel<G, 16>, grid, dim3(16 * 32), 0, s, a, p.Hkv, p.nchunks, W,
-                      (const int *)a.ws_prefix);
+    } else {
+        if (p.nchunks == 1)
+            return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks,
+                              W, (const int *)a.ws_prefix);
+        return launch_pdl(decode_combine_pers_kernel<G, 16>, grid, dim3(16 * 32), 0, s, a, p.Hkv, p.nchunks, W,
+                          (const int *)a.ws_prefix);
+    }
 }
 
 }  // namespace
@@ -318,6 +325,7 @@ cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaSt
         case 1: return launch_combine_g<1>(a, p, s);
         case 2: return launch_combine_g<2>(a, p, s);
         case 4: return launch_combine_g<4>(a, p, s);
+        case 8: return launch_combine_g<8>(a, p, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -1,6 +1,6 @@
 // decode_pers.cu -- persistent, load-balanced split-KV decode attention for
-// e4m3 pools with head_dim 128 and query groups of up to 4 heads, plus the
-// combine kernel that merges its partial rows.
+// FP8 e4m3 or BF16 pools with head_dim 128 and query groups of up to 8 heads
+// (its partial rows are merged by combine_pers.cu).
 //
 // What is computed is the attention of decode.cu (single query per head over
 // the tokens its kv head holds, read through the block table from the FP8
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
                              int nchunks, int chunk_tokens, int *ws_prefix) {
     using C = PersCfg<WK, BF>;
     constexpr int ST = C::STAGES;
-    static_assert(G == 1 || G == 2 || G == 4, "query groups of 1, 2 or 4 heads");
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "query groups of 1, 2, 4 or 8 heads");
     extern __shared__ uint8_t smem_raw[];
     typename C::Smem &sm = *reinterpret_cast<typename C::Smem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -967,7 +967,7 @@ int pers_workers_for(long long units_bound, int num_sms) {
 bool pers_supported(const DecodePlan &p, int num_pages) {
     const long long rows = (long long)num_pages * p.Hkv * kPage;
     const long long K = (long long)p.B * p.Hkv * p.nchunks;
-    return (p.dtype == PFKV_KV_FP8_E4M3 || p.dtype == PFKV_KV_BF16) && p.D == 128 && p.G <= 4 &&
+    return (p.dtype == PFKV_KV_FP8_E4M3 || p.dtype == PFKV_KV_BF16) && p.D == 128 && p.G <= 8 &&
            rows < (1LL << 31) &&
            K <= kPersMaxSegments && p.Breq <= kPersMaxRequests;
 }
@@ -977,6 +977,7 @@ cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStre
         case 1: return launch_pers_g<1>(a, p, s);
         case 2: return launch_pers_g<2>(a, p, s);
         case 4: return launch_pers_g<4>(a, p, s);
+        case 8: return launch_pers_g<8>(a, p, s);
     }
     return cudaErrorInvalidValue;
 }

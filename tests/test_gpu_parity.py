@@ -91,6 +91,16 @@ def test_twelve_worker_shape(B, split):
     run_and_compare(spec, label=f"llama8b-small 12 workers split={split}", max_seq_len=131072)
 
 
+@pytest.mark.parametrize("kv_dtype", ["fp8", "bf16"])
+@pytest.mark.parametrize("bound", [None, 131072])
+def test_groups_of_eight_heads(B, kv_dtype, bound):
+    """64 query heads over 8 kv heads: groups of 8, so every MMA column is a
+    real head; one segment per head.  The large length bound selects the
+    12-worker shape."""
+    spec = dataclasses.replace(W.spec_llama8b("small"), Hq=64, kv_dtype=kv_dtype, name="g8")
+    run_and_compare(spec, label=f"g8 {kv_dtype} bound={bound}", max_seq_len=bound)
+
+
 def test_long_small_split(B):
     run_and_compare(W.spec_long("small"), label="long-small")
 
