@@ -171,7 +171,7 @@ def test_evict_full_without_tags(B):
         _check_head(db, b, int(np.argmax(lens[b])), False)
 
 
-@pytest.mark.parametrize("batch,kv_dtype", [(64, "fp8"), (8, "bf16"), (1, "fp8")])
+@pytest.mark.parametrize("batch,kv_dtype", [(64, "fp8"), (8, "bf16"), (32, "bf16"), (1, "fp8")])
 def test_sweep_points_on_an_80_gb_pool(B, batch, kv_dtype):
     spec = W.spec_sweep(batch, kv_dtype)
     samples = [(0, 0), (batch - 1, 7)]
