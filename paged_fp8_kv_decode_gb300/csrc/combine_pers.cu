@@ -304,13 +304,14 @@ template <int G>
 cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     const int W = p.workers;  // as the plan sized the split kernel
     const dim3 grid((unsigned)(p.B * p.Hkv));
-    // 8 warps for one chunk per head, 16 for many (8 for groups of 8 heads:
-    // 16 warps x 8 heads would not fit static shared memory)
+    // 8 warps for one chunk per head with few rows, 16 for many chunks or
+    // more than 16 workers per head on average (8 for groups of 8 heads: 16
+    // warps x 8 heads would not fit static shared memory)
     if constexpr (G == 8) {
         return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks, W,
                           (const int *)a.ws_prefix);
     } else {
-        if (p.nchunks == 1)
+        if (p.nchunks == 1 && (long long)W <= 16LL * p.B * p.Hkv)
             return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks,
                               W, (const int *)a.ws_prefix);
         return launch_pdl(decode_combine_pers_kernel<G, 16>, grid, dim3(16 * 32), 0, s, a, p.Hkv, p.nchunks, W,
