@@ -5,6 +5,8 @@
 // FP8 e4m3 cache instead of BF16: "Cloudflare quantizes Kimi and GLM caches
 // for 41% faster inference", 2nd paragraph.  Tag check as a separate batch
 // validation before decode reads: same page, 4th paragraph.
+#include <type_traits>
+
 #include "pfkv_internal.cuh"
 
 namespace pfkv {
@@ -21,7 +23,17 @@ constexpr int kAppendWarps = 4;
 template <int D, bool FP8>
 __device__ __forceinline__ void append_unit(const AppendArgs &a, int bh, int k, int lane) {
     constexpr int EPL = D / 32;  // elements per lane per row (4 or 2)
+    using Vec = typename std::conditional<EPL == 4, uint2, uint32_t>::type;
     const int b = bh / a.Hkv, h = bh - b * a.Hkv;
+    // A decode step appends one token: then unit 0 is the only one written, and
+    // its row (row bh of k_new / v_new) does not depend on the position, so it
+    // loads while the position and the page id are fetched.
+    const bool one = a.T == 1;
+    Vec kpre{}, vpre{};
+    if (one && k == 0) {
+        kpre = *reinterpret_cast<const Vec *>(a.k_new + (long long)bh * D + lane * EPL);
+        vpre = *reinterpret_cast<const Vec *>(a.v_new + (long long)bh * D + lane * EPL);
+    }
 
     const long long li = (long long)b * a.len_sb + (long long)h * a.len_sh;
     const int p0 = a.positions[li];
@@ -47,24 +59,45 @@ __device__ __forceinline__ void append_unit(const AppendArgs &a, int bh, int k, 
         return;
     }
     const long long u = (long long)phys * a.Hkv + h;
+    const int slot0 = (int)((p0 + tb) % kPage);
+    // the unit's stored scales (used when this call does not open the unit)
+    // load in the same round as its tag
+    float kscale_st = 1.f, vscale_st = 1.f;
+    if (FP8 && slot0 != 0) {
+        kscale_st = a.k_scale[u];
+        vscale_st = a.v_scale[u];
+    }
     if (a.page_tags && a.expected_tags && a.page_tags[u] != a.expected_tags[bi]) {
         if (lane == 0 && a.flags) atomic_or_byte(a.flags, b, PFKV_FLAG_TAG_MISMATCH);
         return;
     }
-    const int slot0 = (int)((p0 + tb) % kPage);
     const int cnt = (int)(te - tb);
     const long long src_row0 = ((long long)(b * a.Hkv + h) * a.T + tb);
     const __nv_bfloat16 *ksrc = a.k_new + src_row0 * D + lane * EPL;
     const __nv_bfloat16 *vsrc = a.v_new + src_row0 * D + lane * EPL;
     const long long dst_row0 = u * kPage + slot0;
 
+    // element e of this lane's part of row j of the new tokens (K or V)
+    auto elem = [&](const __nv_bfloat16 *src, const Vec &pre, int j, int e) {
+        if (one) {  // the preloaded row (j is 0)
+            uint32_t w;
+            if constexpr (EPL == 4) w = e < 2 ? pre.x : pre.y;
+            else w = pre;
+            return (e & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+        }
+        return __bfloat162float(src[(long long)j * D + e]);
+    };
     if constexpr (!FP8) {
-        using Vec = typename std::conditional<EPL == 4, uint2, uint32_t>::type;
         Vec *kd = reinterpret_cast<Vec *>(static_cast<__nv_bfloat16 *>(a.k_pages) + dst_row0 * D) + lane;
         Vec *vd = reinterpret_cast<Vec *>(static_cast<__nv_bfloat16 *>(a.v_pages) + dst_row0 * D) + lane;
-        for (int j = 0; j < cnt; ++j) {
-            kd[j * (D / EPL)] = *reinterpret_cast<const Vec *>(ksrc + (long long)j * D);
-            vd[j * (D / EPL)] = *reinterpret_cast<const Vec *>(vsrc + (long long)j * D);
+        if (one) {
+            kd[0] = kpre;
+            vd[0] = vpre;
+        } else {
+            for (int j = 0; j < cnt; ++j) {
+                kd[j * (D / EPL)] = *reinterpret_cast<const Vec *>(ksrc + (long long)j * D);
+                vd[j * (D / EPL)] = *reinterpret_cast<const Vec *>(vsrc + (long long)j * D);
+            }
         }
     } else {
         float kscale, vscale;
@@ -74,8 +107,8 @@ __device__ __forceinline__ void append_unit(const AppendArgs &a, int bh, int k, 
             for (int j = 0; j < cnt; ++j) {
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) {
-                    ka = fmaxf(ka, fabsf(__bfloat162float(ksrc[(long long)j * D + e])));
-                    va = fmaxf(va, fabsf(__bfloat162float(vsrc[(long long)j * D + e])));
+                    ka = fmaxf(ka, fabsf(elem(ksrc, kpre, j, e)));
+                    va = fmaxf(va, fabsf(elem(vsrc, vpre, j, e)));
                 }
             }
 #pragma unroll
@@ -90,8 +123,8 @@ __device__ __forceinline__ void append_unit(const AppendArgs &a, int bh, int k, 
                 a.v_scale[u] = vscale;
             }
         } else {
-            kscale = a.k_scale[u];
-            vscale = a.v_scale[u];
+            kscale = kscale_st;
+            vscale = vscale_st;
         }
         uint8_t *kd = static_cast<uint8_t *>(a.k_pages) + dst_row0 * D + lane * EPL;
         uint8_t *vd = static_cast<uint8_t *>(a.v_pages) + dst_row0 * D + lane * EPL;
@@ -99,8 +132,8 @@ __device__ __forceinline__ void append_unit(const AppendArgs &a, int bh, int k, 
             uint32_t kw = 0, vw = 0;
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
-                const float kx = __bfloat162float(ksrc[(long long)j * D + e]);
-                const float vx = __bfloat162float(vsrc[(long long)j * D + e]);
+                const float kx = elem(ksrc, kpre, j, e);
+                const float vx = elem(vsrc, vpre, j, e);
                 kw |= (uint32_t)float_to_e4m3(__fdiv_rn(kx, kscale)) << (8 * e);
                 vw |= (uint32_t)float_to_e4m3(__fdiv_rn(vx, vscale)) << (8 * e);
             }
@@ -145,20 +178,25 @@ cudaError_t launch_kv_append(const AppendArgs &a, int B, cudaStream_t s) {
 __device__ __forceinline__ void validate_tile(const DecodeArgs &a, int Hkv, int bh, int tile) {
     const int b = bh / Hkv, h = bh - b * Hkv;
     const int n = a.seq_lens[(long long)b * a.len_sb + (long long)h * a.len_sh];
+    // the tile's table entries and expected tags load with the length (every
+    // entry below max_pages is in the caller's table); the length then says
+    // which of them are live
+    const int p0 = tile * kValTile + threadIdx.x;
+    const long long row = (long long)b * a.bt_sb + (long long)h * a.bt_sh;
+    int id[kValPer];
+    uint32_t want[kValPer];
+#pragma unroll
+    for (int j = 0; j < kValPer; ++j) {
+        const int p = p0 + j * kValThreads;
+        id[j] = p < a.max_pages ? a.block_tables[row + p] : 0;
+        want[j] = p < a.max_pages ? a.expected_tags[row + p] : 0u;
+    }
     uint32_t bits = 0;
     if (n < 0 || (long long)n > (long long)a.max_pages * kPage || n > a.max_seq_len) {
         bits = PFKV_FLAG_BAD_LENGTH;
     } else {
         const int np = (n + kPage - 1) / kPage;
-        const int p0 = tile * kValTile + threadIdx.x;
-        const long long row = (long long)b * a.bt_sb + (long long)h * a.bt_sh;
-        int id[kValPer];
-#pragma unroll
-        for (int j = 0; j < kValPer; ++j) {
-            const int p = p0 + j * kValThreads;
-            id[j] = p < np ? a.block_tables[row + p] : 0;
-        }
-        uint32_t tag[kValPer], want[kValPer];
+        uint32_t tag[kValPer];
 #pragma unroll
         for (int j = 0; j < kValPer; ++j) {
             const int p = p0 + j * kValThreads;
@@ -167,7 +205,7 @@ __device__ __forceinline__ void validate_tile(const DecodeArgs &a, int Hkv, int 
             if (live && !in_pool) bits |= PFKV_FLAG_BAD_PAGE;
             const bool check = live && in_pool;
             tag[j] = check ? a.page_tags[(long long)id[j] * Hkv + h] : 0u;
-            want[j] = check ? a.expected_tags[row + p] : 0u;
+            if (!check) want[j] = 0u;
         }
 #pragma unroll
         for (int j = 0; j < kValPer; ++j)
