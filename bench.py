@@ -433,63 +433,67 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
+def e2e_step_graph(db, B, fused_tags):
+    """One end-to-end step as a CUDA graph: the host-to-device copy of the
+    step's packed inputs from pinned memory, the public pfkv_decode_step call
+    (or the attention call where the workload does not append), and the
+    device-to-host copy of the packed output (out and flags).  Returns the
+    graph and its pinned host buffers."""
+    import torch
+    s = torch.cuda.Stream()
+    h_in = db.io_in.detach().cpu().pin_memory()
+    h_out = torch.empty_like(db.io_out, device="cpu").pin_memory()
+    step = PreparedStep(db, B, s.cuda_stream, fused_tags=fused_tags)
+    with torch.cuda.stream(s):  # warm the call on the capture stream
+        step.full_step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        db.io_in.copy_(h_in, non_blocking=True)
+        step.full_step()
+        h_out.copy_(db.io_out, non_blocking=True)
+    torch.cuda.synchronize()
+    return g, h_in, h_out
+
+
+def e2e_bytes(db):
+    h2d = sum(t.numel() * t.element_size() for t in
+              [db.q, db.positions, db.seq_lens, db.block_tables]
+              + ([db.k_new, db.v_new] if db.spec.append else [])
+              + ([db.expected_tags] if db.cache.page_tags is not None else []))
+    d2h = db.out.numel() * db.out.element_size() + db.flags.numel()
+    return int(h2d), int(d2h)
+
+
+E2E_API = ("every step: one replay of a CUDA graph holding the host-to-device copy of "
+           "the packed inputs (pinned host memory), the public pfkv_decode_step call and "
+           "the device-to-host copy of the packed outputs; then a stream synchronize")
+
+
 def run_e2e(args, reps, B, stream, step_bytes, world, dev):
     """Same metric through the public API with host buffers: each step copies
     its inputs (q, new K/V rows, positions, lengths, block table, expected
     tags: packed in one buffer) from pinned host memory, runs append +
-    attention, and reads the output and flags (one buffer) back."""
+    attention, and reads the output and flags (one buffer) back, waiting for
+    them before the next step."""
     import torch
     K = max(1, min(args.e2e_steps, args.steps))
-    host = []
-    for p in reps:
-        db = p.db
-        tensors_in, tensors_out = [db.io_in], [db.io_out]
-        h_in = [t.detach().cpu().pin_memory() for t in tensors_in]
-        h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in tensors_out]
-        host.append((tensors_in, h_in, h_out, tensors_out))
-    # one single-layer step graph per replica: the step (append + attention)
-    # is then one launch through the public API
-    graphs = []
-    for p in reps:
-        db = p.db
-        layer = B.Layer(cache=db.cache, q=db.q, out=db.out, k_new=db.k_new, v_new=db.v_new,
-                        flags=db.flags)
-        graphs.append(B.pfkv_step_graph_create(
-            [layer], db.pages, db.positions, None, 1 if db.spec.append else 0, db.append_flags,
-            db.spec.Hq, db.spec.sm_scale, db.split_tokens, db.max_seq_len, db.workspace,
-            B.PFKV_STAGE_FUSED_TAGS if args.fused_tags else 0))
-    # bytes the step's tensors hold (the packing's alignment padding excluded)
-    db0 = reps[0].db
-    h2d = sum(t.numel() * t.element_size() for t in
-              [db0.q, db0.positions, db0.seq_lens, db0.block_tables]
-              + ([db0.k_new, db0.v_new] if db0.spec.append else [])
-              + ([db0.expected_tags] if db0.cache.page_tags is not None else []))
-    d2h = db0.out.numel() * db0.out.element_size() + db0.flags.numel()
+    graphs = [e2e_step_graph(p.db, B, args.fused_tags)[0] for p in reps]
+    h2d, d2h = e2e_bytes(reps[0].db)
     for i in range(5):
-        graphs[i % len(reps)].launch(stream)
+        graphs[i % len(reps)].replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for i in range(K):
-        r = i % len(reps)
-        p = reps[r]
-        d_in, h_in, h_out, d_out = host[r]
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        graphs[r].launch(stream)
-        for h, d in zip(h_out, d_out):
-            h.copy_(d, non_blocking=True)
+        graphs[i % len(reps)].replay()
         stream.synchronize()
     el = time.perf_counter() - t0
     el = reduce_max(el, world, dev)
-    for g in graphs:
-        g.close()
     return {"value": round(aggregate(step_bytes, K, el, world), 2), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K,
-            "ms_per_step": round(el / K * 1e3, 4),
-            "api": "inputs and outputs packed (one copy each way); the step is one "
-                   "pfkv_step_graph_launch of a 1-layer graph"}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "ms_per_step": round(el / K * 1e3, 4), "api": E2E_API}
 
 
 # --------------------------------------------------------------------------
@@ -827,33 +831,21 @@ def run_e2e_flushed(args, p, B, stream, step_bytes, world, dev, flush):
     each step outside the host-timed interval."""
     import torch
     K = max(1, min(args.e2e_steps, args.steps))
-    db = p.db
-    d_in, d_out = [db.io_in], [db.io_out]
-    h_in = [t.detach().cpu().pin_memory() for t in d_in]
-    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in d_out]
-    h2d = sum(t.numel() * t.element_size() for t in
-              [db.q, db.positions, db.seq_lens, db.block_tables]
-              + ([db.k_new, db.v_new] if db.spec.append else [])
-              + ([db.expected_tags] if db.cache.page_tags is not None else []))
-    d2h = db.out.numel() * db.out.element_size() + db.flags.numel()
+    g, _, _ = e2e_step_graph(p.db, B, bool(p.opt))
+    h2d, d2h = e2e_bytes(p.db)
     total = 0.0
     for i in range(K + 2):
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        p.append()
-        p.stage(B.PFKV_STAGE_ALL)
-        for h, d in zip(h_out, d_out):
-            h.copy_(d, non_blocking=True)
+        g.replay()
         stream.synchronize()
         if i >= 2:
             total += time.perf_counter() - t0
     total = reduce_max(total, world, dev)
     return {"value": round(aggregate(step_bytes, K, total, world), 2), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": K, "ms_per_step": round(total / K * 1e3, 4)}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": K, "ms_per_step": round(total / K * 1e3, 4), "api": E2E_API}
 
 
 def run_graph(args):
