@@ -254,19 +254,29 @@ class PreparedMassStep(PreparedStep):
             raise RuntimeError(f"pfkv_paged_decode_attn_mass: status {st}")
 
 
-# the arithmetic of the FP8 path (head_dim 128, query groups of up to 4 heads):
+# the arithmetic of the FP8 path (head_dim 128, query groups of up to 8 heads):
 # e4m3 bytes converted exactly to f16, products on the tensor cores, fp32 sums
 FP8_DTYPE = "fp8_e4m3 KV, f16 x f16 tensor-core MMA with fp32 accumulation, bf16 q/out"
-# BF16 pools with head_dim 128 and groups of up to 4 heads: the same kernel
+# BF16 pools with head_dim 128 and groups of up to 8 heads: the same kernel
 BF16_MMA_DTYPE = "bf16 KV, bf16 x bf16 tensor-core MMA with fp32 accumulation, bf16 q/out"
 
 
-def profiled_traffic(bytes_per_launch: float):
-    """DRAM bytes per launch of the split kernel from the committed ncu summary,
-    scaled to this run's algorithmic bytes; None if the kernel source changed
-    since the capture (or there is no summary)."""
+def path_dtype(spec) -> str:
+    """The arithmetic a workload's split kernel computes in: the tensor-core
+    kernel takes head_dim 128 with groups of up to 8 heads, the CUDA-core
+    kernels everything else."""
+    mma = spec.D == 128 and spec.Hq // spec.Hkv <= 8
+    if spec.kv_dtype == "fp8":
+        return FP8_DTYPE if mma else "fp8_e4m3 KV, fp32 FMA, bf16 q/out"
+    return BF16_MMA_DTYPE if mma else "bf16 KV, fp32 FMA, bf16 q/out"
+
+
+def profiled_traffic(bytes_per_launch: float, summary: str = "decode_split_pers_llama8b_fp8.md"):
+    """DRAM bytes per launch of the split kernel from a committed ncu summary of
+    the same workload, scaled to this run's algorithmic bytes; None if the
+    kernel source changed since the capture (or there is no summary)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "decode_split_pers_llama8b_fp8.md")
+    path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
     kv = {}
@@ -283,6 +293,17 @@ def profiled_traffic(bytes_per_launch: float):
             kv["algorithmic_bytes_per_launch"])
     except (KeyError, OSError, ValueError):
         return None
+
+
+# workloads with a committed ncu capture of their own split-kernel launch
+WORKLOAD_PROFILES = {"long": "decode_split_pers_long_fp8.md"}
+
+
+def workload_traffic(workload: str, bytes_per_launch: float):
+    if workload not in WORKLOAD_PROFILES:
+        return None
+    t = profiled_traffic(bytes_per_launch, WORKLOAD_PROFILES[workload])
+    return None if t is None else int(t)
 
 
 def peaks():
@@ -790,16 +811,15 @@ def run_workload(args):
         "warmup": args.warmup, "ms_per_step": r0["ms_per_step"], "p10_ms": r0["p10_ms"],
         "p90_ms": r0["p90_ms"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": (FP8_DTYPE if spec.kv_dtype == "fp8" else
-                  BF16_MMA_DTYPE if spec.D == 128 and spec.Hq // spec.Hkv <= 4 else
-                  "bf16 KV, fp32 FMA, bf16 q/out"),
+        "dtype": path_dtype(spec),
         "data": "synthetic", "config": cfg,
         "tokens_per_s": round(world * spec.B / (N_LAYERS * med_s), 1),
         "tokens_per_s_per_layer": round(world * spec.B / med_s, 1),
         "pct_of_hbm_peak": round(100 * r0["gbs"] / world / peak, 2),
         "roofline": {"kernel": "decode_split", "bound": "hbm", "achieved": round(split_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(split_gbs / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind,
+                     "traffic": workload_traffic(args.workload, split_bytes),
+                     "peak_kind": peak_kind,
                      "avg_launch_us": round(split_med * 1e3, 3), "stat": "median",
                      "bytes_per_launch": int(split_bytes), "timed_launches": len(split_ms)},
         "variants": results if len(results) > 1 else None,
