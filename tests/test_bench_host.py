@@ -91,3 +91,36 @@ def test_clocks_path_defaults_to_a_temporary_file(tmp_path):
     a = bench.parse_args(["--clocks-csv", str(tmp_path / "sub" / "c.csv")])
     assert bench.clocks_path(a) == str(tmp_path / "sub" / "c.csv")
     assert os.path.isdir(tmp_path / "sub")
+
+
+def test_roofline_traffic_comes_from_the_capture_of_the_same_source(tmp_path, monkeypatch):
+    """roofline.traffic is the committed capture's DRAM bytes scaled to the
+    run's algorithmic bytes, and null once the kernel source has changed, or
+    for a workload with no capture of its own."""
+    for name in ("decode_split_pers_llama8b_fp8.md", "decode_split_pers_long_fp8.md"):
+        assert os.path.exists(os.path.join(ROOT, "profiles", name)), name
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    import hashlib
+    digest = hashlib.sha256(b"kernel v1\n").hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "s.md").write_text(
+        "text: ignored\n    kernel_source: k.cu\n"
+        f"    kernel_source_sha256_16: {digest}\n"
+        "    dram_bytes_per_launch: 1020\n    algorithmic_bytes_per_launch: 1000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic(2000, "s.md") == pytest.approx(2040)
+    assert bench.profiled_traffic(2000, "missing.md") is None
+    monkeypatch.setattr(bench, "WORKLOAD_PROFILES", {"long": "s.md"})
+    assert bench.workload_traffic("long", 500) == 510
+    assert bench.workload_traffic("sweep", 500) is None
+    src.write_text("kernel v2\n")
+    assert bench.profiled_traffic(2000, "s.md") is None
+    assert bench.workload_traffic("long", 500) is None
+
+
+def test_dtype_label_follows_the_kernel_path():
+    llama = W.spec_llama8b("small")
+    assert bench.path_dtype(llama) == bench.FP8_DTYPE
+    assert "fp32 FMA" in bench.path_dtype(W.spec_tiny())  # head_dim 64: CUDA-core kernel
+    assert bench.path_dtype(W.spec_sweep(8, "bf16", "small")) == bench.BF16_MMA_DTYPE
