@@ -30,8 +30,11 @@ __device__ __forceinline__ float plog2(float x) {
 }  // namespace
 
 // --------------------------------------------------------------------------
-// One CTA of NW warps per (request b, kv head h), two rounds of loads (8
-// warps when a head has one chunk and few rows, 16 when it has many chunks):
+// One CTA of NW warps per (request b, kv head h) and group of GS of its G
+// query heads, two rounds of loads.  A head with one chunk and few rows takes
+// one CTA of 8 warps for all G query heads (GS = G); a head with many chunks
+// or many rows takes one CTA of 16 warps per query head (GS = 1), so that the
+// rows' bytes are spread over G times as many SMs:
 //  1. the unit prefix of every segment of the request and of every chunk of
 //     (b, h), the request's lengths and validation words; the chunks' row
 //     counts are scanned into a flat row order (chunk c owns flat rows
@@ -48,7 +51,7 @@ constexpr int kCombMaxChunks = kPersMaxSegments;  // segments per (b, h) <= all 
 constexpr int kCombShortList = 8;                  // status rows a thread gathers itself
 constexpr int kCombMaxDeferred = 256;              // longer lists handed to warps
 
-template <int G, int NW>
+template <int GS, int NW>
 struct CombSmem {
     union {
         struct {
@@ -56,9 +59,9 @@ struct CombSmem {
             int cbase[kCombMaxChunks];
         } rows;
         struct {
-            float acc[NW][G][128];
-            float wsum[NW][G];
-            float wmax[NW][G];
+            float acc[NW][GS][128];
+            float wsum[NW][GS];
+            float wmax[NW][GS];
         } red;
     } u;
     int part[NW * 32];
@@ -67,16 +70,19 @@ struct CombSmem {
     int ndef;
 };
 
-template <int G, int NW>
+template <int G, int GS, int NW>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
                                                                           int nchunks, int W,
                                                                           const int *ws_prefix) {
-    constexpr int D = 128, NT = NW * 32;
-    __shared__ CombSmem<G, NW> sm;
+    static_assert(G % GS == 0, "query-head groups split G evenly");
+    constexpr int D = 128, NT = NW * 32, HG = G / GS;
+    __shared__ CombSmem<GS, NW> sm;
     pdl_enter();
-    const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
+    // CTA (b, h, gi) merges query heads gi GS .. gi GS + GS - 1 of (b, h)
+    const int bhx = blockIdx.x / HG, gi = blockIdx.x - bhx * HG, g0 = gi * GS;
+    const int b = bhx / Hkv, h = bhx - b * Hkv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int B = gridDim.x / Hkv;
+    const int B = gridDim.x / (Hkv * HG);
     const int K = B * Hkv * nchunks;
     const int U = ws_prefix[K];
     W = min(W, U);  // as in the split kernel
@@ -172,33 +178,33 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
         for (int i = 0; i < kCombShortList; ++i)
             if (i < scnt) st[i] = a.status[sk + sp0 + i];
     }
-    float M[G], S[G];
-    float4 acc[G];
+    float M[GS], S[GS];
+    float4 acc[GS];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < GS; ++g) {
         M[g] = -INFINITY;
         S[g] = 0.f;
         acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    constexpr int RB = G == 8 ? 1 : 4;  // rows in flight per warp (registers)
+    constexpr int RB = GS == 8 ? 1 : GS == 1 ? 8 : 4;  // rows in flight per warp (registers)
     for (int j0 = warp; j0 < R; j0 += RB * NW) {
-        float lc[RB][G];
-        float4 ov[RB][G];
+        float lc[RB][GS];
+        float4 ov[RB][GS];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
             const int j = j0 + r * NW;
             const long long row = j < R ? row_of(j) : 0;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                lc[r][g] = j < R ? a.lse[row * G + g] : -INFINITY;
-                ov[r][g] = j < R ? *reinterpret_cast<const float4 *>(a.o + (row * G + g) * D + lane * 4)
+            for (int g = 0; g < GS; ++g) {
+                lc[r][g] = j < R ? a.lse[row * G + g0 + g] : -INFINITY;
+                ov[r][g] = j < R ? *reinterpret_cast<const float4 *>(a.o + (row * G + g0 + g) * D + lane * 4)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < GS; ++g) {
                 if (lc[r][g] == -INFINITY) continue;  // uniform: no token of this head in the row
                 if (lc[r][g] > M[g]) {
                     const float sc = M[g] == -INFINITY ? 0.f : pexp2(M[g] - lc[r][g]);
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
     }
     if (f) atomicOr(&sm.flags, f);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < GS; ++g) {
         *reinterpret_cast<float4 *>(&sm.u.red.acc[warp][g][lane * 4]) = acc[g];
         if (lane == 0) {
             sm.u.red.wsum[warp][g] = S[g];
@@ -257,17 +263,17 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
     }
     __syncthreads();
     const uint32_t flags = sm.flags;
-    if (b == v0 && h == 0 && tid == 0 && a.flags) a.flags[rb] = (uint8_t)flags;
-    if (b == v0 && h == 0 && tid == 0 && a.rflags) a.rflags[rb] = (uint8_t)flags;
+    if (b == v0 && h == 0 && gi == 0 && tid == 0 && a.flags) a.flags[rb] = (uint8_t)flags;
+    if (b == v0 && h == 0 && gi == 0 && tid == 0 && a.rflags) a.rflags[rb] = (uint8_t)flags;
     const int n = max(0, query_len(a, b, h));
-    uint2 *out = reinterpret_cast<uint2 *>(a.out + (long long)(b * Hkv + h) * G * D);
+    uint2 *out = reinterpret_cast<uint2 *>(a.out + ((long long)(b * Hkv + h) * G + g0) * D);
     if (flags != 0 || n == 0 || U == 0) {
-        for (int i = tid; i < G * D / 4; i += NT) out[i] = make_uint2(0u, 0u);
+        for (int i = tid; i < GS * D / 4; i += NT) out[i] = make_uint2(0u, 0u);
         return;
     }
 
     // ---- out = merged sum / merged weight ----
-    for (int i = tid; i < G * D / 4; i += NT) {
+    for (int i = tid; i < GS * D / 4; i += NT) {
         const int g = i / (D / 4), d4 = i - g * (D / 4);
         float Mg = -INFINITY;
 #pragma unroll
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
         }
         const float inv = ws > 0.f ? 1.f / ws : 0.f;
         if (a.lse_fin && d4 == 0)
-            a.lse_fin[(long long)(b * Hkv + h) * G + g] = ws > 0.f ? Mg + plog2(ws) : -INFINITY;
+            a.lse_fin[(long long)(b * Hkv + h) * G + g0 + g] = ws > 0.f ? Mg + plog2(ws) : -INFINITY;
         const __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x * inv, s4.y * inv);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z * inv, s4.w * inv);
         out[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
@@ -303,20 +309,14 @@ namespace {
 template <int G>
 cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     const int W = p.workers;  // as the plan sized the split kernel
-    const dim3 grid((unsigned)(p.B * p.Hkv));
-    // 8 warps for one chunk per head with few rows, 16 for many chunks or
-    // more than 16 workers per head on average (8 for groups of 8 heads: 16
-    // warps x 8 heads would not fit static shared memory)
-    if constexpr (G == 8) {
-        return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks, W,
-                          (const int *)a.ws_prefix);
-    } else {
-        if (p.nchunks == 1 && (long long)W <= 16LL * p.B * p.Hkv)
-            return launch_pdl(decode_combine_pers_kernel<G, 8>, grid, dim3(8 * 32), 0, s, a, p.Hkv, p.nchunks,
-                              W, (const int *)a.ws_prefix);
-        return launch_pdl(decode_combine_pers_kernel<G, 16>, grid, dim3(16 * 32), 0, s, a, p.Hkv, p.nchunks, W,
-                          (const int *)a.ws_prefix);
-    }
+    const int heads = p.B * p.Hkv;
+    // many chunks, or more than 16 workers per head on average: 16 warps and
+    // one CTA per query head; otherwise 8 warps for all G query heads
+    if (p.nchunks > 1 || (long long)W > 16LL * heads)
+        return launch_pdl(decode_combine_pers_kernel<G, 1, 16>, dim3((unsigned)(heads * G)), dim3(16 * 32), 0,
+                          s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+    return launch_pdl(decode_combine_pers_kernel<G, G, 8>, dim3((unsigned)heads), dim3(8 * 32), 0, s, a,
+                      p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
 }
 
 }  // namespace
