@@ -33,8 +33,9 @@ __device__ __forceinline__ float plog2(float x) {
 // One CTA of NW warps per (request b, kv head h) and group of GS of its G
 // query heads, two rounds of loads.  A head with one chunk and few rows takes
 // one CTA of 8 warps for all G query heads (GS = G); a head with many chunks
-// or many rows takes one CTA of 16 warps per query head (GS = 1), so that the
-// rows' bytes are spread over G times as many SMs:
+// or many rows takes CTAs of 16 warps, one per group of GS query heads, with
+// GS as small as keeps all CTAs in one wave, so that the rows' bytes spread
+// over as many SMs as there are:
 //  1. the unit prefix of every segment of the request and of every chunk of
 //     (b, h), the request's lengths and validation words; the chunks' row
 //     counts are scanned into a flat row order (chunk c owns flat rows
@@ -306,17 +307,38 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
 // --------------------------------------------------------------------------
 namespace {
 
+template <int G, int GS, int NW>
+cudaError_t launch_comb(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    const unsigned grid = (unsigned)(p.B * p.Hkv * (G / GS));
+    return launch_pdl(decode_combine_pers_kernel<G, GS, NW>, dim3(grid), dim3(NW * 32), 0, s, a, p.Hkv,
+                      p.nchunks, p.workers, (const int *)a.ws_prefix);
+}
+
 template <int G>
 cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    const int W = p.workers;  // as the plan sized the split kernel
-    const int heads = p.B * p.Hkv;
-    // many chunks, or more than 16 workers per head on average: 16 warps and
-    // one CTA per query head; otherwise 8 warps for all G query heads
-    if (p.nchunks > 1 || (long long)W > 16LL * heads)
-        return launch_pdl(decode_combine_pers_kernel<G, 1, 16>, dim3((unsigned)(heads * G)), dim3(16 * 32), 0,
-                          s, a, p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
-    return launch_pdl(decode_combine_pers_kernel<G, G, 8>, dim3((unsigned)heads), dim3(8 * 32), 0, s, a,
-                      p.Hkv, p.nchunks, W, (const int *)a.ws_prefix);
+    const long long heads = (long long)p.B * p.Hkv;
+    // One chunk per head and at most 16 workers' rows per head on average: 8
+    // warps for all G query heads.
+    if (p.nchunks == 1 && (long long)p.workers <= 16 * heads) return launch_comb<G, G, 8>(a, p, s);
+    // Many rows per head: 16 warps (one CTA per SM), and the G query heads
+    // split into as many groups as keep every CTA in one wave over the SMs.
+    int hg = 1;
+    while (hg < G && heads * hg * 2 <= p.pers_ctas) hg *= 2;
+    if constexpr (G == 8) {
+        if (hg == 8) return launch_comb<8, 1, 16>(a, p, s);
+        if (hg == 4) return launch_comb<8, 2, 16>(a, p, s);
+        if (hg == 2) return launch_comb<8, 4, 16>(a, p, s);
+        return launch_comb<8, 8, 8>(a, p, s);  // 16 warps x 8 heads would not fit static shared memory
+    } else if constexpr (G == 4) {
+        if (hg == 4) return launch_comb<4, 1, 16>(a, p, s);
+        if (hg == 2) return launch_comb<4, 2, 16>(a, p, s);
+        return launch_comb<4, 4, 16>(a, p, s);
+    } else if constexpr (G == 2) {
+        if (hg == 2) return launch_comb<2, 1, 16>(a, p, s);
+        return launch_comb<2, 2, 16>(a, p, s);
+    } else {
+        return launch_comb<1, 1, 16>(a, p, s);
+    }
 }
 
 }  // namespace

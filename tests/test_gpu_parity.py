@@ -101,6 +101,20 @@ def test_groups_of_eight_heads(B, kv_dtype, bound):
     run_and_compare(spec, label=f"g8 {kv_dtype} bound={bound}", max_seq_len=bound)
 
 
+@pytest.mark.parametrize("Bn,G", [(1, 4), (5, 4), (9, 4), (20, 4), (1, 8), (3, 8), (5, 8), (10, 8)])
+def test_combine_query_head_groups(B, Bn, G):
+    """Many partial rows per kv head (64-token chunks): the combine splits each
+    kv head's G query heads over 1, 2, 4 or 8 CTAs, as many as keep one wave
+    over the SMs. On 152 SMs these batches take every split of G = 4 and
+    G = 8; a stale tag flags some requests."""
+    rng = np.random.default_rng(700 + 10 * Bn + G)
+    lens = rng.integers(60, 700, size=Bn, endpoint=True).astype(np.int32)
+    spec = W.Spec(f"comb{Bn}x{G}", B=Bn, Hq=8 * G, Hkv=8, D=128, kv_dtype="fp8",
+                  num_pages=int(((lens + 16) // 16 + 1).sum()) + 8, lens=lens, append=True,
+                  stale_per_mille=2.0 if Bn >= 5 else 0.0, split_tokens=64, seed=7000 + Bn)
+    run_and_compare(spec, label=f"combine groups B={Bn} G={G}")
+
+
 def test_long_small_split(B):
     run_and_compare(W.spec_long("small"), label="long-small")
 
