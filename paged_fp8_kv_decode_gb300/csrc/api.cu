@@ -37,6 +37,20 @@ pfkv_status device_check(int *num_sms) {
         }
         g_dev_sms[dev].store(sms, std::memory_order_relaxed);
         st = (major == 10 && minor == 3) ? 1 : 2;
+        if (st == 1) {
+            // load every kernel now, so that no launch of a later call, maybe
+            // inside a timed or captured region, pays for lazy module loading
+            cudaError_t e = preload_append();
+            if (e == cudaSuccess) e = preload_split_pers();
+            if (e == cudaSuccess) e = preload_combine_pers();
+            if (e == cudaSuccess) e = preload_split_generic();
+            if (e == cudaSuccess) e = preload_split_swz();
+            if (e == cudaSuccess) e = preload_mass();
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return PFKV_ERR_CUDA;
+            }
+        }
         g_dev_state[dev].store(st, std::memory_order_release);
     }
     if (st != 1) return PFKV_ERR_UNSUPPORTED;

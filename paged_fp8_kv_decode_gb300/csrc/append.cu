@@ -307,4 +307,21 @@ cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStre
     return cudaGetLastError();
 }
 
+cudaError_t preload_append() {
+    cudaError_t e = cudaSuccess;
+    auto one = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+    one(preload_kernel(kv_append_kernel<128, true>));
+    one(preload_kernel(kv_append_kernel<64, true>));
+    one(preload_kernel(kv_append_kernel<128, false>));
+    one(preload_kernel(kv_append_kernel<64, false>));
+    one(preload_kernel(validate_kernel));
+    one(preload_kernel(append_validate_kernel<128, true>));
+    one(preload_kernel(append_validate_kernel<64, true>));
+    one(preload_kernel(append_validate_kernel<128, false>));
+    one(preload_kernel(append_validate_kernel<64, false>));
+    one(preload_kernel(e4m3_encode_kernel));
+    one(preload_kernel(e4m3_decode_kernel));
+    return e;
+}
+
 }  // namespace pfkv

@@ -343,6 +343,25 @@ cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStrea
 
 }  // namespace
 
+cudaError_t preload_combine_pers() {
+    cudaError_t e = cudaSuccess;
+    auto one = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+    one(preload_kernel(decode_combine_pers_kernel<8, 8, 8>));
+    one(preload_kernel(decode_combine_pers_kernel<8, 4, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<8, 2, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<8, 1, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 4, 8>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 4, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 2, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 1, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<2, 2, 8>));
+    one(preload_kernel(decode_combine_pers_kernel<2, 2, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<2, 1, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<1, 1, 8>));
+    one(preload_kernel(decode_combine_pers_kernel<1, 1, 16>));
+    return e;
+}
+
 cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     switch (p.G) {
         case 1: return launch_combine_g<1>(a, p, s);

@@ -454,11 +454,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int Hkv
 // --------------------------------------------------------------------------
 // launch
 // --------------------------------------------------------------------------
+// the dynamic shared-memory opt-in is per device; set it once on each
 template <int D, int G, bool FP8>
-static cudaError_t launch_split_t(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    using C = SplitCfg<D, G, FP8>;
-    const size_t smem = sizeof(typename C::Smem);
-    // the dynamic shared-memory opt-in is per device; set it once on each
+static cudaError_t configure_split() {
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -466,10 +464,20 @@ static cudaError_t launch_split_t(const DecodeArgs &a, const DecodePlan &p, cuda
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(decode_split_kernel<D, G, FP8>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(typename SplitCfg<D, G, FP8>::Smem));
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
+    return cudaSuccess;
+}
+
+template <int D, int G, bool FP8>
+static cudaError_t launch_split_t(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    using C = SplitCfg<D, G, FP8>;
+    const size_t smem = sizeof(typename C::Smem);
+    cudaError_t e = configure_split<D, G, FP8>();
+    if (e != cudaSuccess) return e;
     const long long items = (long long)p.B * p.Hkv * p.nchunks;
     return launch_pdl(decode_split_kernel<D, G, FP8>, dim3((unsigned)items), dim3(C::NWARPS * 32),
                       smem, s, a, p.Hkv, p.chunk_tokens, p.nchunks);
@@ -496,6 +504,28 @@ cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t 
     if (p.kind == 1) return launch_split_pers(a, p, s);
     if (swz_supported(p, a.num_pages)) return launch_split_swz(a, p, s);
     return p.D == 128 ? launch_split_g<128>(a, p, s) : launch_split_g<64>(a, p, s);
+}
+
+template <int D>
+static cudaError_t preload_split_d() {
+    cudaError_t e = cudaSuccess;
+    auto one = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+    one(configure_split<D, 1, true>());
+    one(configure_split<D, 2, true>());
+    one(configure_split<D, 4, true>());
+    one(configure_split<D, 8, true>());
+    one(configure_split<D, 1, false>());
+    one(configure_split<D, 2, false>());
+    one(configure_split<D, 4, false>());
+    one(configure_split<D, 8, false>());
+    one(preload_kernel(decode_combine_kernel<D>));
+    return e;
+}
+
+cudaError_t preload_split_generic() {
+    cudaError_t e = preload_split_d<128>();
+    if (e == cudaSuccess) e = preload_split_d<64>();
+    return e;
 }
 
 cudaError_t launch_combine(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {

@@ -911,10 +911,14 @@ cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long rows,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+template <int WK, bool BF>
+constexpr size_t pers_smem_bytes() {
+    return sizeof(typename PersCfg<WK, BF>::Smem) + 1024;
+}
+
+// The dynamic shared-memory opt-in of one instantiation, set once per device.
 template <int G, bool MASS, int WK, bool BF>
-cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    using C = PersCfg<WK, BF>;
-    const size_t smem = sizeof(typename C::Smem) + 1024;
+cudaError_t configure_pers() {
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -922,10 +926,20 @@ cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(decode_split_pers_kernel<G, MASS, WK, BF>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pers_smem_bytes<WK, BF>());
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
+    return cudaSuccess;
+}
+
+template <int G, bool MASS, int WK, bool BF>
+cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    using C = PersCfg<WK, BF>;
+    const size_t smem = pers_smem_bytes<WK, BF>();
+    cudaError_t e = configure_pers<G, MASS, WK, BF>();
+    if (e != cudaSuccess) return e;
     const long long rows = (long long)a.num_pages * p.Hkv * kPage;
     alignas(64) CUtensorMap tmk, tmv;
     if ((e = pool_tensor_map(&tmk, a.k_pages, rows, BF)) != cudaSuccess) return e;
@@ -970,6 +984,31 @@ bool pers_supported(const DecodePlan &p, int num_pages) {
     return (p.dtype == PFKV_KV_FP8_E4M3 || p.dtype == PFKV_KV_BF16) && p.D == 128 && p.G <= 8 &&
            rows < (1LL << 31) &&
            K <= kPersMaxSegments && p.Breq <= kPersMaxRequests;
+}
+
+namespace {
+template <int G>
+cudaError_t preload_pers_g() {
+    cudaError_t e = cudaSuccess;
+    auto one = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+    one(configure_pers<G, false, 8, false>());
+    one(configure_pers<G, true, 8, false>());
+    one(configure_pers<G, false, 12, false>());
+    one(configure_pers<G, true, 12, false>());
+    one(configure_pers<G, false, 8, true>());
+    one(configure_pers<G, true, 8, true>());
+    one(configure_pers<G, false, 12, true>());
+    one(configure_pers<G, true, 12, true>());
+    return e;
+}
+}  // namespace
+
+cudaError_t preload_split_pers() {
+    cudaError_t e = preload_pers_g<1>();
+    if (e == cudaSuccess) e = preload_pers_g<2>();
+    if (e == cudaSuccess) e = preload_pers_g<4>();
+    if (e == cudaSuccess) e = preload_pers_g<8>();
+    return e;
 }
 
 cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {

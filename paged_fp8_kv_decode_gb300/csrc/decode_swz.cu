@@ -486,20 +486,27 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, long long rows) {
 }
 
 template <int G>
-cudaError_t launch_swz_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    using C = SwzCfg<G>;
-    const size_t smem = sizeof(typename C::Smem) + 1024;
+cudaError_t configure_swz() {
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(decode_split_swz_kernel<G>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(decode_split_swz_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(sizeof(typename SwzCfg<G>::Smem) + 1024));
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
+    return cudaSuccess;
+}
+
+template <int G>
+cudaError_t launch_swz_g(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    using C = SwzCfg<G>;
+    const size_t smem = sizeof(typename C::Smem) + 1024;
+    cudaError_t e = configure_swz<G>();
+    if (e != cudaSuccess) return e;
     CUtensorMap tk, tv;
     const long long rows = (long long)a.num_pages * p.Hkv * kPage;
     if (!encode_pool_map(&tk, a.k_pages, rows) || !encode_pool_map(&tv, a.v_pages, rows))
@@ -515,6 +522,13 @@ bool swz_supported(const DecodePlan &p, int num_pages) {
     // TMA row coordinates are 32-bit
     const long long rows = (long long)num_pages * p.Hkv * kPage;
     return p.dtype == PFKV_KV_FP8_E4M3 && p.D == 128 && p.G <= 4 && rows < (1LL << 31);
+}
+
+cudaError_t preload_split_swz() {
+    cudaError_t e = configure_swz<1>();
+    if (e == cudaSuccess) e = configure_swz<2>();
+    if (e == cudaSuccess) e = configure_swz<4>();
+    return e;
 }
 
 cudaError_t launch_split_swz(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {

@@ -47,4 +47,12 @@ cudaError_t launch_mass(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s
     return cudaErrorInvalidValue;
 }
 
+cudaError_t preload_mass() {
+    cudaError_t e = preload_kernel(attn_mass_kernel<1>);
+    if (e == cudaSuccess) e = preload_kernel(attn_mass_kernel<2>);
+    if (e == cudaSuccess) e = preload_kernel(attn_mass_kernel<4>);
+    if (e == cudaSuccess) e = preload_kernel(attn_mass_kernel<8>);
+    return e;
+}
+
 }  // namespace pfkv

@@ -213,6 +213,23 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodePlan &p, cudaStream_
 cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *out, cudaStream_t s);
 cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStream_t s);
 
+// Load every kernel of one source file onto the current device (and set the
+// shared-memory opt-ins its launches need), so that no later launch pays for
+// lazy module loading.  Called once per device, on its first use.
+cudaError_t preload_append();
+cudaError_t preload_split_pers();
+cudaError_t preload_combine_pers();
+cudaError_t preload_split_generic();
+cudaError_t preload_split_swz();
+cudaError_t preload_mass();
+
+// Loads one kernel (a no-op if it is loaded already).
+template <typename F>
+cudaError_t preload_kernel(F *kernel) {
+    cudaFuncAttributes attr;
+    return cudaFuncGetAttributes(&attr, kernel);
+}
+
 // --------------------------------------------------------------------------
 // device helpers
 // --------------------------------------------------------------------------
