@@ -55,7 +55,10 @@ typedef enum {
     PFKV_ERR_UNSUPPORTED = 2,  /* head_dim, group size, page size or device    */
     PFKV_ERR_ALIGNMENT = 3,    /* a pointer is not suitably aligned            */
     PFKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required   */
-    PFKV_ERR_CUDA = 5          /* a CUDA runtime call or launch failed         */
+    PFKV_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed         */
+    PFKV_ERR_DEVICE = 6        /* a device-side wait gave up: returned only by
+                                  pfkv_flags_status (no call synchronises the
+                                  host, so the call that met it cannot)       */
 } pfkv_status;
 
 typedef enum {
@@ -276,6 +279,24 @@ pfkv_status pfkv_decode_step(const pfkv_cache *cache, const pfkv_pages *pages,
                              uint32_t options, void *stream);
 
 /*
+ * pfkv_flags_status -- the library status that a finished call's per-request
+ * flags amount to.  `flags` is HOST memory: the `flags` array of an attention
+ * or decode-step call, copied back by the caller once that call's stream has
+ * completed.  Returns PFKV_ERR_DEVICE if any of the first `batch` requests
+ * carries PFKV_FLAG_DEVICE_TIMEOUT (a bounded device-side wait gave up, so
+ * that request's output is not valid and the device may be unhealthy), else
+ * PFKV_OK.  Tag, page and length flags describe the caller's data, not a
+ * failure of the library, and give PFKV_OK.  No call of this library
+ * synchronises the host, so none can return a device-side failure itself;
+ * the flags carry it, and this query turns it into a status.  Requests
+ * aborted by a mismatching tag are the pages' "aborted request" ("Cloudflare
+ * quantizes Kimi and GLM caches ...", 4th paragraph); a timeout is this
+ * library's own failure and is reported apart from them.  flags NULL with
+ * batch > 0, or batch < 0: PFKV_ERR_INVALID_ARG.  Makes no CUDA call.
+ */
+pfkv_status pfkv_flags_status(const uint8_t *flags, int32_t batch);
+
+/*
  * pfkv_paged_decode_attn_noalloc -- pfkv_paged_decode_attn without a
  * caller-provided workspace.  (The source pages have no counterpart to this
  * call; it exists for callers, not for the method.)
@@ -292,9 +313,12 @@ pfkv_status pfkv_decode_step(const pfkv_cache *cache, const pfkv_pages *pages,
  *  - a call that would need more than PFKV_NOALLOC_WORKSPACE_BYTES of
  *    workspace (pfkv_decode_workspace_size) returns PFKV_ERR_WORKSPACE and
  *    enqueues nothing;
- *  - the first call with a given device current looks up the array's device
- *    address (cudaGetSymbolAddress) for that device; make that first call
- *    before capturing the stream into a CUDA graph;
+ *  - the first call with a given device (and CUDA context) current looks up
+ *    the array's device address (cudaGetSymbolAddress) for it, and so does
+ *    the first call after another context becomes current on that device
+ *    (a plugin host's own context, or the primary context after a
+ *    cudaDeviceReset); make that first call before capturing the stream into
+ *    a CUDA graph;
  *  - all calls share the one array, which keeps the previous call's contents
  *    (this is harmless: the workspace's contents on entry are ignored).  Two
  *    calls whose work overlaps on the GPU (different streams, or different

@@ -24,6 +24,7 @@ PFKV_ERR_UNSUPPORTED = 2
 PFKV_ERR_ALIGNMENT = 3
 PFKV_ERR_WORKSPACE = 4
 PFKV_ERR_CUDA = 5
+PFKV_ERR_DEVICE = 6
 
 PFKV_KV_BF16 = 0
 PFKV_KV_FP8_E4M3 = 1
@@ -48,7 +49,7 @@ EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_a
             "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
             "pfkv_decode_multi_workspace_size", "pfkv_step_graph_create", "pfkv_step_graph_launch",
             "pfkv_step_graph_destroy", "pfkv_selftest_bounded_wait", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string",
-            "pfkv_abi_version")
+            "pfkv_abi_version", "pfkv_flags_status")
 
 
 class PfkvError(RuntimeError):
@@ -152,6 +153,8 @@ def lib() -> ctypes.CDLL:
         L.pfkv_status_string.restype = ctypes.c_char_p
         L.pfkv_abi_version.argtypes = []
         L.pfkv_abi_version.restype = ctypes.c_int32
+        L.pfkv_flags_status.argtypes = [P, I32]
+        L.pfkv_flags_status.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -162,6 +165,17 @@ def pfkv_status_string(status: int) -> str:
 
 def pfkv_abi_version() -> int:
     return int(lib().pfkv_abi_version())
+
+
+def pfkv_flags_status(flags) -> int:
+    """Status that a finished call's flags amount to (see include/pfkv.h):
+    PFKV_ERR_DEVICE if a request carries PFKV_FLAG_DEVICE_TIMEOUT, else
+    PFKV_OK.  ``flags``: host uint8 array or a tensor (copied to the host)."""
+    import numpy as np
+    if isinstance(flags, torch.Tensor):
+        flags = flags.detach().to("cpu").numpy()
+    a = np.ascontiguousarray(flags, dtype=np.uint8)
+    return int(lib().pfkv_flags_status(a.ctypes.data if a.size else None, int(a.size)))
 
 
 # --------------------------------------------------------------------------

@@ -241,11 +241,19 @@ const char *pfkv_status_string(pfkv_status s) {
         case PFKV_ERR_ALIGNMENT: return "misaligned pointer";
         case PFKV_ERR_WORKSPACE: return "workspace missing or too small";
         case PFKV_ERR_CUDA: return "CUDA error";
+        case PFKV_ERR_DEVICE: return "a device-side wait gave up";
     }
     return "unknown status";
 }
 
 int32_t pfkv_abi_version(void) { return PFKV_ABI_VERSION; }
+
+pfkv_status pfkv_flags_status(const uint8_t *flags, int32_t batch) {
+    if (batch < 0 || (batch > 0 && !flags)) return PFKV_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < batch; ++b)
+        if (flags[b] & PFKV_FLAG_DEVICE_TIMEOUT) return PFKV_ERR_DEVICE;
+    return PFKV_OK;
+}
 
 pfkv_status pfkv_kv_append(const pfkv_cache *cache, const pfkv_pages *pages,
                            const int32_t *positions, const int32_t *new_lens,

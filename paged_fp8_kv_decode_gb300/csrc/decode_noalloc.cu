@@ -8,7 +8,10 @@
 // the device.  For them the workspace lives in a fixed-size array in the
 // library's own device memory, reserved when the library is loaded onto a GPU
 // and kept until the process exits.
-#include <atomic>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "pfkv_internal.cuh"
 
@@ -19,10 +22,46 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_workspace[PFKV_NOALLOC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void *> g_workspace_addr[kMaxDevices];
 
-// Device address of the array on the current device, looked up on the first
-// call made with that device current.
+// The address of the array in the context that was current when it was
+// looked up, keyed by the context's unique id.  A module is loaded once per
+// context, so another context on the same device (a plugin host's own, or the
+// primary context re-created after cudaDeviceReset) holds the array at
+// another address; a new context never reuses an id, where it may reuse a
+// handle.
+struct Cached {
+    unsigned long long ctx_id;
+    void *addr;
+};
+std::mutex g_mutex;
+Cached g_cached[kMaxDevices];
+
+// Driver entry points through the runtime (no link against the driver
+// library).
+template <typename Fn>
+Fn driver_fn(const char *name, int version) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the current context; 0 if none is current.
+bool current_context_id(unsigned long long *id) {
+    static const PFN_cuCtxGetCurrent_v4000 get_ctx =
+        driver_fn<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent", 4000);
+    static const PFN_cuCtxGetId_v12000 get_id = driver_fn<PFN_cuCtxGetId_v12000>("cuCtxGetId", 12000);
+    CUcontext ctx = nullptr;
+    if (!get_ctx || !get_id || get_ctx(&ctx) != CUDA_SUCCESS) return false;
+    *id = 0;
+    return ctx == nullptr || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current context, looked up on the first
+// call made with that context current (cudaGetSymbolAddress, which also makes
+// the runtime's context current if none is).
 pfkv_status workspace_address(void **addr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -30,15 +69,22 @@ pfkv_status workspace_address(void **addr) {
         return PFKV_ERR_CUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return PFKV_ERR_UNSUPPORTED;
-    void *p = g_workspace_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return PFKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Cached &c = g_cached[dev];
+    if (id == 0 || c.ctx_id != id || c.addr == nullptr) {
+        void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) {
             cudaGetLastError();
             return PFKV_ERR_CUDA;
         }
-        g_workspace_addr[dev].store(p, std::memory_order_release);
+        // the lookup made the runtime's context current if none was
+        if (!current_context_id(&id) || id == 0) return PFKV_ERR_CUDA;
+        c.ctx_id = id;
+        c.addr = p;
     }
-    *addr = p;
+    *addr = c.addr;
     return PFKV_OK;
 }
 

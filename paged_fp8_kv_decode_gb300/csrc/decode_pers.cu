@@ -31,11 +31,13 @@
 //    by a power of two so that its largest element lies in [1, 2);
 //  * runs the online softmax on the accumulator fragment (lane (g, t) holds
 //    tokens g and g + 8 of heads 2t and 2t + 1), with a lazy rescale;
-//  * accumulates O^T = V^T P^T as eight MMAs: the 128 dims are the M rows (in
-//    eight tiles), tokens the reduction, heads the columns.  A byte permute
-//    pairs two tokens of one dim, the conversion makes the A fragment, and the
-//    probabilities, times the unit's V scale over a power-of-two reference,
-//    become f16 B fragments through four shuffles.
+//  * accumulates O^T = V^T P^T as sixteen MMAs: the 128 dims are the M rows
+//    (in eight tiles), tokens the reduction, heads the columns.  A byte
+//    permute pairs two tokens of one dim, the conversion makes the A
+//    fragment, and the probabilities, times the unit's V scale over a
+//    power-of-two reference, become f16 B fragments through shuffles: each
+//    as a hi + lo pair (two MMAs per tile), so that a weight carries 22 bits
+//    of its fp32 value rather than f16's 11.
 // The dims of the score reduction are taken in a permuted order (lane t owns
 // dims [32t, 32t + 32) of both K and Q), which changes nothing in the sum.
 #include <atomic>
@@ -112,6 +114,24 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Two fp32 values as a sum of two f16 pairs: hi = f16(x), lo = f16(x - hi).
+// hi + lo is within 2^-22 |x| (plus 2^-25 absolute, the f16 subnormal step)
+// of x, where hi alone is within 2^-11 |x|.
+__device__ __forceinline__ void split_half2(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 f = __half22float2(h);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = pack_half2(x - f.x, y - f.y);
+}
+
+// The same with bf16 pairs: hi + lo within 2^-18 |x| (hi alone: 2^-9 |x|).
+__device__ __forceinline__ void split_bf162(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 f = __bfloat1622float2(h);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = pack_bf162(x - f.x, y - f.y);
 }
 
 // 2^e as fp32 for e in [-126, 127]
@@ -733,18 +753,33 @@ __global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
                 lB += pB0 + pB1;
                 if (!FULL && nv[u] == 0) continue;  // uniform: nothing of this unit is live
                 const float vs = um[u].vs * vref;
-                // X0: head A at tokens (fg, fg + 8); X1: head B (BF16: bf16
-                // probabilities, no V scale)
-                const uint32_t X0 = BF ? pack_bf162(pA0, pA1) : pack_half2(pA0 * vs, pA1 * vs);
-                const uint32_t X1 = BF ? pack_bf162(pB0, pB1) : pack_half2(pB0 * vs, pB1 * vs);
+                // X0: head A at tokens (fg, fg + 8); X1: head B.  Each weight
+                // (times the unit's V scale over the reference; BF16: no V
+                // scale) enters the MMA as a hi + lo pair of 16-bit values
+                // (L0, L1: the lo parts): a single 16-bit weight would err by
+                // 2^-11 (bf16: 2^-9) of w |v|, which near-cancelling large
+                // values turn into errors above the output's tolerance.
+                uint32_t X0, X1, L0, L1;
+                if constexpr (BF) {
+                    split_bf162(pA0, pA1, X0, L0);
+                    split_bf162(pB0, pB1, X1, L1);
+                } else {
+                    split_half2(pA0 * vs, pA1 * vs, X0, L0);
+                    split_half2(pB0 * vs, pB1 * vs, X1, L1);
+                }
+                // head fg: Y0 = tokens (a, a + 8), Y1 = (b, b + 8) with (a, b) =
+                // (2 ft, 2 ft + 1) for FP8 and (ft, ft + 4) for BF16 (both
+                // heads of the source lane travel; this lane keeps its own)
                 const uint32_t s00 = __shfl_sync(0xffffffffu, X0, src0), s01 = __shfl_sync(0xffffffffu, X1, src0);
                 const uint32_t s10 = __shfl_sync(0xffffffffu, X0, src1), s11 = __shfl_sync(0xffffffffu, X1, src1);
-                // head fg: Y0 = tokens (a, a + 8), Y1 = (b, b + 8) with (a, b) =
-                // (2 ft, 2 ft + 1) for FP8 and (ft, ft + 4) for BF16
-                const uint32_t Y0 = odd_head ? s01 : s00;
-                const uint32_t Y1 = odd_head ? s11 : s10;
+                const uint32_t l00 = __shfl_sync(0xffffffffu, L0, src0), l01 = __shfl_sync(0xffffffffu, L1, src0);
+                const uint32_t l10 = __shfl_sync(0xffffffffu, L0, src1), l11 = __shfl_sync(0xffffffffu, L1, src1);
+                const uint32_t Y0 = odd_head ? s01 : s00, Y1 = odd_head ? s11 : s10;
+                const uint32_t Z0 = odd_head ? l01 : l00, Z1 = odd_head ? l11 : l10;
                 const uint32_t pb0 = __byte_perm(Y0, Y1, 0x5410);  // tokens a, b
                 const uint32_t pb1 = __byte_perm(Y0, Y1, 0x7632);  // tokens a + 8, b + 8
+                const uint32_t pl0 = __byte_perm(Z0, Z1, 0x5410);
+                const uint32_t pl1 = __byte_perm(Z0, Z1, 0x7632);
 
                 const uint8_t *vb = stage + (C::GU + u) * C::UNITB;
                 if constexpr (BF) {
@@ -768,12 +803,16 @@ __global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
                         // dims (2q, 2q + 1) of chunk A -> tile q; of chunk B -> tile 4 + q
                         uint32_t w0 = word_of(ra[0], q), w1 = word_of(ra[1], q);
                         uint32_t w2 = word_of(ra[2], q), w3 = word_of(ra[3], q);
-                        mma_16816_bf16(o[q], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
-                                       __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+                        uint32_t a0 = __byte_perm(w0, w1, 0x5410), a1 = __byte_perm(w0, w1, 0x7632);
+                        uint32_t a2 = __byte_perm(w2, w3, 0x5410), a3 = __byte_perm(w2, w3, 0x7632);
+                        mma_16816_bf16(o[q], a0, a1, a2, a3, pb0, pb1);
+                        mma_16816_bf16(o[q], a0, a1, a2, a3, pl0, pl1);
                         w0 = word_of(rb[0], q), w1 = word_of(rb[1], q);
                         w2 = word_of(rb[2], q), w3 = word_of(rb[3], q);
-                        mma_16816_bf16(o[4 + q], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
-                                       __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+                        a0 = __byte_perm(w0, w1, 0x5410), a1 = __byte_perm(w0, w1, 0x7632);
+                        a2 = __byte_perm(w2, w3, 0x5410), a3 = __byte_perm(w2, w3, 0x7632);
+                        mma_16816_bf16(o[4 + q], a0, a1, a2, a3, pb0, pb1);
+                        mma_16816_bf16(o[4 + q], a0, a1, a2, a3, pl0, pl1);
                     }
                     continue;
                 }
@@ -796,9 +835,11 @@ __global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
                     e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x5140), a0, a1);  // dims 4wd, 4wd+1
                     e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x5140), a2, a3);
                     mma_16816(o[2 * wd], a0, a1, a2, a3, pb0, pb1);
+                    mma_16816(o[2 * wd], a0, a1, a2, a3, pl0, pl1);
                     e4m3x4_to_f16x2(__byte_perm(w0, w1, 0x7362), a0, a1);  // dims 4wd+2, 4wd+3
                     e4m3x4_to_f16x2(__byte_perm(w2, w3, 0x7362), a2, a3);
                     mma_16816(o[2 * wd + 1], a0, a1, a2, a3, pb0, pb1);
+                    mma_16816(o[2 * wd + 1], a0, a1, a2, a3, pl0, pl1);
                 }
             }
         };

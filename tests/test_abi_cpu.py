@@ -36,7 +36,8 @@ def test_header_declares_the_entry_points():
                             "pfkv_decode_multi_workspace_size",
                             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
                             "pfkv_status_string", "pfkv_selftest_bounded_wait", "pfkv_step_graph_create",
-                            "pfkv_step_graph_destroy", "pfkv_step_graph_launch"])
+                            "pfkv_step_graph_destroy", "pfkv_step_graph_launch",
+                            "pfkv_flags_status"])
 
 
 def test_library_exports_every_declared_symbol(B):
@@ -53,7 +54,7 @@ def test_library_exports_every_declared_symbol(B):
 
 def test_status_strings_and_version(B):
     assert B.pfkv_abi_version() == 1
-    for code in range(6):
+    for code in range(7):
         assert isinstance(B.pfkv_status_string(code), str)
     assert B.pfkv_status_string(0) == "ok"
     assert B.pfkv_status_string(99) == "unknown status"
@@ -244,3 +245,50 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "libpfkv.so"))
     with pytest.raises(RuntimeError, match="missing"):
         binding.lib()
+
+
+def _header_enum(name):
+    m = re.search(r"\b" + name + r"\s*=\s*(\d+)", open(HEADER).read())
+    return int(m.group(1))
+
+
+def _header_macro(name):
+    m = re.search(r"#define\s+" + name + r"\s+\(?(\w+)u?\s*(<<\s*(\d+))?\)?", open(HEADER).read())
+    v = int(m.group(1).rstrip("u"), 0)
+    return v << int(m.group(3)) if m.group(3) else v
+
+
+def test_binding_constants_match_the_header(B):
+    """The binding's copies of the header's numbers, read from the header."""
+    for name in ("PFKV_OK", "PFKV_ERR_INVALID_ARG", "PFKV_ERR_UNSUPPORTED", "PFKV_ERR_ALIGNMENT",
+                 "PFKV_ERR_WORKSPACE", "PFKV_ERR_CUDA", "PFKV_ERR_DEVICE", "PFKV_KV_BF16",
+                 "PFKV_KV_FP8_E4M3"):
+        assert getattr(B, name) == _header_enum(name), name
+    for name in ("PFKV_PAGE_SIZE", "PFKV_FLAG_TAG_MISMATCH", "PFKV_FLAG_BAD_PAGE",
+                 "PFKV_FLAG_BAD_LENGTH", "PFKV_FLAG_DEVICE_TIMEOUT", "PFKV_STAGE_VALIDATE",
+                 "PFKV_STAGE_SPLIT", "PFKV_STAGE_COMBINE", "PFKV_STAGE_ALL", "PFKV_STAGE_FUSED_TAGS",
+                 "PFKV_NOALLOC_WORKSPACE_BYTES"):
+        assert getattr(B, name) == _header_macro(name), name
+    assert B.PFKV_NOALLOC_WORKSPACE_BYTES == 16 << 20
+
+
+def test_flags_status_turns_device_timeouts_into_a_status(B):
+    """Only PFKV_FLAG_DEVICE_TIMEOUT makes a status; data flags do not."""
+    import numpy as np
+    assert B.pfkv_flags_status(np.zeros(5, np.uint8)) == B.PFKV_OK
+    data = np.array([B.PFKV_FLAG_TAG_MISMATCH, B.PFKV_FLAG_BAD_PAGE, B.PFKV_FLAG_BAD_LENGTH,
+                     B.PFKV_FLAG_TAG_MISMATCH | B.PFKV_FLAG_BAD_LENGTH], np.uint8)
+    assert B.pfkv_flags_status(data) == B.PFKV_OK
+    for pos in range(4):
+        f = data.copy()
+        f[pos] |= B.PFKV_FLAG_DEVICE_TIMEOUT
+        assert B.pfkv_flags_status(f) == B.PFKV_ERR_DEVICE
+    assert B.pfkv_flags_status(np.zeros(0, np.uint8)) == B.PFKV_OK
+    L = B.lib()
+    assert L.pfkv_flags_status(None, 3) == B.PFKV_ERR_INVALID_ARG
+    buf = np.zeros(4, np.uint8)
+    assert L.pfkv_flags_status(buf.ctypes.data, -1) == B.PFKV_ERR_INVALID_ARG
+    # only the first `batch` requests count
+    buf[3] = B.PFKV_FLAG_DEVICE_TIMEOUT
+    assert L.pfkv_flags_status(buf.ctypes.data, 3) == B.PFKV_OK
+    assert L.pfkv_flags_status(buf.ctypes.data, 4) == B.PFKV_ERR_DEVICE

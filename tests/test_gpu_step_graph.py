@@ -1,14 +1,17 @@
 """Step graphs: a decode step of several layers captured once and replayed
 must give, layer by layer, exactly the bytes of the direct calls (same
 kernels, same arguments), and must read the buffers' current contents on
-every replay (new queries, new tokens, longer lengths)."""
+every replay (new queries, new tokens, longer lengths).  Every replay is also
+checked against the oracle stepping the same layers: pool bytes, scales and
+flags bit for bit, outputs within the contract tolerance."""
 import dataclasses
 
 import numpy as np
 import pytest
 import torch
 
-from oracle_cases import host_pool
+import oracle
+from oracle_cases import assert_outputs_close, cache_dict, fill_pool, host_pool, pages_dict
 from paged_fp8_kv_decode_gb300 import workloads as W
 from test_gpu_parity import B  # noqa: F401  (fixture)
 
@@ -22,7 +25,7 @@ def _layers(spec, batch, n, max_seq_len):
     for l in range(n):
         sl = dataclasses.replace(spec, seed=spec.seed + 100 * (l + 1))
         rows = (W.draw_kv_rows(sl, T, "k", device="cuda"), W.draw_kv_rows(sl, T, "v", device="cuda"))
-        db = DeviceBatch(batch, rows=rows, q=W.draw_q(sl, device="cuda"))
+        db = DeviceBatch(batch, rows=rows, q=W.draw_q(sl, device="cuda"), keep_rows=True)
         if spec.append:
             db.k_new.copy_(W.draw_new_token(sl, "k", device="cuda"))
             db.v_new.copy_(W.draw_new_token(sl, "v", device="cuda"))
@@ -52,6 +55,49 @@ def _same(a, b, label):
     assert torch.equal(want, b[0].append_flags), label
 
 
+class OracleLayers:
+    """The oracle's copy of every layer's pool, stepped like the GPU's: the
+    fill from the layer's rows, then per step the append of that step's new
+    token (kv_append with the tags checked) and the attention."""
+
+    def __init__(self, spec, batch, dbs):
+        self.spec, self.batch = spec, batch
+        self.pools = []
+        for d in dbs:
+            k, v, ks, vs = fill_pool(spec, batch, W.bf16_bits(d.k_rows), W.bf16_bits(d.v_rows))
+            self.pools.append((k, v, ks, vs))
+        self.aflags = np.zeros(spec.B, np.uint8)  # OR over layers and steps
+
+    def step(self, dbs, step, max_len):
+        """Returns per layer (out, flags) of decode step `step` (positions and
+        lengths grown by `step` tokens)."""
+        spec, batch = self.spec, self.batch
+        res = []
+        for d, (k, v, ks, vs) in zip(dbs, self.pools):
+            cache = cache_dict(spec, batch, k, v, ks, vs)
+            pages = pages_dict(spec, batch, batch.seq_lens + step)
+            if spec.append:
+                fl = np.zeros(spec.B, np.uint8)
+                oracle.kv_append(cache, pages, batch.positions + step, W.bf16_bits(d.k_new),
+                                 W.bf16_bits(d.v_new), flags=fl)
+                self.aflags |= fl
+            res.append(oracle.paged_decode(cache, pages, W.bf16_bits(d.q), spec.Hq, spec.sm_scale,
+                                           max_len))
+        return res
+
+    def compare(self, dbs, res, label):
+        for l, (d, (k, v, ks, vs), (out, flags)) in enumerate(zip(dbs, self.pools, res)):
+            lab = f"{label} layer {l}"
+            assert np.array_equal(host_pool(d.cache.k_pages), k), lab
+            assert np.array_equal(host_pool(d.cache.v_pages), v), lab
+            if ks is not None:
+                assert np.array_equal(d.cache.k_scale.cpu().numpy(), ks), lab
+                assert np.array_equal(d.cache.v_scale.cpu().numpy(), vs), lab
+            assert np.array_equal(d.flags.cpu().numpy()[:self.spec.B], flags), lab
+            assert_outputs_close(d.out, out, lab)
+        assert np.array_equal(dbs[0].append_flags.cpu().numpy()[:self.spec.B], self.aflags), label
+
+
 @pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("which", ["llama8b", "evict", "bf16"])
 def test_graph_replays_equal_direct_calls(B, which, fused):
@@ -78,6 +124,7 @@ def test_graph_replays_equal_direct_calls(B, which, fused):
                                      max_len, ws, B.PFKV_STAGE_FUSED_TAGS if fused else 0)
     for d in direct:
         d.fused_tags = fused
+    ref = OracleLayers(spec, batch, graphed)
     try:
         for step in range(3):
             if step:
@@ -97,6 +144,7 @@ def test_graph_replays_equal_direct_calls(B, which, fused):
             graph.launch()
             torch.cuda.synchronize()
             _same(direct, graphed, f"{which} fused={fused} step {step}")
+            ref.compare(graphed, ref.step(graphed, step, max_len), f"{which} fused={fused} step {step}")
             assert not graphed[0].flags[:spec.B].any() or spec.tags
     finally:
         graph.close()
