@@ -475,27 +475,32 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
-def e2e_step_graph(db, B, fused_tags):
+class E2EStepGraph:
     """One end-to-end step as a CUDA graph: the host-to-device copy of the
     step's packed inputs from pinned memory, the public pfkv_decode_step call
     (or the attention call where the workload does not append), and the
-    device-to-host copy of the packed output (out and flags).  Returns the
-    graph and its pinned host buffers."""
-    import torch
-    s = torch.cuda.Stream()
-    h_in = db.io_in.detach().cpu().pin_memory()
-    h_out = torch.empty_like(db.io_out, device="cpu").pin_memory()
-    step = PreparedStep(db, B, s.cuda_stream, fused_tags=fused_tags)
-    with torch.cuda.stream(s):  # warm the call on the capture stream
-        step.full_step()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        db.io_in.copy_(h_in, non_blocking=True)
-        step.full_step()
-        h_out.copy_(db.io_out, non_blocking=True)
-    torch.cuda.synchronize()
-    return g, h_in, h_out
+    device-to-host copy of the packed output (out and flags).  The object owns
+    the pinned host buffers the graph's copies read and write: they must live
+    as long as the graph is replayed."""
+
+    def __init__(self, db, B, fused_tags):
+        import torch
+        s = torch.cuda.Stream()
+        self.h_in = db.io_in.detach().cpu().pin_memory()
+        self.h_out = torch.empty_like(db.io_out, device="cpu").pin_memory()
+        step = PreparedStep(db, B, s.cuda_stream, fused_tags=fused_tags)
+        with torch.cuda.stream(s):  # warm the call on the capture stream
+            step.full_step()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s):
+            db.io_in.copy_(self.h_in, non_blocking=True)
+            step.full_step()
+            self.h_out.copy_(db.io_out, non_blocking=True)
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
 
 
 def e2e_bytes(db):
@@ -520,7 +525,7 @@ def run_e2e(args, reps, B, stream, step_bytes, world, dev):
     them before the next step."""
     import torch
     K = max(1, min(args.e2e_steps, args.steps))
-    graphs = [e2e_step_graph(p.db, B, args.fused_tags)[0] for p in reps]
+    graphs = [E2EStepGraph(p.db, B, args.fused_tags) for p in reps]
     h2d, d2h = e2e_bytes(reps[0].db)
     for i in range(5):
         graphs[i % len(reps)].replay()
@@ -872,7 +877,7 @@ def run_e2e_flushed(args, p, B, stream, step_bytes, world, dev, flush):
     each step outside the host-timed interval."""
     import torch
     K = max(1, min(args.e2e_steps, args.steps))
-    g, _, _ = e2e_step_graph(p.db, B, bool(p.opt))
+    g = E2EStepGraph(p.db, B, bool(p.opt))
     h2d, d2h = e2e_bytes(p.db)
     total = 0.0
     for i in range(K + 2):
