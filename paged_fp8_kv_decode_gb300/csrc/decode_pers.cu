@@ -360,22 +360,63 @@ __global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
     float cks, cvs, nks, nvs;
     uint32_t cbad, nbad;
     // req: the unit's request (-1 for no unit), for skip_rejected()
-    auto load_ids = [&](int bx, int &phys, uint32_t &bad, int &req) {
-        const int x = bx + lane;
-        phys = -2;
-        bad = 0;
-        req = -1;
-        if (x < x1) {
+    // A window entry: its table entry and page id (with the expected tag for
+    // the fused check), loaded before any is used, then its status bits (one
+    // more round for the pool's tag of the id when the check is fused).
+    struct Entry {
+        long long bi;
+        int h, req, id;
+        uint32_t want;
+        bool live;
+    };
+    auto entry_load = [&](int x, Entry &e) {
+        e.live = x < x1;
+        e.bi = 0;
+        e.h = 0;
+        e.req = -1;
+        e.id = 0;
+        e.want = 0u;
+        if (e.live) {
             const int k = seg_of(sm.prefix, K, x);
             const int bh = k / nchunks, c = k - bh * nchunks;
             const int b = bh / Hkv, h = bh - b * Hkv;
             const int page = c * (chunk_tokens / kPage) + (int)(x - sm.prefix[k]);
-            const long long bi = table_row(a, b, h) + page;
-            const int id = a.block_tables[bi];
-            bad = entry_bits(a, id, h, Hkv, bi);
-            phys = bad ? -1 : id * Hkv + h;  // unit index
-            req = b / a.kq;
+            e.bi = table_row(a, b, h) + page;
+            e.h = h;
+            e.req = b / a.kq;
+            e.id = a.block_tables[e.bi];
+            if (a.fuse_tags) e.want = a.expected_tags[e.bi];
         }
+    };
+    auto entry_tag = [&](const Entry &e) -> uint32_t {
+        const bool in_pool = e.id >= 0 && e.id < a.num_pages;
+        return e.live && a.fuse_tags && in_pool ? a.page_tags[(long long)e.id * Hkv + e.h] : 0u;
+    };
+    // the same bits as entry_bits, from the loaded values
+    auto entry_finish = [&](const Entry &e, uint32_t tag, int &phys, uint32_t &bad, int &req) {
+        phys = -2;
+        bad = 0;
+        req = -1;
+        if (!e.live) return;
+        if (e.id < 0 || e.id >= a.num_pages) bad = PFKV_FLAG_BAD_PAGE;
+        else if (a.fuse_tags && tag != e.want) bad = PFKV_FLAG_TAG_MISMATCH;
+        phys = bad ? -1 : e.id * Hkv + e.h;  // unit index
+        req = e.req;
+    };
+    auto load_ids = [&](int bx, int &phys, uint32_t &bad, int &req) {
+        Entry e;
+        entry_load(bx + lane, e);
+        entry_finish(e, entry_tag(e), phys, bad, req);
+    };
+    // both halves of a window, every load of a round issued before any is used
+    auto load_ids2 = [&](int bx, int &phys0, uint32_t &bad0, int &req0, int &phys1, uint32_t &bad1,
+                         int &req1) {
+        Entry e0, e1;
+        entry_load(bx + lane, e0);
+        entry_load(bx + 32 + lane, e1);
+        const uint32_t t0 = entry_tag(e0), t1 = entry_tag(e1);
+        entry_finish(e0, t0, phys0, bad0, req0);
+        entry_finish(e1, t1, phys1, bad1, req1);
     };
     // units of a request the validation kernel rejected are absent
     auto skip_rejected = [&](int req, int &phys, uint32_t &bad) {
@@ -394,10 +435,7 @@ __global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
         }
     };
     int creq = -1, nreq = -1;
-    if (!idle) {
-        load_ids(base, cphys, cbad, creq);
-        load_ids(base + 32, nphys, nbad, nreq);
-    }
+    if (!idle) load_ids2(base, cphys, cbad, creq, nphys, nbad, nreq);
     // metadata of unit x (in [base, base + 64)).  One uniform branch picks
     // the window half (a select would wait for the next half's loads even
     // when only the current one is read).
