@@ -44,7 +44,6 @@ pfkv_status device_check(int *num_sms) {
             if (e == cudaSuccess) e = preload_split_pers();
             if (e == cudaSuccess) e = preload_combine_pers();
             if (e == cudaSuccess) e = preload_split_generic();
-            if (e == cudaSuccess) e = preload_split_swz();
             if (e == cudaSuccess) e = preload_mass();
             if (e != cudaSuccess) {
                 cudaGetLastError();
@@ -177,27 +176,42 @@ pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_he
     q.D = c->head_dim;
     q.dtype = c->dtype;
     q.tags = c->page_tags != nullptr;
-    // persistent balanced path: one segment per (request, kv head) unless the
-    // caller fixes the split size
-    q.kind = 1;
-    q.chunk_tokens = split_tokens > 0 ? split_tokens
-                                      : (max_seq_len > 0 ? (max_seq_len + kPage - 1) / kPage * kPage
-                                                         : kPage);
-    q.nchunks = max_seq_len > 0 ? (max_seq_len + q.chunk_tokens - 1) / q.chunk_tokens : 1;
-    q.pers_ctas = num_sms;
-    // every (virtual request, kv head) at max_seq_len: an upper bound on the units
-    const long long units_bound =
-        (long long)q.B * q.Hkv * (max_seq_len > 0 ? (max_seq_len + kPage - 1) / kPage : 1);
-    q.workers = num_sms * pers_workers_for(units_bound, num_sms);
-    if (!pers_supported(q, c->num_pages)) {
-        q.kind = 0;
+    // Persistent balanced path (head_dim 128): one segment per (request, kv
+    // head) unless the caller fixes the split size.  Only the output is
+    // contracted, not the split: the split size is coarsened (a multiple of
+    // the caller's) when a launch's segments would not fit the kernels'
+    // tables, and a batch whose (request, kv head) pairs alone would not fit
+    // runs as several launches of whole requests.
+    q.kind = pers_supported(q) && (long long)kq * q.Hkv <= kPersMaxSegments ? 1 : 0;
+    if (q.kind == 1) {
+        q.greq = (int)min((long long)q.Breq,
+                          min((long long)kPersMaxRequests, (long long)(kPersMaxSegments / (kq * q.Hkv))));
+        q.greq = max(q.greq, 1);
+        q.ngroups = (q.Breq + q.greq - 1) / q.greq;
+        const long long pages = max_seq_len > 0 ? (max_seq_len + kPage - 1) / kPage : 1;
+        long long chunk_pages = split_tokens > 0 ? split_tokens / kPage : pages;
+        const long long max_chunks = kPersMaxSegments / ((long long)q.greq * kq * q.Hkv);
+        if ((pages + chunk_pages - 1) / chunk_pages > max_chunks)
+            chunk_pages = (pages + max_chunks - 1) / max_chunks;
+        if (chunk_pages > 0x7fffffffLL / kPage) return PFKV_ERR_UNSUPPORTED;
+        q.chunk_tokens = (int)(chunk_pages * kPage);
+        q.nchunks = (int)((pages + chunk_pages - 1) / chunk_pages);
+        q.pers_ctas = num_sms;
+        // every (virtual request, kv head) at max_seq_len: an upper bound on the units
+        const long long units_bound = (long long)q.B * q.Hkv * pages;
+        q.workers = num_sms * pers_workers_for(units_bound, num_sms);
+    } else {
+        q.greq = q.Breq;
+        q.ngroups = 1;
         q.chunk_tokens = split_tokens > 0 ? split_tokens
                                           : auto_chunk_tokens(q.B, q.Hkv, max_seq_len, num_sms);
         q.nchunks = max_seq_len > 0 ? (max_seq_len + q.chunk_tokens - 1) / q.chunk_tokens : 1;
         q.pers_ctas = q.workers = 0;
     }
     q.htiles = max(1, (p->max_pages + kValTile - 1) / kValTile);
-    const long long items = (long long)q.B * q.Hkv * q.nchunks;
+    // segments of one launch (one request group for the persistent kind)
+    const long long Bl = q.kind == 1 ? (long long)min(q.greq, q.Breq) * kq : q.B;
+    const long long items = Bl * q.Hkv * q.nchunks;
     if (items > 0x7fffffffLL || (long long)q.B * q.Hq > 0x7fffffffLL) return PFKV_ERR_UNSUPPORTED;
     // rows of partial results: one per (b, hq, chunk), or segment + worker
     const size_t rows_kv = q.kind == 1 ? (size_t)items + q.workers : (size_t)items;
@@ -294,6 +308,24 @@ pfkv_status pfkv_decode_workspace_size(const pfkv_cache *cache, const pfkv_pages
 
 namespace {
 
+// The arguments of the request group starting at request r0: every
+// per-request pointer moved to the group's first request.
+DecodeArgs group_args(const DecodeArgs &a, const DecodePlan &p, int r0) {
+    DecodeArgs g = a;
+    const long long v0 = (long long)r0 * p.kq;  // first virtual request
+    g.q = a.q + v0 * p.Hq * p.D;
+    g.out = a.out + v0 * p.Hq * p.D;
+    if (a.flags) g.flags = a.flags + r0;
+    g.block_tables = a.block_tables + (long long)r0 * a.bt_sb;
+    g.seq_lens = a.seq_lens + (long long)r0 * a.len_sb;
+    if (a.expected_tags) g.expected_tags = a.expected_tags + (long long)r0 * a.bt_sb;
+    if (a.hflags) g.hflags = a.hflags + (long long)r0 * p.Hkv * p.htiles;
+    if (a.mscore) g.mscore = a.mscore + v0 * p.Hkv * (long long)a.mlen * p.G;
+    if (a.lse_fin) g.lse_fin = a.lse_fin + v0 * p.Hq;
+    if (a.rflags) g.rflags = a.rflags + r0;
+    return g;
+}
+
 struct MassOut {
     float *mass;
     int64_t sb, sh;
@@ -382,9 +414,32 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
         if (app && launch_kv_append(*app, pages->batch, s) != cudaSuccess) return PFKV_ERR_CUDA;
         if (validate && launch_validate(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     }
-    if ((stages & PFKV_STAGE_SPLIT) && launch_split(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
-    if ((stages & PFKV_STAGE_COMBINE) && launch_combine(a, plan, s) != cudaSuccess)
-        return PFKV_ERR_CUDA;
+    if (plan.ngroups > 1) {
+        // Request groups, each split then combine on its own slice of the
+        // batch: the workspace rows are reused from group to group, so the two
+        // stages run in the same call.
+        if (((stages & PFKV_STAGE_SPLIT) != 0) != ((stages & PFKV_STAGE_COMBINE) != 0))
+            return PFKV_ERR_UNSUPPORTED;
+        if (stages & PFKV_STAGE_SPLIT) {
+            for (int g = 0; g < plan.ngroups; ++g) {
+                const int r0 = g * plan.greq, gr = min(plan.greq, plan.Breq - r0);
+                DecodePlan pg = plan;
+                pg.Breq = gr;
+                pg.B = gr * plan.kq;
+                DecodeArgs ag = group_args(a, plan, r0);
+                // after the first group the kernel before each split is the
+                // previous group's combine, which waits for its own
+                // predecessors first and writes none of the call's inputs
+                if (g > 0) ag.early = 1;
+                if (launch_split(ag, pg, s) != cudaSuccess || launch_combine(ag, pg, s) != cudaSuccess)
+                    return PFKV_ERR_CUDA;
+            }
+        }
+    } else {
+        if ((stages & PFKV_STAGE_SPLIT) && launch_split(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
+        if ((stages & PFKV_STAGE_COMBINE) && launch_combine(a, plan, s) != cudaSuccess)
+            return PFKV_ERR_CUDA;
+    }
     if (mass && launch_mass(a, plan, s) != cudaSuccess) return PFKV_ERR_CUDA;
     return PFKV_OK;
 }

@@ -502,7 +502,6 @@ static cudaError_t launch_split_g(const DecodeArgs &a, const DecodePlan &p, cuda
 
 cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     if (p.kind == 1) return launch_split_pers(a, p, s);
-    if (swz_supported(p, a.num_pages)) return launch_split_swz(a, p, s);
     return p.D == 128 ? launch_split_g<128>(a, p, s) : launch_split_g<64>(a, p, s);
 }
 

@@ -144,24 +144,26 @@ __device__ __forceinline__ int exp_above(float x) {
     return min(126, max(eb, 0) - 126);
 }
 
-// TMA: one 16-row x 128-byte box of a pool (rows = units x 16) into shared
-// memory, 128-byte swizzled, completing its bytes on `bar`
-__device__ __forceinline__ void tma_unit(void *dst, const CUtensorMap *map, int row, uint64_t *bar,
+// TMA: one unit (16 rows x 128 bytes) of an FP8 pool seen as [units][16][128
+// B] into shared memory, 128-byte swizzled, completing its bytes on `bar`
+__device__ __forceinline__ void tma_unit(void *dst, const CUtensorMap *map, int unit, uint64_t *bar,
                                          uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-// the same for the 3-D BF16 map: both lines of each of the 16 rows
-__device__ __forceinline__ void tma_unit3(void *dst, const CUtensorMap *map, int row, uint64_t *bar,
-                                          uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row), "r"(smem_addr(bar)), "l"(policy)
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(unit), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// the same for a BF16 pool seen as [units][16][2][64]: both lines of each of
+// the unit's 16 rows
+__device__ __forceinline__ void tma_unit4(void *dst, const CUtensorMap *map, int unit, uint64_t *bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(unit), "r"(smem_addr(bar)),
+        "l"(policy)
         : "memory");
 }
 
@@ -487,12 +489,12 @@ __global__ void __launch_bounds__(PersCfg<WK, BF>::NT, 1)
 #pragma unroll
                 for (int u = 0; u < C::GU; ++u) {
                     if (pu[u] >= 0 && !BF) {
-                        tma_unit(dst + u * C::UNITB, &tmk, pu[u] * kPage, &full[s], policy);
-                        tma_unit(dst + (C::GU + u) * C::UNITB, &tmv, pu[u] * kPage, &full[s], policy);
+                        tma_unit(dst + u * C::UNITB, &tmk, pu[u], &full[s], policy);
+                        tma_unit(dst + (C::GU + u) * C::UNITB, &tmv, pu[u], &full[s], policy);
                     }
                     if (pu[u] >= 0 && BF) {
-                        tma_unit3(dst + u * C::UNITB, &tmk, pu[u] * kPage, &full[s], policy);
-                        tma_unit3(dst + (C::GU + u) * C::UNITB, &tmv, pu[u] * kPage, &full[s], policy);
+                        tma_unit4(dst + u * C::UNITB, &tmk, pu[u], &full[s], policy);
+                        tma_unit4(dst + (C::GU + u) * C::UNITB, &tmv, pu[u], &full[s], policy);
                     }
                 }
             }
@@ -962,28 +964,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A pool as a tensor read in one box per unit, with the 128-byte swizzle.
-// FP8 [units x 16][128 B]: 2-D, 16-row boxes.  BF16 [units x 16][2][64]: a
+// A pool as a tensor read in one box per unit, with the 128-byte swizzle and
+// the unit index as the outermost coordinate (32-bit, like the unit indices).
+// FP8 [units][16][128 B]: a box is one unit.  BF16 [units][16][2][64]: a
 // 256-byte row is two 128-byte lines (the swizzle spans at most 128 bytes),
-// so the tensor is 3-D and a box is 16 rows x 2 lines.
-cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long rows, bool bf16) {
+// and a box is the unit's 16 rows x 2 lines.
+cudaError_t pool_tensor_map(CUtensorMap *map, const void *pages, long long units, bool bf16) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUresult r;
     if (!bf16) {
-        const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-        const cuuint64_t strides[1] = {128};
-        const cuuint32_t box[2] = {128, (cuuint32_t)kPage};
-        const cuuint32_t estr[2] = {1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pages), dims, strides, box, estr,
+        const cuuint64_t dims[3] = {128, (cuuint64_t)kPage, (cuuint64_t)units};
+        const cuuint64_t strides[2] = {128, 128 * kPage};
+        const cuuint32_t box[3] = {128, (cuuint32_t)kPage, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pages), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
-        const cuuint64_t dims[3] = {64, 2, (cuuint64_t)rows};
-        const cuuint64_t strides[2] = {128, 256};
-        const cuuint32_t box[3] = {64, 2, (cuuint32_t)kPage};
-        const cuuint32_t estr[3] = {1, 1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pages), dims, strides, box,
+        const cuuint64_t dims[4] = {64, 2, (cuuint64_t)kPage, (cuuint64_t)units};
+        const cuuint64_t strides[3] = {128, 256, 256 * kPage};
+        const cuuint32_t box[4] = {64, 2, (cuuint32_t)kPage, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pages), dims, strides, box,
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
@@ -1019,10 +1022,10 @@ cudaError_t launch_pers_gm(const DecodeArgs &a, const DecodePlan &p, cudaStream_
     const size_t smem = pers_smem_bytes<WK, BF>();
     cudaError_t e = configure_pers<G, MASS, WK, BF>();
     if (e != cudaSuccess) return e;
-    const long long rows = (long long)a.num_pages * p.Hkv * kPage;
+    const long long units = (long long)a.num_pages * p.Hkv;
     alignas(64) CUtensorMap tmk, tmv;
-    if ((e = pool_tensor_map(&tmk, a.k_pages, rows, BF)) != cudaSuccess) return e;
-    if ((e = pool_tensor_map(&tmv, a.v_pages, rows, BF)) != cudaSuccess) return e;
+    if ((e = pool_tensor_map(&tmk, a.k_pages, units, BF)) != cudaSuccess) return e;
+    if ((e = pool_tensor_map(&tmv, a.v_pages, units, BF)) != cudaSuccess) return e;
     return launch_pdl(decode_split_pers_kernel<G, MASS, WK, BF>, dim3(p.pers_ctas), dim3(C::NT), smem, s,
                       tmk, tmv, a, p.Hkv, p.B, p.nchunks, p.chunk_tokens, a.ws_prefix);
 }
@@ -1057,12 +1060,8 @@ int pers_workers_for(long long units_bound, int num_sms) {
     return units_bound > (long long)num_sms * 8 * 192 ? 12 : 8;
 }
 
-bool pers_supported(const DecodePlan &p, int num_pages) {
-    const long long rows = (long long)num_pages * p.Hkv * kPage;
-    const long long K = (long long)p.B * p.Hkv * p.nchunks;
-    return (p.dtype == PFKV_KV_FP8_E4M3 || p.dtype == PFKV_KV_BF16) && p.D == 128 && p.G <= 8 &&
-           rows < (1LL << 31) &&
-           K <= kPersMaxSegments && p.Breq <= kPersMaxRequests;
+bool pers_supported(const DecodePlan &p) {
+    return (p.dtype == PFKV_KV_FP8_E4M3 || p.dtype == PFKV_KV_BF16) && p.D == 128 && p.G <= 8;
 }
 
 namespace {

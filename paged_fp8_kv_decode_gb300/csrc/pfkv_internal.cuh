@@ -52,6 +52,10 @@ struct DecodePlan {
     bool mass;
     size_t off_mscore, off_lsefin, off_rflags;
     int Breq, kq;       // requests and query tokens per request (B = Breq * kq)
+    // persistent kind: the batch runs as ngroups launches of up to greq
+    // requests each (split then combine per group), so that one launch's
+    // segments and requests fit the kernels' shared-memory tables
+    int greq, ngroups;
 };
 
 struct DecodeArgs {
@@ -203,12 +207,10 @@ cudaError_t launch_append_validate(const AppendArgs &ap, int B, const DecodeArgs
                                    cudaStream_t s);
 cudaError_t launch_split(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_mass(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
-bool swz_supported(const DecodePlan &p, int num_pages);
-bool pers_supported(const DecodePlan &p, int num_pages);
+bool pers_supported(const DecodePlan &p);
 int pers_workers_for(long long units_bound, int num_sms);
 cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
-cudaError_t launch_split_swz(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *out, cudaStream_t s);
 cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStream_t s);
@@ -220,7 +222,6 @@ cudaError_t preload_append();
 cudaError_t preload_split_pers();
 cudaError_t preload_combine_pers();
 cudaError_t preload_split_generic();
-cudaError_t preload_split_swz();
 cudaError_t preload_mass();
 
 // Loads one kernel (a no-op if it is loaded already).

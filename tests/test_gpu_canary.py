@@ -8,9 +8,10 @@ pools and their scales, the attention-mass totals) sits between two guard
 regions of seeded random bytes, and each test checks, after the call, that
 every guard byte is unchanged and that the guarded call's results equal an
 unguarded call's.  The cases take every kernel path: the persistent split
-kernel (8 and 12 workers, FP8 and BF16, groups of 4 and 8), the combine's
-query-head groups, the per-chunk kernels (many segments; head_dim 64), the
-fused tag check, the attention-mass pass and multi-query verify.
+kernel (8 and 12 workers, FP8 and BF16, groups of 4 and 8, a coarsened split,
+request groups), the combine's query-head groups, the per-chunk kernel
+(head_dim 64), the fused tag check, the attention-mass pass and multi-query
+verify.
 """
 import dataclasses
 
@@ -91,6 +92,9 @@ STEP_CASES = {
                                      num_pages=1024, lens=np.array([3000, 2900, 2950], np.int32),
                                      append=True, split_tokens=16, seed=404), None),
     "head_dim_64": (lambda: dataclasses.replace(W.spec_tiny(), append=True), None),
+    "request_groups": (lambda: W.Spec("groups", B=520, Hq=32, Hkv=8, D=128, kv_dtype="fp8",
+                                      num_pages=1200, lens=np.arange(520, dtype=np.int32) % 37 + 1,
+                                      append=True, stale_per_mille=3.0, seed=515), None),
     "evict": (lambda: dataclasses.replace(W.spec_evict("small"), append=True), None),
 }
 

@@ -1,7 +1,7 @@
 """The tag check fused into the attention kernel (pfkv_paged_decode_attn_fused_tags)
-against the oracle, on every kernel path: the persistent FP8 kernel (head_dim
-128, G <= 4), the per-chunk kernels (BF16, head_dim 64, G = 8) and the
-many-segment fallback.  Flags must equal the oracle's tag/bounds check bit for
+against the oracle, on every kernel path: the persistent tensor-core kernel
+(head_dim 128, FP8 and BF16, with a coarsened split and in request groups) and
+the per-chunk kernel (head_dim 64).  Flags must equal the oracle's tag/bounds check bit for
 bit; outputs are within the contract tolerance (the fused call may split the
 work differently from the two-kernel call, so the two are not compared bit for
 bit with each other)."""
@@ -82,11 +82,22 @@ def test_bad_ids_and_stale_tags_fused(B):
     assert np.array_equal(db.flags.cpu().numpy()[:spec.B], want)
 
 
-def test_many_segments_fallback_fused(B):
-    """More segments than the persistent kernel's prefix table: the swizzled
-    per-chunk kernel runs, with the tag check fused into it."""
+def test_many_segments_coarsened_fused(B):
+    """More segments than the persistent kernel's tables at the caller's split
+    size: a coarser split, with the tag check fused into the kernel."""
     lens = np.array([3000, 2900, 2950], dtype=np.int32)
     spec = W.Spec("manyseg", B=3, Hq=32, Hkv=8, D=128, kv_dtype="fp8", num_pages=1024,
                   lens=lens, tags=True, split_tokens=16, seed=404, stale_per_mille=0.5)
     db, ref, _ = run_and_compare(spec, label="many-segments fused", fused_tags=True)
     assert ref["flags"].any() and not ref["flags"].all()
+
+
+def test_request_groups_fused(B):
+    """520 requests x 8 kv heads: request groups, tag check fused."""
+    rng = np.random.default_rng(909)
+    lens = rng.integers(1, 80, size=520, endpoint=True).astype(np.int32)
+    spec = W.Spec("groups-fused", B=520, Hq=32, Hkv=8, D=128, kv_dtype="fp8",
+                  num_pages=int(((lens + 16) // 16).sum()) + 16, lens=lens, append=True, tags=True,
+                  stale_per_mille=3.0, seed=909)
+    db, ref, _ = run_and_compare(spec, label="request groups fused", fused_tags=True)
+    assert ref["flags"].any()

@@ -90,11 +90,22 @@ def test_per_chunk_kernels(B, kv_dtype, D, G):
     _run(B, spec, label=f"{kv_dtype} D{D} G{G}")
 
 
-def test_many_segments_fallback(B):
+def test_many_segments_coarsened(B):
     lens = np.array([3000, 2900, 2950], dtype=np.int32)
     spec = W.Spec("manyseg", B=3, Hq=32, Hkv=8, D=128, kv_dtype="fp8", num_pages=1024,
                   lens=lens, tags=True, split_tokens=16, seed=404)
     _run(B, spec, label="many-segments")
+
+
+def test_request_groups(B):
+    """520 requests x 8 kv heads: request groups; the scores and final
+    normalisers of every group meet in the one mass pass."""
+    rng = np.random.default_rng(808)
+    lens = rng.integers(1, 60, size=520, endpoint=True).astype(np.int32)
+    spec = W.Spec("groups-mass", B=520, Hq=32, Hkv=8, D=128, kv_dtype="fp8",
+                  num_pages=int(((lens + 16) // 16).sum()) + 16, lens=lens, tags=True,
+                  stale_per_mille=3.0, seed=808)
+    _run(B, spec, label="request groups")
 
 
 def test_zero_length_heads(B):

@@ -3,7 +3,7 @@ candidate tokens per request, the last kq tokens of every head, query token i
 attending to the first n - kq + 1 + i tokens.  Covers the persistent FP8
 kernel (automatic and fixed splits, per-head tables, stale tags with the
 separate and the fused check), the per-chunk kernels (BF16, head_dim 64,
-G = 8), the many-segment fallback, heads shorter than kq, and kq = 1 equal to
+G = 8), a split coarsened to fit, request groups, heads shorter than kq, and kq = 1 equal to
 the plain call.  Outputs within the contract tolerance; flags bit for bit."""
 import dataclasses
 
@@ -66,11 +66,24 @@ def test_per_chunk_kernels(B, kv_dtype, D, G, kq):
     _run(B, spec, kq, label=f"{kv_dtype} D{D} G{G} kq={kq}")
 
 
-def test_many_segments_fallback(B):
+def test_many_segments_coarsened(B):
     lens = np.array([3000, 2900, 2950], dtype=np.int32)
     spec = W.Spec("manyseg", B=3, Hq=32, Hkv=8, D=128, kv_dtype="fp8", num_pages=1024,
                   lens=lens, tags=True, split_tokens=16, seed=404)
     _run(B, spec, 2, label="many-segments kq=2")
+
+
+def test_request_groups(B):
+    """200 requests x 3 query tokens x 8 kv heads > 4,096 virtual (request,
+    kv head) pairs: request groups whose virtual requests stay whole; stale
+    tags flag some requests."""
+    rng = np.random.default_rng(707)
+    lens = rng.integers(3, 70, size=200, endpoint=True).astype(np.int32)
+    spec = W.Spec("groups-kq3", B=200, Hq=32, Hkv=8, D=128, kv_dtype="fp8",
+                  num_pages=int(((lens + 16) // 16).sum()) + 16, lens=lens, tags=True,
+                  stale_per_mille=4.0, seed=707)
+    _, _, _, flags, _ = _run(B, spec, 3, label="request groups kq=3")
+    assert flags.any() and not flags.all()
 
 
 def test_heads_shorter_than_the_candidates(B):

@@ -255,13 +255,41 @@ def test_repeat_calls_are_deterministic(B):
     assert torch.equal(first, db.out)
 
 
-def test_many_segments_fallback_path(B):
-    """More (request, kv head, chunk) segments than the persistent kernel's
-    prefix table holds: the per-chunk kernel takes over; same results."""
+def test_many_segments_coarsen_the_split(B):
+    """A fixed split size that would give more (request, kv head, chunk)
+    segments than the persistent kernel's tables hold: the kernel takes a
+    coarser split (a multiple of the caller's; only the output is
+    contracted); same results."""
     lens = np.array([3000, 2900, 2950], dtype=np.int32)
     spec = W.Spec("manyseg", B=3, Hq=32, Hkv=8, D=128, kv_dtype="fp8", num_pages=1024,
                   lens=lens, tags=True, split_tokens=16, seed=404)
     run_and_compare(spec, label="many-segments")
+
+
+@pytest.mark.parametrize("kv_dtype", ["fp8", "bf16"])
+def test_long_sequences_with_a_small_split(B, kv_dtype):
+    """16-token chunks of 30,000-token sequences: 30,000 segments, coarsened."""
+    lens = np.array([30000, 17000], dtype=np.int32)
+    spec = W.Spec(f"smallsplit-{kv_dtype}", B=2, Hq=16, Hkv=4, D=128, kv_dtype=kv_dtype,
+                  num_pages=int(((lens + 16) // 16).sum()) + 8, lens=lens, append=True,
+                  tags=True, split_tokens=16, seed=405)
+    run_and_compare(spec, label=f"small split {kv_dtype}")
+
+
+@pytest.mark.parametrize("kv_dtype,G", [("fp8", 4), ("bf16", 8), ("fp8", 1)])
+def test_request_groups(B, kv_dtype, G):
+    """More (request, kv head) pairs than one persistent launch's tables
+    hold (520 requests x 8 kv heads > 4,096): the batch runs as request
+    groups, each a split and a combine; stale tags flag requests in both
+    groups."""
+    rng = np.random.default_rng(606 + G)
+    lens = rng.integers(1, 90, size=520, endpoint=True).astype(np.int32)
+    spec = W.Spec(f"groups-{kv_dtype}-g{G}", B=520, Hq=8 * G, Hkv=8, D=128, kv_dtype=kv_dtype,
+                  num_pages=int(((lens + 16) // 16).sum()) + 16, lens=lens, append=True,
+                  tags=True, stale_per_mille=3.0, seed=606 + G)
+    db, ref, _ = run_and_compare(spec, label=f"request groups {kv_dtype} G={G}")
+    f = ref["flags"]
+    assert f[:512].any() and f[512:].any() or f.any()
 
 
 def test_packed_step_io_gives_the_same_outputs(B):

@@ -107,9 +107,11 @@ def test_noalloc_rejects_calls_beyond_its_workspace(B):
     """A call that would need more than the built-in workspace is refused
     with PFKV_ERR_WORKSPACE before anything runs; out is left untouched."""
     from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
-    spec = W.spec_llama8b("small")
+    spec = dataclasses.replace(W.spec_llama8b("small"), Hq=64)  # groups of 8 query heads
     db = DeviceBatch(W.make_batch(spec))
-    split, max_len = 16, 1 << 20    # many 16-token chunks: a large workspace
+    # 16-token chunks of up to 2^20 tokens: the split kernel's tables fill up
+    # (4,096 segments) and every partial row holds 8 heads: a large workspace
+    split, max_len = 16, 1 << 20
     need = B.pfkv_decode_workspace_size(db.cache, db.pages, spec.Hq, split, max_len)
     assert need > B.PFKV_NOALLOC_WORKSPACE_BYTES
     out = torch.full_like(db.out, 3.0)
