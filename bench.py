@@ -263,9 +263,9 @@ BF16_MMA_DTYPE = "bf16 KV, bf16 x bf16 tensor-core MMA with fp32 accumulation, b
 
 def path_dtype(spec) -> str:
     """The arithmetic a workload's split kernel computes in: the tensor-core
-    kernel takes head_dim 128 with groups of up to 8 heads, the CUDA-core
-    kernels everything else."""
-    mma = spec.D == 128 and spec.Hq // spec.Hkv <= 8
+    kernel takes head_dim 128 or 64 with groups of up to 8 heads (every
+    single-query workload), the CUDA-core kernel the rest."""
+    mma = spec.D in (64, 128) and spec.Hq // spec.Hkv <= 8
     if spec.kv_dtype == "fp8":
         return FP8_DTYPE if mma else "fp8_e4m3 KV, fp32 FMA, bf16 q/out"
     return BF16_MMA_DTYPE if mma else "bf16 KV, fp32 FMA, bf16 q/out"

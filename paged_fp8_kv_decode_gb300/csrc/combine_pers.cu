@@ -27,6 +27,24 @@ __device__ __forceinline__ float plog2(float x) {
     return y;
 }
 
+// VL consecutive floats (4 or 2: one vector load)
+template <int VL>
+__device__ __forceinline__ void load_vec(float (&v)[VL], const float *p) {
+    if constexpr (VL == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(p);
+        v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2 *>(p);
+        v[0] = t.x, v[1] = t.y;
+    }
+}
+
+template <int VL>
+__device__ __forceinline__ void store_vec(float *p, const float (&v)[VL]) {
+    if constexpr (VL == 4) *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    else *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+}
+
 }  // namespace
 
 // --------------------------------------------------------------------------
@@ -42,9 +60,9 @@ __device__ __forceinline__ float plog2(float x) {
 //     [cstart[c], cstart[c+1]), the first at workspace row cbase[c]);
 //  2. the status rows of the request's segments (a thread per segment; lists
 //     of 8 or more rows go to a warp each) and the rows of (b, h): warp w
-//     merges flat rows w, w + NW, ..., four at a time with their loads issued
-//     together, with a running max per query head (lane l owns dims
-//     [4l, 4l + 4) of every head);
+//     merges flat rows w, w + NW, ..., several at a time with their loads
+//     issued together, with a running max per query head (lane l owns dims
+//     [l D / 32, (l + 1) D / 32) of every head);
 //  the warps' (max, weight, sum) meet in shared memory; out = sum / weight,
 //  bf16, or zeros if the request carries a flag.
 // --------------------------------------------------------------------------
@@ -52,7 +70,7 @@ constexpr int kCombMaxChunks = kPersMaxSegments;  // segments per (b, h) <= all 
 constexpr int kCombShortList = 8;                  // status rows a thread gathers itself
 constexpr int kCombMaxDeferred = 256;              // longer lists handed to warps
 
-template <int GS, int NW>
+template <int GS, int NW, int D>
 struct CombSmem {
     union {
         struct {
@@ -60,7 +78,7 @@ struct CombSmem {
             int cbase[kCombMaxChunks];
         } rows;
         struct {
-            float acc[NW][GS][128];
+            float acc[NW][GS][D];
             float wsum[NW][GS];
             float wmax[NW][GS];
         } red;
@@ -71,13 +89,14 @@ struct CombSmem {
     int ndef;
 };
 
-template <int G, int GS, int NW>
+template <int G, int GS, int NW, int D>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
                                                                           int nchunks, int W,
                                                                           const int *ws_prefix) {
     static_assert(G % GS == 0, "query-head groups split G evenly");
-    constexpr int D = 128, NT = NW * 32, HG = G / GS;
-    __shared__ CombSmem<GS, NW> sm;
+    static_assert(D == 128 || D == 64, "head_dim 128 or 64");
+    constexpr int NT = NW * 32, HG = G / GS, VL = D / 32;
+    __shared__ CombSmem<GS, NW, D> sm;
     pdl_enter();
     // CTA (b, h, gi) merges query heads gi GS .. gi GS + GS - 1 of (b, h)
     const int bhx = blockIdx.x / HG, gi = blockIdx.x - bhx * HG, g0 = gi * GS;
@@ -180,17 +199,18 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
             if (i < scnt) st[i] = a.status[sk + sp0 + i];
     }
     float M[GS], S[GS];
-    float4 acc[GS];
+    float acc[GS][VL];
 #pragma unroll
     for (int g = 0; g < GS; ++g) {
         M[g] = -INFINITY;
         S[g] = 0.f;
-        acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int v = 0; v < VL; ++v) acc[g][v] = 0.f;
     }
     constexpr int RB = GS == 8 ? 1 : GS == 1 ? 8 : 4;  // rows in flight per warp (registers)
     for (int j0 = warp; j0 < R; j0 += RB * NW) {
         float lc[RB][GS];
-        float4 ov[RB][GS];
+        float ov[RB][GS][VL];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
             const int j = j0 + r * NW;
@@ -198,8 +218,12 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
 #pragma unroll
             for (int g = 0; g < GS; ++g) {
                 lc[r][g] = j < R ? a.lse[row * G + g0 + g] : -INFINITY;
-                ov[r][g] = j < R ? *reinterpret_cast<const float4 *>(a.o + (row * G + g0 + g) * D + lane * 4)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < R) {
+                    load_vec<VL>(ov[r][g], a.o + (row * G + g0 + g) * D + lane * VL);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < VL; ++v) ov[r][g][v] = 0.f;
+                }
             }
         }
 #pragma unroll
@@ -210,18 +234,14 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
                 if (lc[r][g] > M[g]) {
                     const float sc = M[g] == -INFINITY ? 0.f : pexp2(M[g] - lc[r][g]);
                     S[g] *= sc;
-                    acc[g].x *= sc;
-                    acc[g].y *= sc;
-                    acc[g].z *= sc;
-                    acc[g].w *= sc;
+#pragma unroll
+                    for (int v = 0; v < VL; ++v) acc[g][v] *= sc;
                     M[g] = lc[r][g];
                 }
                 const float wt = pexp2(lc[r][g] - M[g]);
                 S[g] += wt;
-                acc[g].x = fmaf(wt, ov[r][g].x, acc[g].x);
-                acc[g].y = fmaf(wt, ov[r][g].y, acc[g].y);
-                acc[g].z = fmaf(wt, ov[r][g].z, acc[g].z);
-                acc[g].w = fmaf(wt, ov[r][g].w, acc[g].w);
+#pragma unroll
+                for (int v = 0; v < VL; ++v) acc[g][v] = fmaf(wt, ov[r][g][v], acc[g][v]);
             }
         }
     }
@@ -256,7 +276,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
     if (f) atomicOr(&sm.flags, f);
 #pragma unroll
     for (int g = 0; g < GS; ++g) {
-        *reinterpret_cast<float4 *>(&sm.u.red.acc[warp][g][lane * 4]) = acc[g];
+        store_vec<VL>(&sm.u.red.acc[warp][g][lane * VL], acc[g]);
         if (lane == 0) {
             sm.u.red.wsum[warp][g] = S[g];
             sm.u.red.wmax[warp][g] = M[g];
@@ -307,11 +327,17 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
 // --------------------------------------------------------------------------
 namespace {
 
+template <int G, int GS, int NW, int D>
+cudaError_t launch_comb_d(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
+    const unsigned grid = (unsigned)(p.B * p.Hkv * (G / GS));
+    return launch_pdl(decode_combine_pers_kernel<G, GS, NW, D>, dim3(grid), dim3(NW * 32), 0, s, a, p.Hkv,
+                      p.nchunks, p.workers, (const int *)a.ws_prefix);
+}
+
 template <int G, int GS, int NW>
 cudaError_t launch_comb(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
-    const unsigned grid = (unsigned)(p.B * p.Hkv * (G / GS));
-    return launch_pdl(decode_combine_pers_kernel<G, GS, NW>, dim3(grid), dim3(NW * 32), 0, s, a, p.Hkv,
-                      p.nchunks, p.workers, (const int *)a.ws_prefix);
+    if (p.D == 64) return launch_comb_d<G, GS, NW, 64>(a, p, s);
+    return p.D == 128 ? launch_comb_d<G, GS, NW, 128>(a, p, s) : cudaErrorInvalidValue;
 }
 
 template <int G>
@@ -343,22 +369,31 @@ cudaError_t launch_combine_g(const DecodeArgs &a, const DecodePlan &p, cudaStrea
 
 }  // namespace
 
-cudaError_t preload_combine_pers() {
+namespace {
+template <int D>
+cudaError_t preload_combine_d() {
     cudaError_t e = cudaSuccess;
     auto one = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
-    one(preload_kernel(decode_combine_pers_kernel<8, 8, 8>));
-    one(preload_kernel(decode_combine_pers_kernel<8, 4, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<8, 2, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<8, 1, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<4, 4, 8>));
-    one(preload_kernel(decode_combine_pers_kernel<4, 4, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<4, 2, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<4, 1, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<2, 2, 8>));
-    one(preload_kernel(decode_combine_pers_kernel<2, 2, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<2, 1, 16>));
-    one(preload_kernel(decode_combine_pers_kernel<1, 1, 8>));
-    one(preload_kernel(decode_combine_pers_kernel<1, 1, 16>));
+    one(preload_kernel(decode_combine_pers_kernel<8, 8, 8, D>));
+    one(preload_kernel(decode_combine_pers_kernel<8, 4, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<8, 2, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<8, 1, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 4, 8, D>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 4, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 2, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<4, 1, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<2, 2, 8, D>));
+    one(preload_kernel(decode_combine_pers_kernel<2, 2, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<2, 1, 16, D>));
+    one(preload_kernel(decode_combine_pers_kernel<1, 1, 8, D>));
+    one(preload_kernel(decode_combine_pers_kernel<1, 1, 16, D>));
+    return e;
+}
+}  // namespace
+
+cudaError_t preload_combine_pers() {
+    cudaError_t e = preload_combine_d<128>();
+    if (e == cudaSuccess) e = preload_combine_d<64>();
     return e;
 }
 

@@ -42,8 +42,8 @@ struct DecodePlan {
     bool tags;
     // kind 0: one CTA per (request, kv head, chunk), workspace rows indexed
     //         [b][hq][chunk];
-    // kind 1: persistent balanced workers (FP8, head_dim 128, G <= 4), rows
-    //         indexed segment + worker, pers_ctas CTAs
+    // kind 1: persistent balanced workers (FP8 or BF16, head_dim 128 or 64,
+    //         G <= 8), rows indexed segment + worker, pers_ctas CTAs
     int kind;
     int pers_ctas, workers;
     int htiles;         // validation tiles per table row: ceil(max_pages / kValTile)
@@ -210,6 +210,7 @@ cudaError_t launch_mass(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s
 bool pers_supported(const DecodePlan &p);
 int pers_workers_for(long long units_bound, int num_sms);
 cudaError_t launch_split_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
+cudaError_t launch_split_pers_d64(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_combine_pers(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *out, cudaStream_t s);
@@ -220,6 +221,7 @@ cudaError_t launch_e4m3_decode(const uint8_t *c, int64_t n, float *out, cudaStre
 // lazy module loading.  Called once per device, on its first use.
 cudaError_t preload_append();
 cudaError_t preload_split_pers();
+cudaError_t preload_split_pers_d64();
 cudaError_t preload_combine_pers();
 cudaError_t preload_split_generic();
 cudaError_t preload_mass();

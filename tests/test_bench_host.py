@@ -122,5 +122,5 @@ def test_roofline_traffic_comes_from_the_capture_of_the_same_source(tmp_path, mo
 def test_dtype_label_follows_the_kernel_path():
     llama = W.spec_llama8b("small")
     assert bench.path_dtype(llama) == bench.FP8_DTYPE
-    assert "fp32 FMA" in bench.path_dtype(W.spec_tiny())  # head_dim 64: CUDA-core kernel
+    assert bench.path_dtype(W.spec_tiny()) == bench.BF16_MMA_DTYPE  # head_dim 64: tensor cores too
     assert bench.path_dtype(W.spec_sweep(8, "bf16", "small")) == bench.BF16_MMA_DTYPE

@@ -8,10 +8,11 @@ pools and their scales, the attention-mass totals) sits between two guard
 regions of seeded random bytes, and each test checks, after the call, that
 every guard byte is unchanged and that the guarded call's results equal an
 unguarded call's.  The cases take every kernel path: the persistent split
-kernel (8 and 12 workers, FP8 and BF16, groups of 4 and 8, a coarsened split,
-request groups), the combine's query-head groups, the per-chunk kernel
-(head_dim 64), the fused tag check, the attention-mass pass and multi-query
-verify.
+kernel (8 and 12 workers, FP8 and BF16, head_dim 128 and 64, groups of 4
+and 8, a coarsened split, request groups), the combine's query-head groups,
+the per-chunk kernel (multi-query verify with more query tokens x kv heads
+than a persistent launch holds), the fused tag check, the attention-mass pass
+and multi-query verify.
 """
 import dataclasses
 
@@ -92,6 +93,9 @@ STEP_CASES = {
                                      num_pages=1024, lens=np.array([3000, 2900, 2950], np.int32),
                                      append=True, split_tokens=16, seed=404), None),
     "head_dim_64": (lambda: dataclasses.replace(W.spec_tiny(), append=True), None),
+    "head_dim_64_fp8_long": (lambda: W.Spec("d64", B=3, Hq=16, Hkv=4, D=64, kv_dtype="fp8",
+                                            num_pages=600, lens=np.array([4000, 1500, 33], np.int32),
+                                            append=True, stale_per_mille=2.0, seed=919), 131072),
     "request_groups": (lambda: W.Spec("groups", B=520, Hq=32, Hkv=8, D=128, kv_dtype="fp8",
                                       num_pages=1200, lens=np.arange(520, dtype=np.int32) % 37 + 1,
                                       append=True, stale_per_mille=3.0, seed=515), None),
@@ -148,12 +152,16 @@ def test_attention_mass_writes_only_its_buffers(B, case):
     assert torch.equal(g["flags"].t[:spec.B], want_flags[:spec.B]), case
 
 
-@pytest.mark.parametrize("case", ["llama8b", "evict", "head_dim_64", "many_segments", "g8_bf16"])
-def test_multi_query_writes_only_its_buffers(B, case):
+@pytest.mark.parametrize("case,kq", [("llama8b", 3), ("evict", 3), ("head_dim_64", 3),
+                                     ("many_segments", 3), ("g8_bf16", 3), ("llama8b", 520)])
+def test_multi_query_writes_only_its_buffers(B, case, kq):
+    """kq = 520 on 8 kv heads: the per-chunk kernel and its combine."""
     make, bound = STEP_CASES[case]
     spec = dataclasses.replace(make(), append=False)
+    if kq > 3:
+        spec = dataclasses.replace(spec, B=2, lens=spec.lens[:2])
     db = _db(spec, bound)
-    kq, L = 3, db.max_seq_len
+    L = db.max_seq_len
     gen = torch.Generator(device="cuda").manual_seed(99)
     q = torch.randn((spec.B, kq, spec.Hq, spec.D), generator=gen, device="cuda").to(torch.bfloat16)
     need = B.pfkv_decode_multi_workspace_size(db.cache, db.pages, spec.Hq, kq, spec.split_tokens, L)

@@ -1,8 +1,8 @@
 """The tag check fused into the attention kernel (pfkv_paged_decode_attn_fused_tags)
 against the oracle, on every kernel path: the persistent tensor-core kernel
-(head_dim 128, FP8 and BF16, with a coarsened split and in request groups) and
-the per-chunk kernel (head_dim 64).  Flags must equal the oracle's tag/bounds check bit for
-bit; outputs are within the contract tolerance (the fused call may split the
+(head_dim 128 and 64, FP8 and BF16, with a coarsened split and in request
+groups; the per-chunk kernel's fused check is in the multi-query tests).
+Flags must equal the oracle's tag/bounds check bit for bit; outputs are within the contract tolerance (the fused call may split the
 work differently from the two-kernel call, so the two are not compared bit for
 bit with each other)."""
 import dataclasses

@@ -1,7 +1,7 @@
 """Attention mass (pfkv_paged_decode_attn_mass) against the oracle on every
-kernel path: the persistent FP8 kernel (automatic and fixed splits, per-head
-tables, stale tags), the per-chunk kernels (BF16, head_dim 64, G = 8) and the
-many-segment fallback, with the separate and the fused tag check.
+kernel configuration: the persistent kernel (FP8 and BF16, head_dim 128 and
+64, G up to 8, automatic and fixed splits, per-head tables, stale tags) and
+its many-segment coarsening, with the separate and the fused tag check.
 
 The accumulator starts from seeded non-zero values and has padded rows, so
 the test sees accumulation, strides, and that entries past a head's length

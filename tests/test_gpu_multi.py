@@ -2,9 +2,10 @@
 candidate tokens per request, the last kq tokens of every head, query token i
 attending to the first n - kq + 1 + i tokens.  Covers the persistent FP8
 kernel (automatic and fixed splits, per-head tables, stale tags with the
-separate and the fused check), the per-chunk kernels (BF16, head_dim 64,
-G = 8), a split coarsened to fit, request groups, heads shorter than kq, and kq = 1 equal to
-the plain call.  Outputs within the contract tolerance; flags bit for bit."""
+separate and the fused check, BF16, head_dim 64, G = 8), a split coarsened to
+fit, request groups, the per-chunk kernel (more query tokens x kv heads than
+one persistent launch's tables hold), heads shorter than kq, and kq = 1 equal
+to the plain call.  Outputs within the contract tolerance; flags bit for bit."""
 import dataclasses
 
 import numpy as np
@@ -58,12 +59,27 @@ def test_evict_small_per_head_and_stale_tags(B, fused):
 
 
 @pytest.mark.parametrize("kv_dtype,D,G,kq", [("bf16", 128, 4, 3), ("fp8", 64, 2, 2),
-                                             ("fp8", 128, 8, 4), ("bf16", 64, 1, 5)])
-def test_per_chunk_kernels(B, kv_dtype, D, G, kq):
+                                             ("fp8", 128, 8, 4), ("bf16", 64, 1, 5),
+                                             ("fp8", 64, 8, 3), ("bf16", 64, 4, 2)])
+def test_dtypes_head_dims_and_groups(B, kv_dtype, D, G, kq):
     base = W.spec_sweep(5, kv_dtype, scale="small")
     spec = dataclasses.replace(base, D=D, Hkv=4, Hq=4 * G,
                                lens=np.array([1000, 37, 512, 16, 700], np.int32))
     _run(B, spec, kq, label=f"{kv_dtype} D{D} G{G} kq={kq}")
+
+
+@pytest.mark.parametrize("kv_dtype,D,fused", [("fp8", 128, False), ("fp8", 128, True),
+                                              ("bf16", 64, False), ("fp8", 64, True)])
+def test_per_chunk_kernel_for_many_query_tokens(B, kv_dtype, D, fused):
+    """520 query tokens x 8 kv heads = 4,160 virtual (request, kv head)
+    pairs: more than one persistent launch holds even for one request, so
+    the per-chunk kernel and its combine take the call (with the separate or
+    the fused tag check; a stale tag flags a request)."""
+    lens = np.array([700, 530], dtype=np.int32)
+    spec = W.Spec(f"perchunk-{kv_dtype}-d{D}", B=2, Hq=16, Hkv=8, D=D, kv_dtype=kv_dtype,
+                  num_pages=int(((lens + 16) // 16).sum()) + 8, lens=lens, tags=True,
+                  stale_per_mille=30.0, split_tokens=0, seed=808 + D)
+    _run(B, spec, 520, fused=fused, label=f"per-chunk {kv_dtype} D{D} fused={fused} kq=520")
 
 
 def test_many_segments_coarsened(B):

@@ -151,6 +151,20 @@ def test_group_sizes_and_head_dims(B, kv_dtype, D, G):
     run_and_compare(spec, label=spec.name)
 
 
+@pytest.mark.parametrize("kv_dtype", ["fp8", "bf16"])
+@pytest.mark.parametrize("split", [0, 48])
+@pytest.mark.parametrize("bound", [None, 131072])
+def test_head_dim_64_worker_shapes_and_splits(B, kv_dtype, split, bound):
+    """head_dim 64 on the persistent tensor-core kernel: sequences of many
+    units (each worker streams several, crossing segment edges), one segment
+    per head or 48-token chunks, the 8- and 12-worker shapes."""
+    lens = np.array([1, 17, 300, 1000, 2049, 4000], dtype=np.int32)
+    spec = W.Spec(f"d64-{kv_dtype}", B=len(lens), Hq=16, Hkv=4, D=64, kv_dtype=kv_dtype,
+                  num_pages=int(((lens + 16) // 16).sum()) + 8, lens=lens, append=True,
+                  tags=True, stale_per_mille=2.0, split_tokens=split, seed=909)
+    run_and_compare(spec, label=f"d64 {kv_dtype} split={split} bound={bound}", max_seq_len=bound)
+
+
 @pytest.mark.parametrize("split", [16, 32, 0])
 def test_per_head_lengths_with_zero_length_heads(B, split):
     lens = np.array([[0, 5, 16, 31], [64, 0, 0, 1], [200, 17, 33, 0]], dtype=np.int32)
@@ -177,10 +191,11 @@ def test_all_lengths_zero(B):
 # wholly different output
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
-def test_dominant_key_at_page_and_chunk_edges(B, kv_dtype):
+@pytest.mark.parametrize("D", [128, 64])
+def test_dominant_key_at_page_and_chunk_edges(B, kv_dtype, D):
     split = 64
     lens = np.array([1, 16, 17, 64, 65, 130, 191, 300], dtype=np.int32)
-    spec = W.Spec("needle", B=len(lens), Hq=8, Hkv=2, D=128, kv_dtype=kv_dtype, num_pages=256,
+    spec = W.Spec("needle", B=len(lens), Hq=8, Hkv=2, D=D, kv_dtype=kv_dtype, num_pages=256,
                   lens=lens, tags=True, split_tokens=split, seed=31, outlier_prob=0.0)
     T = int(lens.max())
     q = W.draw_q(spec)
@@ -193,7 +208,7 @@ def test_dominant_key_at_page_and_chunk_edges(B, kv_dtype):
         for h in range(spec.Hkv):
             j = int(cands[(b + h) % len(cands)])
             k_rows[b, h, j] = (q[b, h * spec.G].float() * 3.0).to(torch.bfloat16)
-    db, ref, _ = run_and_compare(spec, rows=(k_rows, v_rows), q=q, label=f"needle-{kv_dtype}")
+    db, ref, _ = run_and_compare(spec, rows=(k_rows, v_rows), q=q, label=f"needle-{kv_dtype}-d{D}")
     # the first q head of each group is dominated by its needle token
     for b in range(spec.B):
         for h in range(spec.Hkv):
@@ -266,25 +281,26 @@ def test_many_segments_coarsen_the_split(B):
     run_and_compare(spec, label="many-segments")
 
 
-@pytest.mark.parametrize("kv_dtype", ["fp8", "bf16"])
-def test_long_sequences_with_a_small_split(B, kv_dtype):
+@pytest.mark.parametrize("kv_dtype,D", [("fp8", 128), ("bf16", 128), ("fp8", 64)])
+def test_long_sequences_with_a_small_split(B, kv_dtype, D):
     """16-token chunks of 30,000-token sequences: 30,000 segments, coarsened."""
     lens = np.array([30000, 17000], dtype=np.int32)
-    spec = W.Spec(f"smallsplit-{kv_dtype}", B=2, Hq=16, Hkv=4, D=128, kv_dtype=kv_dtype,
+    spec = W.Spec(f"smallsplit-{kv_dtype}-d{D}", B=2, Hq=16, Hkv=4, D=D, kv_dtype=kv_dtype,
                   num_pages=int(((lens + 16) // 16).sum()) + 8, lens=lens, append=True,
                   tags=True, split_tokens=16, seed=405)
     run_and_compare(spec, label=f"small split {kv_dtype}")
 
 
-@pytest.mark.parametrize("kv_dtype,G", [("fp8", 4), ("bf16", 8), ("fp8", 1)])
-def test_request_groups(B, kv_dtype, G):
+@pytest.mark.parametrize("kv_dtype,G,D", [("fp8", 4, 128), ("bf16", 8, 128), ("fp8", 1, 128),
+                                          ("fp8", 2, 64)])
+def test_request_groups(B, kv_dtype, G, D):
     """More (request, kv head) pairs than one persistent launch's tables
     hold (520 requests x 8 kv heads > 4,096): the batch runs as request
     groups, each a split and a combine; stale tags flag requests in both
     groups."""
     rng = np.random.default_rng(606 + G)
     lens = rng.integers(1, 90, size=520, endpoint=True).astype(np.int32)
-    spec = W.Spec(f"groups-{kv_dtype}-g{G}", B=520, Hq=8 * G, Hkv=8, D=128, kv_dtype=kv_dtype,
+    spec = W.Spec(f"groups-{kv_dtype}-g{G}-d{D}", B=520, Hq=8 * G, Hkv=8, D=D, kv_dtype=kv_dtype,
                   num_pages=int(((lens + 16) // 16).sum()) + 16, lens=lens, append=True,
                   tags=True, stale_per_mille=3.0, seed=606 + G)
     db, ref, _ = run_and_compare(spec, label=f"request groups {kv_dtype} G={G}")

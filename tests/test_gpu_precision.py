@@ -140,10 +140,10 @@ CASES = {
 }
 
 
-def _run(B, kv_dtype, case, Hq, seed, bound=None):
+def _run(B, kv_dtype, case, Hq, seed, bound=None, D=128):
     lens, same_unit = CASES[case]
     pages = int(((lens + 15) // 16).sum()) + 16
-    spec = W.Spec(f"cancel-{case}-{kv_dtype}", B=len(lens), Hq=Hq, Hkv=2, D=128,
+    spec = W.Spec(f"cancel-{case}-{kv_dtype}-d{D}", B=len(lens), Hq=Hq, Hkv=2, D=D,
                   kv_dtype=kv_dtype, num_pages=pages, lens=lens, tags=True, seed=seed,
                   outlier_prob=0.0)
     batch = W.make_batch(spec)
@@ -153,7 +153,7 @@ def _run(B, kv_dtype, case, Hq, seed, bound=None):
     assert np.median(stress[:, 0]) < 0.25 and np.median(stress[:, 1]) > 20.0, \
         (np.median(stress[:, 0]), np.median(stress[:, 1]))
     db, ref, _ = run_and_compare(spec, rows=(k_rows, v_rows), q=q,
-                                 label=f"cancel {case} {kv_dtype} Hq={Hq} bound={bound}",
+                                 label=f"cancel {case} {kv_dtype} Hq={Hq} D={D} bound={bound}",
                                  max_seq_len=bound)
     assert np.median(np.abs(ref["out"])) < 0.5, np.median(np.abs(ref["out"]))
 
@@ -173,3 +173,11 @@ def test_cancelling_large_values_groups_of_eight(B, kv_dtype, case):
     """The same construction with 8 query heads per kv head (every MMA column
     a real head)."""
     _run(B, kv_dtype, case, Hq=16, seed=43)
+
+
+@pytest.mark.parametrize("kv_dtype", ["fp8", "bf16"])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_cancelling_large_values_head_dim_64(B, kv_dtype, case):
+    """The same construction at head_dim 64 (its own fragment layout of the
+    value product)."""
+    _run(B, kv_dtype, case, Hq=8, seed=47, D=64)
