@@ -49,33 +49,43 @@ __device__ __forceinline__ void store_vec(float *p, const float (&v)[VL]) {
 
 // --------------------------------------------------------------------------
 // One CTA of NW warps per (request b, kv head h) and group of GS of its G
-// query heads, two rounds of loads.  A head with one chunk and few rows takes
-// one CTA of 8 warps for all G query heads (GS = G); a head with many chunks
-// or many rows takes CTAs of 16 warps, one per group of GS query heads, with
-// GS as small as keeps all CTAs in one wave, so that the rows' bytes spread
-// over as many SMs as there are:
-//  1. the unit prefix of every segment of the request and of every chunk of
-//     (b, h), the request's lengths and validation words; the chunks' row
-//     counts are scanned into a flat row order (chunk c owns flat rows
-//     [cstart[c], cstart[c+1]), the first at workspace row cbase[c]);
-//  2. the status rows of the request's segments (a thread per segment; lists
-//     of 8 or more rows go to a warp each) and the rows of (b, h): warp w
-//     merges flat rows w, w + NW, ..., several at a time with their loads
-//     issued together, with a running max per query head (lane l owns dims
-//     [l D / 32, (l + 1) D / 32) of every head);
+// query heads.  A head with one chunk and few rows takes one CTA of 8 warps
+// for all G query heads (GS = G); a head with many chunks or many rows takes
+// CTAs of 16 warps, one per group of GS query heads, with GS as small as keeps
+// all CTAs in one wave, so that the rows' bytes spread over as many SMs as
+// there are:
+//  1. before the wait for the split kernel: the request's lengths and
+//     validation words, and the unit prefix of every segment of the request
+//     (the split kernel's prologue arithmetic on the same lengths, so the
+//     same integers); the chunks of (b, h) are scanned into a flat row order
+//     (chunk c owns flat rows [cstart[c], cstart[c+1])).  A CTA starts as soon
+//     as the split kernel's CTA on its SM has ended, so this part overlaps the
+//     split kernel's last workers.  Where the grid's share of length loads
+//     would be large (kCombEarlyLoads), the prefix is read from the split
+//     kernel's copy after the wait instead;
+//  2. after the wait: the status rows of the request's segments (a thread per
+//     segment; lists of 8 or more rows go to a warp each) and the rows of
+//     (b, h): warp w merges flat rows w, w + NW, ..., several at a time with
+//     their loads issued together, with a running max per query head (lane l
+//     owns dims [l D / 32, (l + 1) D / 32) of every head);
 //  the warps' (max, weight, sum) meet in shared memory; out = sum / weight,
 //  bf16, or zeros if the request carries a flag.
+//
+// Before its wait the kernel reads only the call's inputs and the validation
+// words: the validation kernel had completed when the split kernel passed its
+// own wait, and the split kernel lets this kernel launch only after that.
 // --------------------------------------------------------------------------
 constexpr int kCombMaxChunks = kPersMaxSegments;  // segments per (b, h) <= all segments
 constexpr int kCombShortList = 8;                  // status rows a thread gathers itself
 constexpr int kCombMaxDeferred = 256;              // longer lists handed to warps
+constexpr long long kCombEarlyLoads = 1LL << 20;   // segments x CTAs for the early prefix
 
 template <int GS, int NW, int D>
 struct CombSmem {
     union {
         struct {
-            int cstart[kCombMaxChunks + 1];
-            int cbase[kCombMaxChunks];
+            int pfx[kCombMaxChunks + 1];     // unit prefix at the request's segments
+            int cstart[kCombMaxChunks + 1];  // flat row order of the chunks of (b, h)
         } rows;
         struct {
             float acc[NW][GS][D];
@@ -86,99 +96,130 @@ struct CombSmem {
     int part[NW * 32];
     int defk[kCombMaxDeferred];
     uint32_t flags;
-    int ndef;
+    int ndef, U;
 };
+
+// Exclusive scan of one int per thread over the block (NT threads, one warp
+// scans the per-thread values); returns this thread's prefix, and the total
+// in *total.  Ends with the block synchronised.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int *part, int *total) {
+    const int tid = threadIdx.x;
+    part[tid] = v;
+    __syncthreads();
+    if (tid < 32) {
+        int carry = 0;
+        for (int base = 0; base < NT; base += 32) {
+            const int x0 = part[base + tid];
+            int x = x0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (tid >= off) x += y;
+            }
+            part[base + tid] = carry + x - x0;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (tid == 0) *total = carry;
+    }
+    __syncthreads();
+    return part[tid];
+}
 
 template <int G, int GS, int NW, int D>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(DecodeArgs a, int Hkv,
-                                                                          int nchunks, int W,
-                                                                          const int *ws_prefix) {
+                                                                          int nchunks, int chunk_tokens,
+                                                                          int W, const int *ws_prefix) {
     static_assert(G % GS == 0, "query-head groups split G evenly");
     static_assert(D == 128 || D == 64, "head_dim 128 or 64");
     constexpr int NT = NW * 32, HG = G / GS, VL = D / 32;
     __shared__ CombSmem<GS, NW, D> sm;
-    pdl_enter();
     // CTA (b, h, gi) merges query heads gi GS .. gi GS + GS - 1 of (b, h)
     const int bhx = blockIdx.x / HG, gi = blockIdx.x - bhx * HG, g0 = gi * GS;
     const int b = bhx / Hkv, h = bhx - b * Hkv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = gridDim.x / (Hkv * HG);
     const int K = B * Hkv * nchunks;
-    const int U = ws_prefix[K];
-    W = min(W, U);  // as in the split kernel
+    const bool early = (long long)K * gridDim.x <= kCombEarlyLoads;  // uniform
+    if (!early) pdl_enter();
     if (tid == 0) {
         sm.flags = 0;
         sm.ndef = 0;
     }
 
     // ---- 1. request flags (b is a virtual request; the flags belong to the
-    //      request rb and cover all of its query tokens), segment row lists,
-    //      the chunks of (b, h) ----
+    //      request rb and cover all of its query tokens), the unit prefix at
+    //      the request's segments, the chunks of (b, h) ----
     const int rb = b / a.kq, v0 = rb * a.kq;
     uint32_t f = 0;
     for (int i = tid; i < Hkv; i += NT)
         if (query_len(a, v0, i) < 0) f |= PFKV_FLAG_BAD_LENGTH;
     if (a.hflags)
         for (int i = tid; i < Hkv * a.htiles; i += NT) f |= a.hflags[(long long)rb * Hkv * a.htiles + i];
+    const int nseg = a.kq * Hkv * nchunks, kseg0 = v0 * Hkv * nchunks;
+    int *pfx = sm.u.rows.pfx;  // pfx[i]: first unit of segment kseg0 + i (i <= nseg)
+    if (early) {
+        const int per = (K + NT - 1) / NT;
+        const int k0 = min(K, tid * per), k1 = min(K, k0 + per);
+        int local = 0, nbh = -1, n = 0;
+        for (int k = k0; k < k1; ++k) {
+            const int bh = k / nchunks;
+            if (bh != nbh) {
+                n = query_len(a, bh / Hkv, bh - bh / Hkv * Hkv);
+                nbh = bh;
+            }
+            local += segment_units(n, k - bh * nchunks, chunk_tokens);
+        }
+        int run = block_exclusive_scan<NT>(local, sm.part, &sm.U);
+        nbh = -1;
+        for (int k = k0; k < k1; ++k) {
+            const int bh = k / nchunks;
+            if (bh != nbh) {
+                n = query_len(a, bh / Hkv, bh - bh / Hkv * Hkv);
+                nbh = bh;
+            }
+            if (k >= kseg0 && k <= kseg0 + nseg) pfx[k - kseg0] = run;
+            run += segment_units(n, k - bh * nchunks, chunk_tokens);
+        }
+        if (kseg0 + nseg == K && tid == 0) pfx[nseg] = sm.U;  // the request's end is the end
+    } else {
+        for (int i = tid; i <= nseg; i += NT) pfx[i] = ws_prefix[kseg0 + i];
+        if (tid == 0) sm.U = ws_prefix[K];
+    }
+    __syncthreads();
+    const int U = sm.U;
+    W = min(W, U);  // as in the split kernel
     // status rows of this thread's segment (one segment per thread covers
     // every request of up to NT segments; more go round the loop below)
-    const int nseg = a.kq * Hkv * nchunks, kseg0 = v0 * Hkv * nchunks;
     int sk = -1, sp0 = 0, scnt = 0;
     if (U > 0 && tid < nseg) {
-        const int k = kseg0 + tid;
-        const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+        const int u0 = pfx[tid], u1 = pfx[tid + 1];
         if (u1 > u0) {
-            sk = k;
+            sk = kseg0 + tid;
             sp0 = pers_worker_of(u0, U, W);
             scnt = pers_worker_of(u1 - 1, U, W) - sp0 + 1;
         }
     }
-    const int kbase = (b * Hkv + h) * nchunks;
+    const int kbase = (b * Hkv + h) * nchunks, cb = kbase - kseg0;  // chunk c: pfx[cb + c]
     const int per = (nchunks + NT - 1) / NT;
     const int c0 = min(nchunks, tid * per), c1 = min(nchunks, c0 + per);
     int local = 0;
     for (int c = c0; c < c1; ++c) {
-        const int k = kbase + c;
-        const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
-        int cnt = 0, base = 0;
-        if (U > 0 && u1 > u0) {
-            const int p0 = pers_worker_of(u0, U, W), p1 = pers_worker_of(u1 - 1, U, W);
-            cnt = p1 - p0 + 1;
-            base = k + p0;
-        }
-        sm.u.rows.cstart[c] = cnt;  // the count, turned into the start below
-        sm.u.rows.cbase[c] = base;
-        local += cnt;
+        const int u0 = pfx[cb + c], u1 = pfx[cb + c + 1];
+        if (U > 0 && u1 > u0) local += pers_worker_of(u1 - 1, U, W) - pers_worker_of(u0, U, W) + 1;
     }
-    sm.part[tid] = local;
-    __syncthreads();
-    if (tid < 32) {
-        int carry = 0;
-        for (int base = 0; base < NT; base += 32) {
-            const int v = sm.part[base + tid];
-            int x = v;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, off);
-                if (tid >= off) x += y;
-            }
-            sm.part[base + tid] = carry + x - v;
-            carry += __shfl_sync(0xffffffffu, x, 31);
-        }
-        if (tid == 0) sm.u.rows.cstart[nchunks] = carry;
-    }
-    __syncthreads();
     {
-        int run = sm.part[tid];
+        int run = block_exclusive_scan<NT>(local, sm.part, &sm.u.rows.cstart[nchunks]);
         for (int c = c0; c < c1; ++c) {
-            const int cnt = sm.u.rows.cstart[c];
+            const int u0 = pfx[cb + c], u1 = pfx[cb + c + 1];
             sm.u.rows.cstart[c] = run;
-            run += cnt;
+            if (U > 0 && u1 > u0) run += pers_worker_of(u1 - 1, U, W) - pers_worker_of(u0, U, W) + 1;
         }
     }
     __syncthreads();
     const int R = sm.u.rows.cstart[nchunks];
-    // workspace row of flat row j (chunks with no rows never contain j)
+    // workspace row of flat row j (chunks with no rows never contain j): the
+    // first worker of chunk c writes row kbase + c + its worker index
     auto row_of = [&](int j) {
         int lo = 0, hi = nchunks;  // cstart[lo] <= j < cstart[hi]
         while (hi - lo > 1) {
@@ -186,8 +227,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
             if (sm.u.rows.cstart[mid] <= j) lo = mid;
             else hi = mid;
         }
-        return (long long)sm.u.rows.cbase[lo] + (j - sm.u.rows.cstart[lo]);
+        return (long long)(kbase + lo) + pers_worker_of(pfx[cb + lo], U, W) + (j - sm.u.rows.cstart[lo]);
     };
+    if (early) pdl_enter();  // what follows reads the split kernel's results
 
     // ---- 2. status rows (loaded now, used after the merge) and the rows ----
     uint32_t st[kCombShortList];
@@ -257,7 +299,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
     // chunks): the same gathering, a thread per segment
     for (int it = tid + NT; U > 0 && it < nseg; it += NT) {
         const int k = kseg0 + it;
-        const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];
+        const int u0 = pfx[it], u1 = pfx[it + 1];
         if (u1 == u0) continue;
         const int p0 = pers_worker_of(u0, U, W), p1 = pers_worker_of(u1 - 1, U, W);
         for (int p = p0; p <= p1; ++p) f |= a.status[k + p];
@@ -331,7 +373,7 @@ template <int G, int GS, int NW, int D>
 cudaError_t launch_comb_d(const DecodeArgs &a, const DecodePlan &p, cudaStream_t s) {
     const unsigned grid = (unsigned)(p.B * p.Hkv * (G / GS));
     return launch_pdl(decode_combine_pers_kernel<G, GS, NW, D>, dim3(grid), dim3(NW * 32), 0, s, a, p.Hkv,
-                      p.nchunks, p.workers, (const int *)a.ws_prefix);
+                      p.nchunks, p.chunk_tokens, p.workers, (const int *)a.ws_prefix);
 }
 
 template <int G, int GS, int NW>

@@ -265,11 +265,9 @@ __global__ void __launch_bounds__(PersCfg<WK, BF, HD>::NT, 1)
             n = query_len(a, b, h);
             nbh = bh;
         }
-        int units = 0, lastnv = 0;
+        const int units = segment_units(n, c, chunk_tokens);
+        int lastnv = 0;
         if (n >= 0) {
-            const int pages = (n + kPage - 1) / kPage;
-            const int cp = chunk_tokens / kPage;
-            units = max(0, min(pages, (c + 1) * cp) - c * cp);
             const int tok_end = min(n, (c + 1) * chunk_tokens);
             lastnv = tok_end - (tok_end - 1) / kPage * kPage;
         }
@@ -410,16 +408,6 @@ __global__ void __launch_bounds__(PersCfg<WK, BF, HD>::NT, 1)
         entry_load(bx + lane, e);
         entry_finish(e, entry_tag(e), phys, bad, req);
     };
-    // both halves of a window, every load of a round issued before any is used
-    auto load_ids2 = [&](int bx, int &phys0, uint32_t &bad0, int &req0, int &phys1, uint32_t &bad1,
-                         int &req1) {
-        Entry e0, e1;
-        entry_load(bx + lane, e0);
-        entry_load(bx + 32 + lane, e1);
-        const uint32_t t0 = entry_tag(e0), t1 = entry_tag(e1);
-        entry_finish(e0, t0, phys0, bad0, req0);
-        entry_finish(e1, t1, phys1, bad1, req1);
-    };
     // units of a request the validation kernel rejected are absent
     auto skip_rejected = [&](int req, int &phys, uint32_t &bad) {
         if (req >= 0 && sm.rflag[req]) {
@@ -437,7 +425,13 @@ __global__ void __launch_bounds__(PersCfg<WK, BF, HD>::NT, 1)
         }
     };
     int creq = -1, nreq = -1;
-    if (!idle) load_ids2(base, cphys, cbad, creq, nphys, nbad, nreq);
+    // the first window's table entries (both halves): loaded here, used after
+    // the wait below, so that their loads overlap those of the validation bits
+    Entry first0, first1;
+    if (!idle) {
+        entry_load(base + lane, first0);
+        entry_load(base + 32 + lane, first1);
+    }
     // metadata of unit x (in [base, base + 64)).  One uniform branch picks
     // the window half (a select would wait for the next half's loads even
     // when only the current one is read).
@@ -533,6 +527,11 @@ __global__ void __launch_bounds__(PersCfg<WK, BF, HD>::NT, 1)
     }
     __syncthreads();
     if (idle) return;  // no block-wide barrier follows
+    {
+        const uint32_t t0 = entry_tag(first0), t1 = entry_tag(first1);
+        entry_finish(first0, t0, cphys, cbad, creq);
+        entry_finish(first1, t1, nphys, nbad, nreq);
+    }
     // no page is read before its request has passed validation
     skip_rejected(creq, cphys, cbad);
     skip_rejected(nreq, nphys, nbad);

@@ -167,6 +167,16 @@ __device__ __forceinline__ uint32_t entry_bits(const DecodeArgs &a, int id, int 
 
 // Persistent layout: the worker of global unit x when U units are shared by W
 // workers (worker w takes units [ceil(wU/W), ceil((w+1)U/W))).
+// 16-token units of chunk c (chunk_tokens tokens each) of a head with n
+// tokens; none for a flagged length (n < 0).  The persistent split kernel and
+// its combine count units with this one function.
+__device__ __forceinline__ int segment_units(int n, int c, int chunk_tokens) {
+    if (n < 0) return 0;
+    const int pages = (n + kPage - 1) / kPage;
+    const int cp = chunk_tokens / kPage;
+    return max(0, min(pages, (c + 1) * cp) - c * cp);
+}
+
 __device__ __forceinline__ int pers_worker_of(long long x, long long U, int W) {
     return (int)((x * W) / U);
 }
@@ -226,11 +236,17 @@ cudaError_t preload_combine_pers();
 cudaError_t preload_split_generic();
 cudaError_t preload_mass();
 
-// Loads one kernel (a no-op if it is loaded already).
+// Loads one kernel (a no-op if it is loaded already) and gives it the
+// largest shared-memory carveout, the one the persistent split kernel runs
+// with: an SM then never changes its L1 / shared-memory split between the
+// kernels of a call, so a dependent launch's CTAs can become resident beside
+// the previous kernel's last CTAs instead of waiting for the SM to drain.
 template <typename F>
 cudaError_t preload_kernel(F *kernel) {
     cudaFuncAttributes attr;
-    return cudaFuncGetAttributes(&attr, kernel);
+    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return e;
 }
 
 // --------------------------------------------------------------------------
