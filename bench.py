@@ -476,31 +476,40 @@ def run_gpu(args):
 
 
 class E2EStepGraph:
-    """One end-to-end step as a CUDA graph: the host-to-device copy of the
-    step's packed inputs from pinned memory, the public pfkv_decode_step call
-    (or the attention call where the workload does not append), and the
-    device-to-host copy of the packed output (out and flags).  The object owns
-    the pinned host buffers the graph's copies read and write: they must live
-    as long as the graph is replayed."""
+    """One end-to-end step through the library's public API with host buffers:
+    a one-layer pfkv_step_graph (pfkv_decode_step, or the attention call where
+    the workload does not append) whose inputs (q, new K/V rows, positions,
+    lengths, block table, expected tags) and outputs (out, flags) live in
+    pinned host memory.  The kernels read and write those buffers directly
+    over the CPU-GPU link (no staging copy); the pools, scales, tags and
+    workspace stay in HBM.  The object owns the pinned buffers the graph
+    points at: they live as long as the graph."""
 
     def __init__(self, db, B, fused_tags):
         import torch
-        s = torch.cuda.Stream()
         self.h_in = db.io_in.detach().cpu().pin_memory()
-        self.h_out = torch.empty_like(db.io_out, device="cpu").pin_memory()
-        step = PreparedStep(db, B, s.cuda_stream, fused_tags=fused_tags)
-        with torch.cuda.stream(s):  # warm the call on the capture stream
-            step.full_step()
-        torch.cuda.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph, stream=s):
-            db.io_in.copy_(self.h_in, non_blocking=True)
-            step.full_step()
-            self.h_out.copy_(db.io_out, non_blocking=True)
-        torch.cuda.synchronize()
+        self.h_out = torch.zeros_like(db.io_out, device="cpu").pin_memory()
+        hin = lambda t: self.h_in.data_ptr() + (t.data_ptr() - db.io_in.data_ptr())
+        hout = lambda t: self.h_out.data_ptr() + (t.data_ptr() - db.io_out.data_ptr())
+        sb, sh = db.batch.len_strides
+        tb, th = db.batch.bt_strides
+        tags = db.pages.expected_tags
+        self.pages = B.Pages(db.spec.B, db.batch.max_pages, hin(db.block_tables), tb, th,
+                             hin(db.seq_lens), sb, sh, None if tags is None else hin(tags))
+        appends = db.spec.append
+        self.layer = B.Layer(db.cache, hin(db.q), hout(db.out),
+                             hin(db.k_new) if appends else None, hin(db.v_new) if appends else None,
+                             hout(db.flags))
+        self.graph = B.pfkv_step_graph_create(
+            [self.layer], self.pages, hin(db.positions) if appends else None, None, 1,
+            db.append_flags if appends else None, db.spec.Hq, db.spec.sm_scale, db.split_tokens,
+            db.max_seq_len, db.workspace, B.PFKV_STAGE_FUSED_TAGS if fused_tags else 0)
+        self.B = B
+        self.stream = torch.cuda.current_stream(db.q.device)
+        self.out_offset = db.out.data_ptr() - db.io_out.data_ptr()
 
     def replay(self):
-        self.graph.replay()
+        self.B.pfkv_step_graph_launch(self.graph, self.stream)
 
 
 def e2e_bytes(db):
@@ -512,9 +521,10 @@ def e2e_bytes(db):
     return int(h2d), int(d2h)
 
 
-E2E_API = ("every step: one replay of a CUDA graph holding the host-to-device copy of "
-           "the packed inputs (pinned host memory), the public pfkv_decode_step call and "
-           "the device-to-host copy of the packed outputs; then a stream synchronize")
+E2E_API = ("every step: pfkv_step_graph_launch of a one-layer step graph (pfkv_decode_step) "
+           "whose inputs (q, new K/V rows, positions, lengths, block table, expected tags) and "
+           "outputs (out, flags) are pinned host memory that the kernels read and write "
+           "directly over NVLink-C2C, no staging copy; then a stream synchronize")
 
 
 def run_e2e(args, reps, B, stream, step_bytes, world, dev):

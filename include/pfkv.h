@@ -19,11 +19,18 @@
  *    aborted, and with checking disabled a no-op tracker costs nothing.
  *
  * Conventions for every call:
- *  - Memory: every pointer argument not marked "host" is DEVICE memory owned
- *    by the caller.  The library never allocates device memory for data and
- *    keeps no state between calls, except the step-graph objects that a caller
- *    creates and destroys explicitly (CUDA graphs, a driver resource); calls on
- *    different streams are independent.
+ *  - Memory: every pointer argument not marked "host" is memory the GPU can
+ *    address, owned by the caller: device memory, or host memory the device
+ *    maps (pinned with cudaHostAlloc / cudaHostRegister, or any host memory on
+ *    a system with a coherent CPU-GPU link such as Grace + NVLink-C2C).  The
+ *    kernels read and write host memory directly, without a staging copy:
+ *    per-step inputs and outputs (q, new K/V rows, positions, lengths, block
+ *    tables, expected tags, out, flags) may live there; the pools, scales,
+ *    tags and workspace belong in HBM, which the kernels stream.  The library
+ *    never allocates device memory for data and keeps no state between calls,
+ *    except the step-graph objects that a caller creates and destroys
+ *    explicitly (CUDA graphs, a driver resource); calls on different streams
+ *    are independent.
  *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
  *    work is enqueued asynchronously on it; no call synchronises the host.
  *  - Alignment: k_pages, v_pages, q, out, k_new and v_new 16-byte aligned;
@@ -189,7 +196,16 @@ pfkv_status pfkv_decode_workspace_size(const pfkv_cache *cache, const pfkv_pages
  * For each (b, hq) with h = hq / G and n = seq_lens(b, h):
  *   out = sum_j softmax_j(sm_scale * q . k_j) v_j over tokens j < n, where
  *   token j is slot j % 16 of unit (block_tables[b,h,j/16], h) and FP8 values
- *   are e4m3 value x unit scale.  Computed in fp32, rounded to bf16.
+ *   are e4m3 value x unit scale, rounded to bf16.  Arithmetic: the two
+ *   products run on the tensor cores with fp32 accumulation.  FP8 pools:
+ *   e4m3 values are exact in f16; q enters as f16 after a power-of-two
+ *   scaling (exact for every element within 2^14 of its largest); each
+ *   softmax weight (times the unit's V scale over a power-of-two reference)
+ *   enters as a pair of f16 values whose sum is within 2^-22 of it
+ *   (relative; 2^-25 absolute where the low part is subnormal).  BF16 pools:
+ *   K, V and q are exact in bf16 and each weight is a pair of bf16 values
+ *   whose sum is within 2^-18 of it.  Scores, the running max and sums, and
+ *   the merge of partial results are fp32.
  * out is zero for a zero-length head and for every head of a flagged request.
  * When page_tags is non-NULL every live entry's pool tag is compared with the
  * expected tag before any page of the batch is read (a separate validation

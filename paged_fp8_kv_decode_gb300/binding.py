@@ -228,12 +228,14 @@ class Pages:
 
 
 def _ptr(t) -> Optional[int]:
+    """Address of a device tensor, or of a pinned host tensor (which the
+    kernels read and write directly over the CPU-GPU link)."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
-    if not t.is_cuda:
-        raise ValueError("device tensor expected")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("device tensor or pinned host tensor expected")
     return t.data_ptr()
 
 
