@@ -424,6 +424,48 @@ def run_gpu(args):
     split_gbs = split_bytes / split_avg / 1e9
     peak, peak_kind = peaks()
 
+    # The same split stage on the per-chunk CUDA-core kernels, for comparison
+    # with the tensor-core kernel (PFKV_STAGE_CUDA_CORES; a workspace of its own).
+    cuda_core = None
+    CC = B.PFKV_STAGE_CUDA_CORES
+    for p in reps:
+        p.args_tc = p.args
+
+    def use(p, ws):
+        a = list(p.args_tc)
+        if ws is not None:
+            a[7], a[8] = ws.data_ptr(), ws.numel()
+        p.args = tuple(a)
+    try:
+        ws_cc = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+        for p in reps:  # warm the CUDA-core kernels on every replica
+            use(p, ws_cc)
+            p.stage(S_V | CC), p.stage(S_S | CC), p.stage(S_C | CC)
+        KC = max(len(reps), min(KS, 1000))
+        ev_cc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(KC)]
+        gpu_hold(stream)
+        for i in range(KC):
+            p = reps[i % len(reps)]
+            p.append()
+            p.stage(S_V | CC)
+            ev_cc[i][0].record(stream)
+            p.stage(S_S | CC)
+            ev_cc[i][1].record(stream)
+            p.stage(S_C | CC)
+        torch.cuda.synchronize()
+        cc_avg = sum(a.elapsed_time(b) for a, b in ev_cc) / KC / 1e3
+        cuda_core = {"kernel": "decode_split_kernel (per-chunk CTAs, e4m3 dequantised to fp32 in "
+                               "registers, fp32 FMAs, no tensor cores)",
+                     "achieved": round(split_bytes / cc_avg / 1e9, 1), "unit": "GB/s",
+                     "frac": round(split_bytes / cc_avg / 1e9 / peak, 4),
+                     "avg_launch_us": round(cc_avg * 1e6, 3), "timed_launches": KC}
+    except RuntimeError as e:  # a workspace too small for the per-chunk plan
+        cuda_core = {"unavailable": str(e)}
+    finally:
+        for p in reps:
+            use(p, None)
+
     # check the last step's flags (no request should be flagged in this workload)
     for p in reps:
         if int(p.db.flags[:spec0.B].sum()) or int(p.db.append_flags[:spec0.B].sum()):
@@ -467,6 +509,7 @@ def run_gpu(args):
                          "peak_kind": peak_kind, "avg_launch_us": round(split_avg * 1e6, 3),
                          "bytes_per_launch": int(split_bytes),
                          "timed_launches": len(split_ms)},
+            "cuda_core_split": cuda_core,
             "e2e": e2e, "gpu_launches": 3 * K,
             "clocks": clocks, "cpu_baseline": cpu,
         }

@@ -227,6 +227,13 @@ pfkv_status pfkv_paged_decode_attn(const pfkv_cache *cache, const pfkv_pages *pa
  * tag comparison runs inside the SPLIT stage's page loop, as in
  * pfkv_paged_decode_attn_fused_tags, and VALIDATE launches nothing. */
 #define PFKV_STAGE_FUSED_TAGS 0x8u
+/* Not a stage either: with it SPLIT and COMBINE run the per-chunk CUDA-core
+ * kernels (e4m3 dequantised to fp32 in registers, fp32 FMAs, no tensor cores)
+ * for every shape, instead of the persistent tensor-core kernel.  The result
+ * is the same computation within the tolerance; the option exists to measure
+ * the two designs against each other.  Its workspace can be larger than
+ * pfkv_decode_workspace_size reports (PFKV_ERR_WORKSPACE if too small). */
+#define PFKV_STAGE_CUDA_CORES 0x10u
 
 /*
  * pfkv_paged_decode_attn_stages -- the same computation as

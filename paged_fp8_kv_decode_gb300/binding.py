@@ -40,6 +40,7 @@ PFKV_STAGE_SPLIT = 0x2
 PFKV_STAGE_COMBINE = 0x4
 PFKV_STAGE_ALL = 0x7
 PFKV_STAGE_FUSED_TAGS = 0x8
+PFKV_STAGE_CUDA_CORES = 0x10
 
 # every symbol include/pfkv.h declares
 EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_attn",

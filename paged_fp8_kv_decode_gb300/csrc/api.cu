@@ -161,7 +161,7 @@ pfkv_status append_args(const pfkv_cache *cache, const pfkv_pages *pages, const 
 
 pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_heads,
                       int32_t split_tokens, int32_t max_seq_len, int num_sms, DecodePlan *plan,
-                      bool mass = false, int32_t kq = 1) {
+                      bool mass = false, int32_t kq = 1, bool cuda_cores = false) {
     const pfkv_status st = check_decode_args(c, num_q_heads, split_tokens, max_seq_len);
     if (st != PFKV_OK) return st;
     if (kq < 1 || (long long)p->batch * kq > 0x7fffffffLL) return PFKV_ERR_INVALID_ARG;
@@ -182,7 +182,7 @@ pfkv_status make_plan(const pfkv_cache *c, const pfkv_pages *p, int32_t num_q_he
     // the caller's) when a launch's segments would not fit the kernels'
     // tables, and a batch whose (request, kv head) pairs alone would not fit
     // runs as several launches of whole requests.
-    q.kind = pers_supported(q) && (long long)kq * q.Hkv <= kPersMaxSegments ? 1 : 0;
+    q.kind = !cuda_cores && pers_supported(q) && (long long)kq * q.Hkv <= kPersMaxSegments ? 1 : 0;
     if (q.kind == 1) {
         q.greq = (int)min((long long)q.Breq,
                           min((long long)kPersMaxRequests, (long long)(kPersMaxSegments / (kq * q.Hkv))));
@@ -341,7 +341,8 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
                       uint8_t *flags, uint32_t stages, const MassOut *mass, void *stream,
                       int32_t kq = 1, const AppendArgs *app = nullptr) {
     if (kq < 1 || (mass && kq != 1)) return kq < 1 ? PFKV_ERR_INVALID_ARG : PFKV_ERR_UNSUPPORTED;
-    if ((stages & PFKV_STAGE_ALL) == 0 || (stages & ~(PFKV_STAGE_ALL | PFKV_STAGE_FUSED_TAGS)))
+    if ((stages & PFKV_STAGE_ALL) == 0 ||
+        (stages & ~(PFKV_STAGE_ALL | PFKV_STAGE_FUSED_TAGS | PFKV_STAGE_CUDA_CORES)))
         return PFKV_ERR_INVALID_ARG;
     const bool fused = (stages & PFKV_STAGE_FUSED_TAGS) != 0;
     pfkv_status st = check_cache(cache);
@@ -362,7 +363,7 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
     if (st != PFKV_OK) return st;
     DecodePlan plan;
     st = make_plan(cache, pages, num_q_heads, split_tokens, max_seq_len, sms, &plan,
-                   mass != nullptr, kq);
+                   mass != nullptr, kq, (stages & PFKV_STAGE_CUDA_CORES) != 0);
     if (st != PFKV_OK) return st;
     if (workspace_bytes < plan.total) return PFKV_ERR_WORKSPACE;
 

@@ -119,8 +119,8 @@ def test_host_rejects_bad_call_arguments(B):
 def test_stage_mask_is_checked(B):
     c, p = _structs(B)
     L = B.lib()
-    # no stage bit (the fused-tag option alone counts as none), or an unknown bit
-    for mask in (0, 8, 0x17, 0x18):
+    # no stage bit (the option bits alone count as none), or an unknown bit
+    for mask in (0, 8, 0x10, 0x18, 0x27, 0x20):
         assert L.pfkv_paged_decode_attn_stages(ctypes.byref(c), ctypes.byref(p), 0xA0000, 4, 0.125,
                                                0, 64, 0xB0000, 1 << 30, 0xC0000, None, mask,
                                                None) == 1
@@ -267,7 +267,7 @@ def test_binding_constants_match_the_header(B):
     for name in ("PFKV_PAGE_SIZE", "PFKV_FLAG_TAG_MISMATCH", "PFKV_FLAG_BAD_PAGE",
                  "PFKV_FLAG_BAD_LENGTH", "PFKV_FLAG_DEVICE_TIMEOUT", "PFKV_STAGE_VALIDATE",
                  "PFKV_STAGE_SPLIT", "PFKV_STAGE_COMBINE", "PFKV_STAGE_ALL", "PFKV_STAGE_FUSED_TAGS",
-                 "PFKV_NOALLOC_WORKSPACE_BYTES"):
+                 "PFKV_STAGE_CUDA_CORES", "PFKV_NOALLOC_WORKSPACE_BYTES"):
         assert getattr(B, name) == _header_macro(name), name
     assert B.PFKV_NOALLOC_WORKSPACE_BYTES == 16 << 20
 

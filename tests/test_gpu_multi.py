@@ -119,3 +119,26 @@ def test_one_query_token_equals_the_plain_call(B):
     db.attend()
     torch.cuda.synchronize()
     assert torch.equal(db.out, out[:, 0])
+
+
+@pytest.mark.parametrize("kv_dtype,D", [("fp8", 128), ("bf16", 128), ("fp8", 64)])
+def test_cuda_core_option_matches_the_oracle(B, kv_dtype, D):
+    """PFKV_STAGE_CUDA_CORES runs the per-chunk CUDA-core kernels for a shape
+    the tensor-core kernel would take; the result matches the oracle too."""
+    from paged_fp8_kv_decode_gb300.device_batch import DeviceBatch
+    base = W.spec_sweep(5, kv_dtype, scale="small")
+    spec = dataclasses.replace(base, D=D, Hkv=4, Hq=16, lens=np.array([1000, 37, 512, 16, 700], np.int32))
+    batch = W.make_batch(spec)
+    db = DeviceBatch(batch, keep_rows=True)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(db.out)
+    B.pfkv_paged_decode_attn_stages(db.cache, db.pages, db.q, spec.sm_scale, 0, db.max_seq_len, ws, out,
+                                    db.flags, B.PFKV_STAGE_ALL | B.PFKV_STAGE_CUDA_CORES)
+    torch.cuda.synchronize()
+    k, v, ks, vs = fill_pool(spec, batch, W.bf16_bits(db.k_rows), W.bf16_bits(db.v_rows))
+    cache = cache_dict(spec, batch, k, v, ks, vs)
+    pages = pages_dict(spec, batch, batch.seq_lens)
+    ref, rflags = oracle.paged_decode_multi(cache, pages, W.bf16_bits(db.q[:, None]), spec.Hq, 1,
+                                            spec.sm_scale, db.max_seq_len)
+    assert np.array_equal(db.flags.cpu().numpy()[:spec.B], rflags)
+    assert_outputs_close(out, ref[:, 0], f"cuda cores {kv_dtype} D{D}")
