@@ -334,24 +334,8 @@ __global__ void __launch_bounds__(PersCfg<WK, BF, HD>::NT, 1)
             c.seg_end = min(sm.prefix[c.k + 1], x1);
         }
     };
-    int ngran = 0;
-    if (!idle) {
-        int x = x0;
-        int k = seg_of(sm.prefix, K, x);
-        while (x < x1) {
-            const int e = min(sm.prefix[k + 1], x1);
-            ngran += (e - x + C::GU - 1) / C::GU;
-            x = e;
-            ++k;
-            while (k < K && sm.prefix[k + 1] == sm.prefix[k]) ++k;
-        }
-    }
-    if (!idle && lane == 0) {
-        for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    const uint64_t policy = l2_policy_evict_first();
+    int ngran = 0;        // granules of the worker's range, counted below
+    uint64_t policy = 0;  // L2 policy of the copies, made below
 
     // unit metadata window: lane l holds unit base + l (cur) and base + 32 + l
     // (nxt): unit index (-1 bad, -2 absent), the two scales and the bad bits
@@ -512,6 +496,25 @@ __global__ void __launch_bounds__(PersCfg<WK, BF, HD>::NT, 1)
     uint32_t qb0[C::KS], qb1[C::KS];
     float qmul = 0.f;
     if (!idle) q_fetch(con.k);
+    // what the first copies need but no load waits for: done while the
+    // table-entry and query loads above are in flight
+    if (!idle) {
+        int x = x0;
+        int k = seg_of(sm.prefix, K, x);
+        while (x < x1) {
+            const int e = min(sm.prefix[k + 1], x1);
+            ngran += (e - x + C::GU - 1) / C::GU;
+            x = e;
+            ++k;
+            while (k < K && sm.prefix[k + 1] == sm.prefix[k]) ++k;
+        }
+    }
+    if (!idle && lane == 0) {
+        for (int s = 0; s < ST; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    policy = l2_policy_evict_first();
 
     // ---------------- after the previous kernels: validation bits ----------------
     if (a.early) pdl_enter();
