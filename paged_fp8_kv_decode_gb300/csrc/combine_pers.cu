@@ -217,9 +217,14 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
         }
     }
     __syncthreads();
+    // Each chunk's first workspace row (its first worker writes row
+    // kbase + c + the worker's index), written over the chunk's unit prefix,
+    // which nothing reads any more: one division per chunk, not per row.
+    int *crow = pfx + cb;
+    for (int c = c0; c < c1; ++c) crow[c] = kbase + c + (U > 0 ? pers_worker_of(crow[c], U, W) : 0);
+    __syncthreads();
     const int R = sm.u.rows.cstart[nchunks];
-    // workspace row of flat row j (chunks with no rows never contain j): the
-    // first worker of chunk c writes row kbase + c + its worker index
+    // workspace row of flat row j (chunks with no rows never contain j)
     auto row_of = [&](int j) {
         int lo = 0, hi = nchunks;  // cstart[lo] <= j < cstart[hi]
         while (hi - lo > 1) {
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
             if (sm.u.rows.cstart[mid] <= j) lo = mid;
             else hi = mid;
         }
-        return (long long)(kbase + lo) + pers_worker_of(pfx[cb + lo], U, W) + (j - sm.u.rows.cstart[lo]);
+        return (long long)crow[lo] + (j - sm.u.rows.cstart[lo]);
     };
     if (early) pdl_enter();  // what follows reads the split kernel's results
 
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_combine_pers_kernel(D
     // chunks): the same gathering, a thread per segment
     for (int it = tid + NT; U > 0 && it < nseg; it += NT) {
         const int k = kseg0 + it;
-        const int u0 = pfx[it], u1 = pfx[it + 1];
+        const int u0 = ws_prefix[k], u1 = ws_prefix[k + 1];  // pfx now holds chunk rows
         if (u1 == u0) continue;
         const int p0 = pers_worker_of(u0, U, W), p1 = pers_worker_of(u1 - 1, U, W);
         for (int p = p0; p <= p1; ++p) f |= a.status[k + p];

@@ -236,17 +236,11 @@ cudaError_t preload_combine_pers();
 cudaError_t preload_split_generic();
 cudaError_t preload_mass();
 
-// Loads one kernel (a no-op if it is loaded already) and gives it the
-// largest shared-memory carveout, the one the persistent split kernel runs
-// with: an SM then never changes its L1 / shared-memory split between the
-// kernels of a call, so a dependent launch's CTAs can become resident beside
-// the previous kernel's last CTAs instead of waiting for the SM to drain.
+// Loads one kernel (a no-op if it is loaded already).
 template <typename F>
 cudaError_t preload_kernel(F *kernel) {
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    return e;
+    return cudaFuncGetAttributes(&attr, kernel);
 }
 
 // --------------------------------------------------------------------------
