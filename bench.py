@@ -34,6 +34,7 @@ timed interval of each step.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import ctypes
 import json
 import math
@@ -83,6 +84,7 @@ def parse_args(argv=None):
                          "and attend with all of them, causally (pfkv_paged_decode_attn_multi)")
     ap.add_argument("--batch", type=int, default=32, help="sweep: batch size")
     ap.add_argument("--kv-dtype", default="fp8", choices=["fp8", "bf16"], help="sweep: pool dtype")
+    ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128], help="sweep: head_dim")
     return ap.parse_args(argv)
 
 
@@ -726,7 +728,8 @@ def workload_spec(args, rank: int = 0):
     if args.workload == "long":
         return W.spec_long("full", seed=seed)
     if args.workload == "sweep":
-        return W.spec_sweep(args.batch, args.kv_dtype, seed=seed)
+        spec = W.spec_sweep(args.batch, args.kv_dtype, seed=seed)
+        return dataclasses.replace(spec, D=args.head_dim) if args.head_dim != spec.D else spec
     if args.workload == "evict":
         return W.spec_evict("full", seed=seed)
     return W.spec_llama8b("full", seed=seed)
@@ -779,6 +782,8 @@ def run_workload(args):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     spec = workload_spec(args, rank)
+    if args.split:  # a caller's fixed split size instead of the workload's
+        spec.split_tokens = args.split
     db = DeviceBatch(W.make_batch(spec), device=dev)
     db.pack_step_io()  # one host-to-device and one device-to-host copy per e2e step
     variants = [("tags" if spec.tags else "no_tags", PreparedStep(db, B, sh), spec.tags)]

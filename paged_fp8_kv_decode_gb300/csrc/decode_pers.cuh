@@ -169,10 +169,12 @@ constexpr int kNoScale = -1000; // V-scale reference of a worker that has seen n
 }  // namespace
 
 // Kernel shape: worker warps per CTA, ring stages per worker, and units per
-// granule (one ring stage: two FP8 units or one BF16 unit, 8 KB at head_dim
-// 128 and 4 KB at 64).  Two worker counts are built, both with 192 KB of
-// rings: 8 workers x 24 KB, and 12 workers x 16 KB, which hides more latency
-// when every worker streams long runs (see pers_workers_for).
+// granule.  A ring stage (granule) is 8 KB: two FP8 units or one BF16 unit at
+// head_dim 128, four FP8 or two BF16 units at 64 (where per-token work weighs
+// twice as much per byte, and a granule's fixed work is spread over more
+// tokens).  Two worker counts are built, both with 192 KB of rings: 8 workers
+// x 3 stages, and 12 workers x 2 stages, which hides more latency when every
+// worker streams long runs (see pers_workers_for).
 template <int WK, bool BF, int HD>
 struct PersCfg {
     static_assert(WK == 8 || WK == 12, "8 or 12 workers per CTA");
@@ -180,10 +182,11 @@ struct PersCfg {
     static constexpr int D = HD;
     static constexpr int ROWB = D * (BF ? 2 : 1);  // one token row of a slab
     static constexpr int UNITB = kPage * ROWB;     // FP8 2 KB / 1 KB, BF16 4 KB / 2 KB
-    static constexpr int GU = BF ? 1 : 2;
+    static constexpr int GU = (BF ? 1 : 2) * (128 / HD);
     static constexpr int STAGEB = 2 * GU * UNITB;  // K u0 .. K u(GU-1) | V u0 .. V u(GU-1)
     static constexpr int WORKERS = WK;
-    static constexpr int STAGES = (WK == 8 ? 3 : 2) * (8192 / STAGEB);
+    static constexpr int STAGES = WK == 8 ? 3 : 2;
+    static_assert(STAGEB == 8192, "8 KB granules");
     static constexpr int KS = D / 16;  // k-steps of the score MMAs (the dims)
     static constexpr int MT = D / 16;  // m-tiles of the value MMAs (the dims)
     static constexpr int QW = D / 32;  // 16-byte words of a lane's query dims
