@@ -33,6 +33,10 @@ def test_workload_spec_names_and_sizes():
     assert s.per_head and s.lens.shape == (16, 8) and s.stale_per_mille == 1.0
     s = bench.workload_spec(bench.parse_args([]))
     assert s.name == "llama8b" and s.B == 32 and s.append
+    s = bench.workload_spec(bench.parse_args(["--workload", "sweep", "--head-dim", "64"]))
+    assert s.D == 64 and s.Hq == 32 and int(s.lens[0]) == 32768
+    # an admissible batch counts the head dim: half the bytes per token at 64
+    assert bench.sweep_admissible(s) == 74
 
 
 def test_sample_shape_bounds_the_oracle_work():
