@@ -521,40 +521,38 @@ def run_gpu(args):
 
 
 class E2EStepGraph:
-    """One end-to-end step through the library's public API with host buffers:
-    a one-layer pfkv_step_graph (pfkv_decode_step, or the attention call where
-    the workload does not append) whose inputs (q, new K/V rows, positions,
-    lengths, block table, expected tags) and outputs (out, flags) live in
-    pinned host memory.  The kernels read and write those buffers directly
-    over the CPU-GPU link (no staging copy); the pools, scales, tags and
-    workspace stay in HBM.  The object owns the pinned buffers the graph
-    points at: they live as long as the graph."""
+    """One end-to-end step through the library's public API with host buffers,
+    as one CUDA graph of two calls: pfkv_stage_copy of the step's packed inputs
+    (q, new K/V rows, positions, lengths, block table, expected tags) from
+    pinned host memory into device memory (a copy kernel over the CPU-GPU
+    link), then pfkv_decode_step (or the attention call where the workload does
+    not append), whose kernels write out and flags straight into pinned host
+    memory.  The object owns the pinned buffers the graph reads and writes:
+    they live as long as the graph."""
 
     def __init__(self, db, B, fused_tags):
         import torch
+        s = torch.cuda.Stream()
         self.h_in = db.io_in.detach().cpu().pin_memory()
         self.h_out = torch.zeros_like(db.io_out, device="cpu").pin_memory()
-        hin = lambda t: self.h_in.data_ptr() + (t.data_ptr() - db.io_in.data_ptr())
         hout = lambda t: self.h_out.data_ptr() + (t.data_ptr() - db.io_out.data_ptr())
-        sb, sh = db.batch.len_strides
-        tb, th = db.batch.bt_strides
-        tags = db.pages.expected_tags
-        self.pages = B.Pages(db.spec.B, db.batch.max_pages, hin(db.block_tables), tb, th,
-                             hin(db.seq_lens), sb, sh, None if tags is None else hin(tags))
-        appends = db.spec.append
-        self.layer = B.Layer(db.cache, hin(db.q), hout(db.out),
-                             hin(db.k_new) if appends else None, hin(db.v_new) if appends else None,
-                             hout(db.flags))
-        self.graph = B.pfkv_step_graph_create(
-            [self.layer], self.pages, hin(db.positions) if appends else None, None, 1,
-            db.append_flags if appends else None, db.spec.Hq, db.spec.sm_scale, db.split_tokens,
-            db.max_seq_len, db.workspace, B.PFKV_STAGE_FUSED_TAGS if fused_tags else 0)
-        self.B = B
-        self.stream = torch.cuda.current_stream(db.q.device)
-        self.out_offset = db.out.data_ptr() - db.io_out.data_ptr()
+        step = PreparedStep(db, B, s.cuda_stream, fused_tags=fused_tags)
+        a = list(step.args)
+        a[9], a[10] = hout(db.out), hout(db.flags)  # out and flags: host memory
+        step.args = tuple(a)
+        n = db.io_in.numel()
+        with torch.cuda.stream(s):  # warm both calls on the capture stream
+            B.pfkv_stage_copy(db.io_in, self.h_in, n, s)
+            step.full_step()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s):
+            B.pfkv_stage_copy(db.io_in, self.h_in, n, s)
+            step.full_step()
+        torch.cuda.synchronize()
 
     def replay(self):
-        self.B.pfkv_step_graph_launch(self.graph, self.stream)
+        self.graph.replay()
 
 
 def e2e_bytes(db):
@@ -566,10 +564,11 @@ def e2e_bytes(db):
     return int(h2d), int(d2h)
 
 
-E2E_API = ("every step: pfkv_step_graph_launch of a one-layer step graph (pfkv_decode_step) "
-           "whose inputs (q, new K/V rows, positions, lengths, block table, expected tags) and "
-           "outputs (out, flags) are pinned host memory that the kernels read and write "
-           "directly over NVLink-C2C, no staging copy; then a stream synchronize")
+E2E_API = ("every step: one replay of a CUDA graph of two public calls, pfkv_stage_copy of the "
+           "packed inputs (q, new K/V rows, positions, lengths, block table, expected tags) from "
+           "pinned host memory into device memory (a copy kernel over NVLink-C2C), then "
+           "pfkv_decode_step, whose kernels write out and flags straight into pinned host "
+           "memory; then a stream synchronize")
 
 
 def run_e2e(args, reps, B, stream, step_bytes, world, dev):

@@ -50,7 +50,7 @@ EXPORTED = ("pfkv_kv_append", "pfkv_decode_workspace_size", "pfkv_paged_decode_a
             "pfkv_decode_mass_workspace_size", "pfkv_paged_decode_attn_multi",
             "pfkv_decode_multi_workspace_size", "pfkv_step_graph_create", "pfkv_step_graph_launch",
             "pfkv_step_graph_destroy", "pfkv_selftest_bounded_wait", "pfkv_e4m3_encode", "pfkv_e4m3_decode", "pfkv_status_string",
-            "pfkv_abi_version", "pfkv_flags_status")
+            "pfkv_abi_version", "pfkv_flags_status", "pfkv_stage_copy")
 
 
 class PfkvError(RuntimeError):
@@ -156,6 +156,8 @@ def lib() -> ctypes.CDLL:
         L.pfkv_abi_version.restype = ctypes.c_int32
         L.pfkv_flags_status.argtypes = [P, I32]
         L.pfkv_flags_status.restype = ctypes.c_int
+        L.pfkv_stage_copy.argtypes = [P, P, ctypes.c_size_t, P]
+        L.pfkv_stage_copy.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -166,6 +168,15 @@ def pfkv_status_string(status: int) -> str:
 
 def pfkv_abi_version() -> int:
     return int(lib().pfkv_abi_version())
+
+
+def pfkv_stage_copy(dst, src, nbytes: Optional[int] = None, stream=None) -> None:
+    """Copy ``nbytes`` (default: all of ``src``) from ``src`` to ``dst`` with a
+    kernel; each a device tensor, a pinned host tensor or an address."""
+    if nbytes is None:
+        nbytes = src.numel() * src.element_size()
+    _check(lib().pfkv_stage_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream)),
+           "pfkv_stage_copy")
 
 
 def pfkv_flags_status(flags) -> int:

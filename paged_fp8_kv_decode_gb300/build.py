@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libpfkv.so")
 SOURCES = ["api.cu", "append.cu", "decode.cu", "decode_pers.cu", "decode_pers_d64.cu", "combine_pers.cu",
-           "decode_noalloc.cu", "graph.cu", "mass.cu", "selftest.cu"]
+           "decode_noalloc.cu", "graph.cu", "mass.cu", "selftest.cu", "stage.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

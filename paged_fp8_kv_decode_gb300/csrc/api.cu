@@ -45,6 +45,7 @@ pfkv_status device_check(int *num_sms) {
             if (e == cudaSuccess) e = preload_combine_pers();
             if (e == cudaSuccess) e = preload_split_generic();
             if (e == cudaSuccess) e = preload_mass();
+            if (e == cudaSuccess) e = preload_stage();
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 return PFKV_ERR_CUDA;
@@ -448,6 +449,20 @@ pfkv_status attn_impl(const pfkv_cache *cache, const pfkv_pages *pages, const vo
 }  // namespace
 
 extern "C" {
+
+pfkv_status pfkv_stage_copy(void *dst, const void *src, size_t bytes, void *stream) {
+    if (bytes == 0) return PFKV_OK;
+    if (!dst || !src) return PFKV_ERR_INVALID_ARG;
+    if (!aligned(dst, 16) || !aligned(src, 16) || (bytes & 15u)) return PFKV_ERR_ALIGNMENT;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), r = reinterpret_cast<uintptr_t>(src);
+    if (d < r + bytes && r < d + bytes) return PFKV_ERR_INVALID_ARG;  // overlapping ranges
+    int sms = 0;
+    const pfkv_status st = device_check(&sms);
+    if (st != PFKV_OK) return st;
+    return launch_stage_copy(dst, src, bytes, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PFKV_OK
+               : PFKV_ERR_CUDA;
+}
 
 pfkv_status pfkv_decode_step(const pfkv_cache *cache, const pfkv_pages *pages,
                              const int32_t *positions, const int32_t *new_lens, int32_t num_new_tokens,

@@ -235,6 +235,8 @@ cudaError_t preload_split_pers_d64();
 cudaError_t preload_combine_pers();
 cudaError_t preload_split_generic();
 cudaError_t preload_mass();
+cudaError_t preload_stage();
+cudaError_t launch_stage_copy(void *dst, const void *src, size_t bytes, int num_sms, cudaStream_t s);
 
 // Loads one kernel (a no-op if it is loaded already).
 template <typename F>

@@ -37,7 +37,7 @@ def test_header_declares_the_entry_points():
                             "pfkv_paged_decode_attn_noalloc", "pfkv_paged_decode_attn_stages",
                             "pfkv_status_string", "pfkv_selftest_bounded_wait", "pfkv_step_graph_create",
                             "pfkv_step_graph_destroy", "pfkv_step_graph_launch",
-                            "pfkv_flags_status"])
+                            "pfkv_flags_status", "pfkv_stage_copy"])
 
 
 def test_library_exports_every_declared_symbol(B):
@@ -292,3 +292,15 @@ def test_flags_status_turns_device_timeouts_into_a_status(B):
     buf[3] = B.PFKV_FLAG_DEVICE_TIMEOUT
     assert L.pfkv_flags_status(buf.ctypes.data, 3) == B.PFKV_OK
     assert L.pfkv_flags_status(buf.ctypes.data, 4) == B.PFKV_ERR_DEVICE
+
+
+def test_stage_copy_checks_arguments_before_any_cuda_call(B):
+    L = B.lib()
+    assert L.pfkv_stage_copy(None, None, 0, None) == B.PFKV_OK          # nothing to copy
+    assert L.pfkv_stage_copy(None, 0x10000, 64, None) == B.PFKV_ERR_INVALID_ARG
+    assert L.pfkv_stage_copy(0x20000, None, 64, None) == B.PFKV_ERR_INVALID_ARG
+    assert L.pfkv_stage_copy(0x20008, 0x10000, 64, None) == B.PFKV_ERR_ALIGNMENT
+    assert L.pfkv_stage_copy(0x20000, 0x10000, 40, None) == B.PFKV_ERR_ALIGNMENT
+    assert L.pfkv_stage_copy(0x10020, 0x10000, 64, None) == B.PFKV_ERR_INVALID_ARG  # overlap
+    # valid arguments reach the device check: no GPU here
+    assert L.pfkv_stage_copy(0x20000, 0x10000, 64, None) in (B.PFKV_ERR_CUDA, B.PFKV_ERR_UNSUPPORTED)

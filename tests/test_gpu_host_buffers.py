@@ -4,7 +4,8 @@ memory, which the kernels read and write directly (no staging copy), gives
 the same bytes as the call with device buffers: outputs, flags and the pool
 after the append.  Covers pfkv_decode_step (separate and fused tag check),
 the attention call on per-head tables, a BF16 pool, and a step graph whose
-buffers are host memory."""
+buffers are host memory; and pfkv_stage_copy, which stages a step's packed
+host inputs into device memory with a kernel."""
 import dataclasses
 
 import pytest
@@ -124,3 +125,45 @@ def test_step_graph_with_host_buffers(B):
         for a, b in zip(got_pool, _pool(db)):
             assert torch.equal(a, b), rnd
     g.close()
+
+
+def test_stage_copy_moves_bytes_between_host_and_device(B):
+    g = torch.Generator().manual_seed(3)
+    n = (1 << 20) + 48  # a multiple of 16, not of the kernel's grid
+    host = torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8).pin_memory()
+    dev = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    B.pfkv_stage_copy(dev, host)
+    back = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    dev2 = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    B.pfkv_stage_copy(dev2, dev)         # device to device
+    B.pfkv_stage_copy(back, dev2)        # device to host
+    B.pfkv_stage_copy(dev2, host, 0)     # nothing
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), host) and torch.equal(back, host)
+
+
+def test_staged_inputs_give_the_same_step(B):
+    """A step whose packed inputs are staged from pinned host memory by
+    pfkv_stage_copy, with out and flags in host memory, gives the bytes of the
+    step on device inputs."""
+    spec = W.spec_llama8b("small")
+    db = _db(spec)
+    db.pack_step_io()
+    before = _pool(db)
+    db.step()
+    torch.cuda.synchronize()
+    want_out, want_flags, want_pool = db.out.clone(), db.flags.clone(), _pool(db)
+    _restore(db, before)
+    h_in = db.io_in.detach().cpu().pin_memory()
+    db.io_in.zero_()  # the staged copy must bring every input back
+    out = torch.full(db.out.shape, 7.0, dtype=db.out.dtype).pin_memory()
+    flags = torch.full(db.flags.shape, 0xEE, dtype=db.flags.dtype).pin_memory()
+    B.pfkv_stage_copy(db.io_in, h_in)
+    B.pfkv_decode_step(db.cache, db.pages, db.positions, db.k_new, db.v_new, db.q, spec.sm_scale,
+                       db.split_tokens, db.max_seq_len, db.workspace, out, flags,
+                       append_flags=db.append_flags)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want_out.cpu())
+    assert torch.equal(flags[:spec.B], want_flags.cpu()[:spec.B])
+    for a, b in zip(_pool(db), want_pool):
+        assert torch.equal(a, b)
