@@ -6,13 +6,15 @@
 
 namespace pfkv {
 
-// 12 workers when each SM has more than 8 x 192 units to stream (by the
+// 12 workers when each SM has more than 8 x 64 units to stream (by the
 // host-known bound: every head at max_seq_len); 8 otherwise.  Measured on the
-// GB300: 12 x 2 stages was 6% faster on 128K-512K contexts and 4% faster on a
-// 64 x 32K batch, but 4% slower on a batch of 32 lengths up to 8K, where the
-// per-worker startup and the partial rows weigh more.
+// GB300: 12 workers (2 stages each) beat 8 (3 stages) on long contexts and
+// large sweeps, by 1 us per step on the Llama-shaped layer (B=32, bound 131K
+// units) in back-to-back steps, and by 4 us on the B=8 BF16 sweep; with fewer
+// units per worker (the B=1 sweep: 16K units) the per-worker startup and the
+// partial rows weigh more and 8 workers were 1.5-2 us faster.
 int pers_workers_for(long long units_bound, int num_sms) {
-    return units_bound > (long long)num_sms * 8 * 192 ? 12 : 8;
+    return units_bound > (long long)num_sms * 8 * 64 ? 12 : 8;
 }
 
 bool pers_supported(const DecodePlan &p) {

@@ -85,7 +85,7 @@ def test_llama8b_small_fp8_append(B, split):
 @pytest.mark.parametrize("split", [0, 1024])
 def test_twelve_worker_shape(B, split):
     """A large host-known length bound (4 requests x 8 kv heads x 8,192 units,
-    above 8 x 192 units per SM) selects the split kernel's 12-worker shape,
+    above 8 x 64 units per SM) selects the split kernel's 12-worker shape,
     while the actual lengths stay small enough for the oracle."""
     spec = dataclasses.replace(W.spec_llama8b("small"), split_tokens=split)
     run_and_compare(spec, label=f"llama8b-small 12 workers split={split}", max_seq_len=131072)

@@ -160,10 +160,10 @@ def _run(B, kv_dtype, case, Hq, seed, bound=None, D=128):
 
 @pytest.mark.parametrize("kv_dtype", ["fp8", "bf16"])
 @pytest.mark.parametrize("case", sorted(CASES))
-@pytest.mark.parametrize("bound", [None, 131072])
+@pytest.mark.parametrize("bound", [None, 262144])
 def test_cancelling_large_values(B, kv_dtype, case, bound):
-    """Groups of 4 query heads; the large length bound selects the 12-worker
-    shape of the split kernel."""
+    """Groups of 4 query heads; the large length bound (4 requests x 2 kv heads
+    x 16,384 units) selects the 12-worker shape of the split kernel."""
     _run(B, kv_dtype, case, Hq=8, seed=41, bound=bound)
 
 
